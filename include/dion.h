@@ -1,0 +1,180 @@
+/*
+ * dion.h -- C ABI of libdion.so: the Dion / Orth-Dion optimizer step, batched
+ * over many weight matrices, on one NVIDIA B300 (sm_103a).
+ *
+ * The operation (junaidaliop.github.io "Orth-Dion", update equations and the
+ * symbol glossary under them; Dion's column normalisation from the abstract
+ * of Orth-Dion, thelatestinai.com 2605.16341), applied independently to every
+ * matrix of a plan:
+ *
+ *     M     = G + R                       m x n   (error-feedback buffer)
+ *     U     = orth(M V)                   m x r   (V: warm start, n x r)
+ *     W     = M^T U                       n x r
+ *     Vbar  = orth(W)        Orth-Dion    n x r
+ *           = colnorm(W)     Dion         (each column scaled to unit length)
+ *     X    <- X - eta * s * U Vbar^T      (s = scale; sqrt(m/n) when scale <= 0)
+ *     R    <- beta * (M - U W^T)          (= beta (M - U U^T M))
+ *     V    <- Vbar                        (warm start of the next step)
+ *
+ * orth() is the Q factor of a thin QR whose triangular factor has a positive
+ * diagonal (the pages leave the sign open; this choice makes Q unique).
+ *
+ * Conventions shared by every entry point:
+ *  - All matrices are row-major.  X, R (fp32) and G (fp32 or bf16) are m x n
+ *    with leading dimensions ld_x, ld_g, ld_r in ELEMENTS (>= n).  V is a
+ *    dense n x r fp32 array (leading dimension r).
+ *  - Every data pointer is a DEVICE pointer owned by the caller; the library
+ *    never allocates device memory and never frees caller memory.  Pointers
+ *    must stay valid while a plan that names them is used.
+ *  - X, R, V are updated in place; G is only read.  The writable buffers of
+ *    different matrices must not overlap (checked at plan creation).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Entry points that launch work are asynchronous with respect to
+ *    the host unless stated otherwise.
+ *  - Return values are host-side status codes (dion_status_t).  Numerical
+ *    trouble inside a step never traps or hangs: it sets per-matrix bits in
+ *    device status words, read with dion_plan_get_status().  A matrix whose
+ *    status is not DION_MAT_OK after a step was left unchanged (X, R, V).
+ *  - Thread safety: a plan may be used by one host thread at a time.
+ *    dion_last_error() is per host thread.
+ */
+#ifndef DION_H_
+#define DION_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DION_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define DION_API __attribute__((visibility("default")))
+#else
+#define DION_API
+#endif
+
+typedef enum {
+  DION_OK = 0,
+  DION_ERR_INVALID_ARG = 1,   /* bad pointer, size, rank, dtype, overlap ... */
+  DION_ERR_CUDA = 2,          /* a CUDA runtime call or launch failed        */
+  DION_ERR_WORKSPACE = 3,     /* workspace NULL, too small or misaligned     */
+  DION_ERR_UNSUPPORTED = 4    /* valid request this build does not handle    */
+} dion_status_t;
+
+/* Per-matrix device status bits (OR-ed together). */
+enum {
+  DION_MAT_OK = 0,
+  DION_MAT_CHOL_BREAKDOWN = 1,  /* orth(): non-positive Cholesky pivot (rank-deficient argument) */
+  DION_MAT_NONFINITE = 2        /* orth(): non-finite value met (NaN / Inf in the inputs)        */
+};
+
+typedef enum { DION_VARIANT_DION = 0, DION_VARIANT_ORTH = 1 } dion_variant_t;
+typedef enum { DION_DTYPE_F32 = 0, DION_DTYPE_BF16 = 1 } dion_dtype_t;
+
+/* One weight matrix and its optimizer state (all device pointers, caller-owned).
+ * Requirements: 1 <= r <= min(m, n); ld_* >= n; every pointer 16-byte aligned;
+ * ld_x, ld_r multiples of 4 and ld_g a multiple of 16 bytes / element size. */
+typedef struct {
+  float* X;          /* parameters, m x n fp32, updated in place                 */
+  const void* G;     /* gradient, m x n, fp32 or bf16 (g_dtype), read only        */
+  float* R;          /* error-feedback residual, m x n fp32, updated in place     */
+  float* V;          /* n x r fp32: V_prev on entry, Vbar on exit                 */
+  int64_t m, n, r;
+  int64_t ld_x, ld_g, ld_r;
+  int32_t g_dtype;   /* dion_dtype_t */
+  int32_t variant;   /* dion_variant_t */
+  float eta;         /* learning rate                                             */
+  float beta;        /* error-feedback coefficient                                */
+  float scale;       /* s; <= 0 selects sqrt(m / n)                               */
+  float reserved;    /* must be 0                                                 */
+} dion_matrix_desc;
+
+typedef struct dion_plan dion_plan;
+
+/* Version of this ABI (DION_ABI_VERSION of the built library). */
+DION_API int32_t dion_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+DION_API const char* dion_status_string(dion_status_t s);
+
+/* Detail of the last error returned on the calling host thread ("" if none). */
+DION_API const char* dion_last_error(void);
+
+/*
+ * Validate `count` descriptors and build a plan (host only: no CUDA call).
+ * On success *out receives the plan and *workspace_bytes the size of the
+ * device workspace every launching call needs (caller-allocated, 256-byte
+ * aligned, contents need not be initialised).  The descriptors are copied.
+ * Errors: DION_ERR_INVALID_ARG (bad descriptor or overlapping buffers; see
+ * dion_last_error()), DION_ERR_UNSUPPORTED (alignment / leading dimension).
+ */
+DION_API dion_status_t dion_plan_create(const dion_matrix_desc* descs, int32_t count,
+                               size_t* workspace_bytes, dion_plan** out);
+
+/* Free a plan (host memory only).  NULL is ignored. */
+DION_API void dion_plan_destroy(dion_plan* plan);
+
+/* Number of matrices in the plan, or -1 for NULL. */
+DION_API int32_t dion_plan_count(const dion_plan* plan);
+
+/*
+ * Change eta / beta of matrix `idx` (host only).  Takes effect at the next
+ * launching call, which re-uploads the plan's tables into the workspace.
+ */
+DION_API dion_status_t dion_plan_set_hparams(dion_plan* plan, int32_t idx, float eta, float beta);
+
+/*
+ * Copy the plan's device tables into `workspace` on `stream` (one
+ * cudaMemcpyAsync).  Launching calls do this themselves whenever the
+ * workspace pointer or the hyper-parameters changed; call it explicitly
+ * before capturing dion_step_batched() into a CUDA graph.
+ */
+DION_API dion_status_t dion_plan_upload(dion_plan* plan, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * One full optimizer step for every matrix of the plan, enqueued on
+ * `stream` (phases (a)-(e) below, all asynchronous, no host sync).
+ */
+DION_API dion_status_t dion_step_batched(dion_plan* plan, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Run phases first..last (inclusive) of a step, for tests and profiling:
+ *   0 (a): reset status, P = (G + R) V                    (P in the workspace)
+ *   1 (b): U = orth(P)                                     (U in the workspace)
+ *   2 (c): W = (G + R)^T U                                 (W in the workspace)
+ *   3 (d): Vbar = orth(W) or colnorm(W), written into V
+ *   4 (e): X <- X - eta s U Vbar^T,  R <- beta (G + R - U W^T)
+ * Running 0..4 equals dion_step_batched().
+ */
+DION_API dion_status_t dion_step_phases(dion_plan* plan, void* workspace, size_t ws_bytes,
+                               int32_t first, int32_t last, void* stream);
+
+/* Intermediates of matrix `idx` that tests may read back from the workspace. */
+enum { DION_BUF_P = 0, DION_BUF_U = 1, DION_BUF_W = 2 };
+
+/*
+ * Locate intermediate `which` of matrix `idx`: byte offset from the
+ * workspace base, rows, valid columns (= r) and leading dimension (elements,
+ * fp32).  Host only.
+ */
+DION_API dion_status_t dion_plan_buffer(const dion_plan* plan, int32_t idx, int32_t which,
+                               size_t* byte_offset, int64_t* rows, int64_t* cols, int64_t* ld);
+
+/*
+ * Copy the per-matrix status words of the last step into host array
+ * `per_matrix` (count entries).  Synchronises `stream`.
+ */
+DION_API dion_status_t dion_plan_get_status(dion_plan* plan, const void* workspace, size_t ws_bytes,
+                                   uint32_t* per_matrix, void* stream);
+
+/* Kernel launches enqueued by one dion_step_batched() call of this plan. */
+DION_API int32_t dion_plan_launches_per_step(const dion_plan* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DION_H_ */

@@ -1,0 +1,78 @@
+// Device-side tables shared by every kernel of libdion.
+//
+// The host builds these once per plan (dion_plan_create) and copies them into
+// the caller's workspace (dion_plan_upload); every grouped launch walks them.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace dion {
+
+// Per-matrix status bits (same values as DION_MAT_* in dion.h).
+constexpr unsigned ST_BREAKDOWN = 1u;
+constexpr unsigned ST_NONFINITE = 2u;
+
+// One weight matrix of the batch, with the workspace buffers of its step.
+struct MatDev {
+  float* X;            // m x n, ld ldx
+  const void* G;       // m x n, ld ldg, fp32 or bf16
+  float* R;            // m x n, ld ldr
+  float* V;            // n x r dense: V_prev in, Vbar out
+  long long m, n, r, rp;       // rp = r rounded up to the tile granule
+  long long ldx, ldg, ldr;
+  int g_bf16;          // 1: G is bf16
+  int variant;         // 0 Dion (colnorm), 1 Orth-Dion (QR)
+  float eta_s;         // eta * s
+  float beta;
+  float* P;            // m x rp   P = M V
+  float* U;            // m x rp   U = orth(P)
+  float* W;            // n x rp   W = M^T U
+  float* Wpart;        // ksplit x n x rp partial sums of W (when ksplit > 1)
+  int ksplit;          // split of the m-range in phase (c)
+  int kchunk;          // rows of M per split
+  unsigned* status;    // per-matrix status word
+};
+
+// One orth() problem: A (rows x r, lda) -> out (rows x r, ldo), by CholeskyQR2.
+struct OrthJob {
+  const float* A;      // input, rows x r (ld lda)
+  long long lda;
+  float* Q;            // first-pass factor, rows x rp (ld rp)
+  float* out;          // result, rows x out_cols (ld ldo)
+  long long ldo;
+  long long out_cols;  // columns written to out (rp in the workspace, r into V)
+  float* gpart;        // nchunk x rp x rp Gram partial sums
+  float* S;            // rp x rp Gram / Cholesky factor
+  float* T;            // rp x rp inverse of the Cholesky factor
+  long long rows, r, rp;
+  int nchunk;          // row chunks of the Gram reduction
+  int chunk;           // rows per chunk
+  unsigned* status;
+};
+
+// Largest j in [0, n) with start[j] <= t (start[0] == 0, start[n] == total).
+__device__ __forceinline__ int find_job(const int* __restrict__ start, int n, int t) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (start[mid] <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ float load_g(const MatDev& d, long long i, long long k) {
+  if (d.g_bf16) {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(d.G)[i * d.ldg + k]);
+  }
+  return reinterpret_cast<const float*>(d.G)[i * d.ldg + k];
+}
+
+// M = G + R, element (i, k); zero outside the matrix.
+__device__ __forceinline__ float load_m(const MatDev& d, long long i, long long k) {
+  if (i >= d.m || k >= d.n) return 0.f;
+  return load_g(d, i, k) + d.R[i * d.ldr + k];
+}
+
+}  // namespace dion

@@ -1,0 +1,488 @@
+// Host side of libdion: descriptor validation, workspace layout, device
+// tables, and the grouped launches of each phase of the Dion / Orth-Dion step
+// (junaidaliop.github.io "Orth-Dion", update equations and glossary).
+#include "dion.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "simt.cuh"
+
+using namespace dion;
+
+namespace {
+
+thread_local std::string g_err;
+
+dion_status_t fail(dion_status_t s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+dion_status_t ok() {
+  g_err.clear();
+  return DION_OK;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+// rank padding granule: the tensor-core tiles take N in multiples of 16
+constexpr long long kRankGranule = 16;
+
+}  // namespace
+
+struct dion_plan {
+  std::vector<dion_matrix_desc> descs;
+  int count = 0;
+  std::vector<long long> rp;
+  std::vector<int> ksplit, kchunk;
+  std::vector<int> nchunk_p, chunk_p, nchunk_w, chunk_w;
+  std::vector<int> orth_idx, dion_idx;   // matrices by right-factor variant
+
+  // workspace layout (byte offsets from the workspace base)
+  size_t ws_bytes = 0;
+  size_t off_tables = 0, tables_bytes = 0, off_status = 0;
+  std::vector<size_t> off_P, off_Q, off_U, off_W, off_Wpart, off_gpart, off_S, off_T;
+
+  // table image layout (byte offsets inside the tables region)
+  size_t t_mats = 0, t_jobs_p = 0, t_jobs_w = 0;
+  size_t t_ts_mv = 0, t_ts_gram_p = 0, t_ts_trmm_p = 0, t_ts_mtu = 0, t_ts_wred = 0,
+         t_ts_epi = 0, t_ts_gram_w = 0, t_ts_trmm_w = 0, t_ts_coln = 0, t_coln_idx = 0;
+  std::vector<int> ts_mv, ts_gram_p, ts_trmm_p, ts_mtu, ts_wred, ts_epi, ts_gram_w, ts_trmm_w, ts_coln;
+  bool any_split = false;
+
+  std::vector<unsigned char> image;
+  const void* uploaded_ws = nullptr;
+  bool dirty = true;
+};
+
+namespace {
+
+dion_status_t validate(const dion_matrix_desc* d, int count) {
+  struct Range { uintptr_t lo, hi; bool writable; int idx; };
+  std::vector<Range> ranges;
+  ranges.reserve((size_t)count * 4);
+  for (int i = 0; i < count; ++i) {
+    const dion_matrix_desc& x = d[i];
+    if (!x.X || !x.G || !x.R || !x.V)
+      return fail(DION_ERR_INVALID_ARG, "matrix %d: NULL pointer", i);
+    if (x.m < 1 || x.n < 1 || x.m > (1LL << 31) || x.n > (1LL << 31))
+      return fail(DION_ERR_INVALID_ARG, "matrix %d: bad shape %lld x %lld", i, (long long)x.m, (long long)x.n);
+    if (x.r < 1 || x.r > std::min(x.m, x.n))
+      return fail(DION_ERR_INVALID_ARG, "matrix %d: rank %lld outside [1, min(m, n) = %lld]", i,
+                  (long long)x.r, (long long)std::min(x.m, x.n));
+    if (x.ld_x < x.n || x.ld_g < x.n || x.ld_r < x.n)
+      return fail(DION_ERR_INVALID_ARG, "matrix %d: leading dimension below n", i);
+    if (x.g_dtype != DION_DTYPE_F32 && x.g_dtype != DION_DTYPE_BF16)
+      return fail(DION_ERR_INVALID_ARG, "matrix %d: unknown g_dtype %d", i, x.g_dtype);
+    if (x.variant != DION_VARIANT_DION && x.variant != DION_VARIANT_ORTH)
+      return fail(DION_ERR_INVALID_ARG, "matrix %d: unknown variant %d", i, x.variant);
+    if (!std::isfinite(x.eta) || !std::isfinite(x.beta) || !std::isfinite(x.scale))
+      return fail(DION_ERR_INVALID_ARG, "matrix %d: non-finite eta / beta / scale", i);
+    if (x.reserved != 0.f)
+      return fail(DION_ERR_INVALID_ARG, "matrix %d: reserved field must be 0", i);
+    const size_t gsz = x.g_dtype == DION_DTYPE_BF16 ? 2 : 4;
+    if (((uintptr_t)x.X | (uintptr_t)x.G | (uintptr_t)x.R | (uintptr_t)x.V) & 15)
+      return fail(DION_ERR_UNSUPPORTED, "matrix %d: pointers must be 16-byte aligned", i);
+    if ((x.ld_x * 4) % 16 || (x.ld_r * 4) % 16 || (x.ld_g * (long long)gsz) % 16)
+      return fail(DION_ERR_UNSUPPORTED, "matrix %d: row pitch of X, G, R must be a multiple of 16 bytes", i);
+    auto span = [](const void* p, long long rows, long long cols, long long ld, size_t es) {
+      const uintptr_t lo = (uintptr_t)p;
+      return Range{lo, lo + (uintptr_t)(((rows - 1) * ld + cols) * (long long)es), false, 0};
+    };
+    Range rx = span(x.X, x.m, x.n, x.ld_x, 4); rx.writable = true; rx.idx = i;
+    Range rr = span(x.R, x.m, x.n, x.ld_r, 4); rr.writable = true; rr.idx = i;
+    Range rv = span(x.V, x.n, x.r, x.r, 4); rv.writable = true; rv.idx = i;
+    Range rg = span(x.G, x.m, x.n, x.ld_g, gsz); rg.writable = false; rg.idx = i;
+    ranges.push_back(rx); ranges.push_back(rr); ranges.push_back(rv); ranges.push_back(rg);
+  }
+  std::sort(ranges.begin(), ranges.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
+  uintptr_t end_any = 0, end_w = 0;
+  for (const Range& g : ranges) {
+    if (g.writable ? g.lo < end_any : g.lo < end_w)
+      return fail(DION_ERR_INVALID_ARG, "matrix %d: buffer overlaps another matrix's buffer", g.idx);
+    end_any = std::max(end_any, g.hi);
+    if (g.writable) end_w = std::max(end_w, g.hi);
+  }
+  return DION_OK;
+}
+
+template <class T>
+void put(std::vector<unsigned char>& img, size_t off, const T* src, size_t n) {
+  std::memcpy(img.data() + off, src, n * sizeof(T));
+}
+
+void layout(dion_plan* p) {
+  const int cnt = p->count;
+  p->rp.resize(cnt); p->ksplit.resize(cnt); p->kchunk.resize(cnt);
+  p->nchunk_p.resize(cnt); p->chunk_p.resize(cnt); p->nchunk_w.resize(cnt); p->chunk_w.resize(cnt);
+  for (int i = 0; i < cnt; ++i) {
+    const auto& d = p->descs[i];
+    p->rp[i] = cdiv(d.r, kRankGranule) * kRankGranule;
+    (d.variant == DION_VARIANT_ORTH ? p->orth_idx : p->dion_idx).push_back(i);
+  }
+  // split of the row range in phase (c) so that a lone matrix still fills the GPU
+  long long tiles_c = 0;
+  for (int i = 0; i < cnt; ++i)
+    tiles_c += cdiv(p->descs[i].n, simt::TM) * cdiv(p->rp[i], simt::TN);
+  const long long want = 4LL * 148;
+  const long long split = tiles_c >= want ? 1 : cdiv(want, tiles_c);
+  for (int i = 0; i < cnt; ++i) {
+    const long long m = p->descs[i].m;
+    long long s = std::min<long long>(split, std::max<long long>(1, m / 256));
+    long long ch = cdiv(cdiv(m, s), 16) * 16;
+    p->kchunk[i] = (int)ch;
+    p->ksplit[i] = (int)cdiv(m, ch);
+    if (p->ksplit[i] > 1) p->any_split = true;
+  }
+  auto chunks = [](long long rows, int* nch, int* ch) {
+    long long n = std::min<long long>(32, std::max<long long>(1, cdiv(rows, 512)));
+    long long c = cdiv(cdiv(rows, n), 64) * 64;
+    *ch = (int)c;
+    *nch = (int)cdiv(rows, c);
+  };
+  for (int i = 0; i < cnt; ++i) {
+    chunks(p->descs[i].m, &p->nchunk_p[i], &p->chunk_p[i]);
+    chunks(p->descs[i].n, &p->nchunk_w[i], &p->chunk_w[i]);
+  }
+
+  // ---- tile prefix sums
+  auto prefix = [&](std::vector<int>& ts, const std::vector<int>& ids, auto tiles_of) {
+    ts.assign(ids.size() + 1, 0);
+    for (size_t k = 0; k < ids.size(); ++k) ts[k + 1] = ts[k] + (int)tiles_of(ids[k]);
+  };
+  std::vector<int> all(cnt);
+  for (int i = 0; i < cnt; ++i) all[i] = i;
+  auto D = [&](int i) -> const dion_matrix_desc& { return p->descs[i]; };
+  prefix(p->ts_mv, all, [&](int i) { return cdiv(D(i).m, simt::TM) * cdiv(p->rp[i], simt::TN); });
+  prefix(p->ts_gram_p, all, [&](int i) { long long t = cdiv(p->rp[i], simt::TN); return p->nchunk_p[i] * t * t; });
+  prefix(p->ts_trmm_p, all, [&](int i) { return cdiv(D(i).m, simt::TM) * cdiv(p->rp[i], simt::TN); });
+  prefix(p->ts_mtu, all, [&](int i) {
+    return (long long)p->ksplit[i] * cdiv(D(i).n, simt::TM) * cdiv(p->rp[i], simt::TN); });
+  prefix(p->ts_wred, all, [&](int i) { return p->ksplit[i] > 1 ? cdiv(D(i).n * p->rp[i], 1024) : 1; });
+  prefix(p->ts_epi, all, [&](int i) { return cdiv(D(i).m, simt::TM) * cdiv(D(i).n, simt::TN); });
+  prefix(p->ts_gram_w, p->orth_idx, [&](int i) { long long t = cdiv(p->rp[i], simt::TN); return p->nchunk_w[i] * t * t; });
+  prefix(p->ts_trmm_w, p->orth_idx, [&](int i) { return cdiv(D(i).n, simt::TM) * cdiv(p->rp[i], simt::TN); });
+  prefix(p->ts_coln, p->dion_idx, [&](int i) { return cdiv(D(i).r, 32); });
+
+  // ---- tables region
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 16); return o; };
+  p->t_mats = take(sizeof(MatDev) * cnt);
+  p->t_jobs_p = take(sizeof(OrthJob) * cnt);
+  p->t_jobs_w = take(sizeof(OrthJob) * std::max<size_t>(1, p->orth_idx.size()));
+  p->t_ts_mv = take(4 * p->ts_mv.size());
+  p->t_ts_gram_p = take(4 * p->ts_gram_p.size());
+  p->t_ts_trmm_p = take(4 * p->ts_trmm_p.size());
+  p->t_ts_mtu = take(4 * p->ts_mtu.size());
+  p->t_ts_wred = take(4 * p->ts_wred.size());
+  p->t_ts_epi = take(4 * p->ts_epi.size());
+  p->t_ts_gram_w = take(4 * p->ts_gram_w.size());
+  p->t_ts_trmm_w = take(4 * p->ts_trmm_w.size());
+  p->t_ts_coln = take(4 * p->ts_coln.size());
+  p->t_coln_idx = take(4 * std::max<size_t>(1, p->dion_idx.size()));
+  p->tables_bytes = off;
+
+  // ---- workspace regions
+  size_t ws = 0;
+  auto region = [&](size_t bytes) { size_t o = ws; ws = align_up(ws + std::max<size_t>(bytes, 4), kAlign); return o; };
+  p->off_tables = region(p->tables_bytes);
+  p->off_status = region(4 * (size_t)cnt);
+  p->off_P.resize(cnt); p->off_Q.resize(cnt); p->off_U.resize(cnt); p->off_W.resize(cnt);
+  p->off_Wpart.resize(cnt); p->off_gpart.resize(cnt); p->off_S.resize(cnt); p->off_T.resize(cnt);
+  for (int i = 0; i < cnt; ++i) {
+    const long long m = D(i).m, n = D(i).n, rp = p->rp[i];
+    p->off_P[i] = region(4 * (size_t)(m * rp));
+    p->off_Q[i] = region(4 * (size_t)(std::max(m, n) * rp));
+    p->off_U[i] = region(4 * (size_t)(m * rp));
+    p->off_W[i] = region(4 * (size_t)(n * rp));
+    p->off_Wpart[i] = region(p->ksplit[i] > 1 ? 4 * (size_t)p->ksplit[i] * (size_t)(n * rp) : 4);
+    p->off_gpart[i] = region(4 * (size_t)std::max(p->nchunk_p[i], p->nchunk_w[i]) * (size_t)(rp * rp));
+    p->off_S[i] = region(4 * (size_t)(rp * rp));
+    p->off_T[i] = region(4 * (size_t)(rp * rp));
+  }
+  p->ws_bytes = ws;
+}
+
+void build_image(dion_plan* p, unsigned char* base) {
+  const int cnt = p->count;
+  p->image.assign(p->tables_bytes, 0);
+  std::vector<MatDev> mats(cnt);
+  std::vector<OrthJob> jp(cnt), jw(std::max<size_t>(1, p->orth_idx.size()));
+  unsigned* status = reinterpret_cast<unsigned*>(base + p->off_status);
+  for (int i = 0; i < cnt; ++i) {
+    const auto& d = p->descs[i];
+    MatDev& x = mats[i];
+    x.X = d.X; x.G = d.G; x.R = d.R; x.V = d.V;
+    x.m = d.m; x.n = d.n; x.r = d.r; x.rp = p->rp[i];
+    x.ldx = d.ld_x; x.ldg = d.ld_g; x.ldr = d.ld_r;
+    x.g_bf16 = d.g_dtype == DION_DTYPE_BF16;
+    x.variant = d.variant;
+    const float s = d.scale > 0.f ? d.scale : (float)std::sqrt((double)d.m / (double)d.n);
+    x.eta_s = d.eta * s;
+    x.beta = d.beta;
+    x.P = reinterpret_cast<float*>(base + p->off_P[i]);
+    x.U = reinterpret_cast<float*>(base + p->off_U[i]);
+    x.W = reinterpret_cast<float*>(base + p->off_W[i]);
+    x.Wpart = reinterpret_cast<float*>(base + p->off_Wpart[i]);
+    x.ksplit = p->ksplit[i];
+    x.kchunk = p->kchunk[i];
+    x.status = status + i;
+    auto job = [&](OrthJob& o, const float* A, long long rows, float* out, long long ldo,
+                   long long ocols, int nch, int ch) {
+      o.A = A; o.lda = x.rp;
+      o.Q = reinterpret_cast<float*>(base + p->off_Q[i]);
+      o.out = out; o.ldo = ldo; o.out_cols = ocols;
+      o.gpart = reinterpret_cast<float*>(base + p->off_gpart[i]);
+      o.S = reinterpret_cast<float*>(base + p->off_S[i]);
+      o.T = reinterpret_cast<float*>(base + p->off_T[i]);
+      o.rows = rows; o.r = x.r; o.rp = x.rp;
+      o.nchunk = nch; o.chunk = ch;
+      o.status = x.status;
+    };
+    job(jp[i], x.P, x.m, x.U, x.rp, x.rp, p->nchunk_p[i], p->chunk_p[i]);
+  }
+  for (size_t k = 0; k < p->orth_idx.size(); ++k) {
+    const int i = p->orth_idx[k];
+    const MatDev& x = mats[i];
+    OrthJob& o = jw[k];
+    o = jp[i];
+    o.A = x.W; o.lda = x.rp; o.rows = x.n;
+    o.out = x.V; o.ldo = x.r; o.out_cols = x.r;
+    o.nchunk = p->nchunk_w[i]; o.chunk = p->chunk_w[i];
+  }
+  put(p->image, p->t_mats, mats.data(), mats.size());
+  put(p->image, p->t_jobs_p, jp.data(), jp.size());
+  put(p->image, p->t_jobs_w, jw.data(), jw.size());
+  put(p->image, p->t_ts_mv, p->ts_mv.data(), p->ts_mv.size());
+  put(p->image, p->t_ts_gram_p, p->ts_gram_p.data(), p->ts_gram_p.size());
+  put(p->image, p->t_ts_trmm_p, p->ts_trmm_p.data(), p->ts_trmm_p.size());
+  put(p->image, p->t_ts_mtu, p->ts_mtu.data(), p->ts_mtu.size());
+  put(p->image, p->t_ts_wred, p->ts_wred.data(), p->ts_wred.size());
+  put(p->image, p->t_ts_epi, p->ts_epi.data(), p->ts_epi.size());
+  put(p->image, p->t_ts_gram_w, p->ts_gram_w.data(), p->ts_gram_w.size());
+  put(p->image, p->t_ts_trmm_w, p->ts_trmm_w.data(), p->ts_trmm_w.size());
+  put(p->image, p->t_ts_coln, p->ts_coln.data(), p->ts_coln.size());
+  if (!p->dion_idx.empty()) put(p->image, p->t_coln_idx, p->dion_idx.data(), p->dion_idx.size());
+}
+
+dion_status_t check_ws(const dion_plan* p, const void* ws, size_t bytes) {
+  if (!p) return fail(DION_ERR_INVALID_ARG, "NULL plan");
+  if (!ws) return fail(DION_ERR_WORKSPACE, "NULL workspace");
+  if ((uintptr_t)ws % kAlign) return fail(DION_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (bytes < p->ws_bytes)
+    return fail(DION_ERR_WORKSPACE, "workspace of %zu bytes, plan needs %zu", bytes, p->ws_bytes);
+  return DION_OK;
+}
+
+dion_status_t cuda_check(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(DION_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return DION_OK;
+}
+
+template <class T>
+const T* tab(const dion_plan* p, unsigned char* base, size_t off) {
+  return reinterpret_cast<const T*>(base + p->off_tables + off);
+}
+
+// orth() of every job of one list: CholeskyQR2 = two rounds of
+// (Gram partials, reduce + Cholesky + inverse, A T).
+dion_status_t launch_orth(const dion_plan* p, unsigned char* base, cudaStream_t s, size_t t_jobs,
+                          size_t t_ts_gram, size_t t_ts_trmm, const std::vector<int>& ts_gram,
+                          const std::vector<int>& ts_trmm, int njob) {
+  if (njob == 0) return DION_OK;
+  const OrthJob* jobs = tab<OrthJob>(p, base, t_jobs);
+  const int* tg = tab<int>(p, base, t_ts_gram);
+  const int* tt = tab<int>(p, base, t_ts_trmm);
+  for (int pass = 0; pass < 2; ++pass) {
+    simt::k_gram<<<ts_gram[njob], simt::NT, 0, s>>>(jobs, tg, njob, pass);
+    simt::k_chol_inv<<<njob, simt::CHOL_NT, 0, s>>>(jobs);
+    simt::k_trmm<<<ts_trmm[njob], simt::NT, 0, s>>>(jobs, tt, njob, pass);
+  }
+  return cuda_check("orth launch");
+}
+
+dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int first, int last,
+                         void* stream) {
+  dion_status_t st = check_ws(p, workspace, ws_bytes);
+  if (st) return st;
+  if (first < 0 || last > 4 || first > last)
+    return fail(DION_ERR_INVALID_ARG, "phase range %d..%d outside 0..4", first, last);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned char* base = static_cast<unsigned char*>(workspace);
+  if (p->dirty || p->uploaded_ws != workspace) {
+    st = dion_plan_upload(p, workspace, ws_bytes, stream);
+    if (st) return st;
+  }
+  const MatDev* mats = tab<MatDev>(p, base, p->t_mats);
+  const int cnt = p->count;
+  for (int ph = first; ph <= last; ++ph) {
+    switch (ph) {
+      case 0:
+        if (cudaMemsetAsync(base + p->off_status, 0, 4 * (size_t)cnt, s) != cudaSuccess)
+          return cuda_check("status reset");
+        simt::k_mv<<<p->ts_mv[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_mv), cnt);
+        break;
+      case 1:
+        st = launch_orth(p, base, s, p->t_jobs_p, p->t_ts_gram_p, p->t_ts_trmm_p, p->ts_gram_p,
+                         p->ts_trmm_p, cnt);
+        if (st) return st;
+        break;
+      case 2:
+        simt::k_mtu<<<p->ts_mtu[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_mtu), cnt);
+        if (p->any_split)
+          simt::k_wreduce<<<p->ts_wred[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_wred), cnt);
+        break;
+      case 3:
+        st = launch_orth(p, base, s, p->t_jobs_w, p->t_ts_gram_w, p->t_ts_trmm_w, p->ts_gram_w,
+                         p->ts_trmm_w, (int)p->orth_idx.size());
+        if (st) return st;
+        if (!p->dion_idx.empty())
+          simt::k_colnorm<<<p->ts_coln[p->dion_idx.size()], simt::NT, 0, s>>>(
+              mats, tab<int>(p, base, p->t_ts_coln), tab<int>(p, base, p->t_coln_idx),
+              (int)p->dion_idx.size());
+        break;
+      case 4:
+        simt::k_epilogue<<<p->ts_epi[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_epi), cnt);
+        break;
+    }
+    st = cuda_check("phase launch");
+    if (st) return st;
+  }
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dion_abi_version(void) { return DION_ABI_VERSION; }
+
+const char* dion_status_string(dion_status_t s) {
+  switch (s) {
+    case DION_OK: return "DION_OK";
+    case DION_ERR_INVALID_ARG: return "DION_ERR_INVALID_ARG";
+    case DION_ERR_CUDA: return "DION_ERR_CUDA";
+    case DION_ERR_WORKSPACE: return "DION_ERR_WORKSPACE";
+    case DION_ERR_UNSUPPORTED: return "DION_ERR_UNSUPPORTED";
+  }
+  return "DION_ERR_UNKNOWN";
+}
+
+const char* dion_last_error(void) { return g_err.c_str(); }
+
+dion_status_t dion_plan_create(const dion_matrix_desc* descs, int32_t count, size_t* workspace_bytes,
+                               dion_plan** out) {
+  if (!descs || !workspace_bytes || !out) return fail(DION_ERR_INVALID_ARG, "NULL argument");
+  *out = nullptr;
+  if (count < 1 || count > (1 << 20)) return fail(DION_ERR_INVALID_ARG, "count %d outside [1, 2^20]", count);
+  dion_status_t st = validate(descs, count);
+  if (st) return st;
+  dion_plan* p = new dion_plan();
+  p->descs.assign(descs, descs + count);
+  p->count = count;
+  layout(p);
+  // every grouped launch must fit in one grid dimension
+  const long long grids[] = {p->ts_mv[count], p->ts_gram_p[count], p->ts_mtu[count], p->ts_epi[count]};
+  for (long long g : grids)
+    if (g >= (1LL << 31)) {
+      delete p;
+      return fail(DION_ERR_UNSUPPORTED, "batch too large for one grouped launch");
+    }
+  *workspace_bytes = p->ws_bytes;
+  *out = p;
+  return ok();
+}
+
+void dion_plan_destroy(dion_plan* plan) { delete plan; }
+
+int32_t dion_plan_count(const dion_plan* plan) { return plan ? plan->count : -1; }
+
+dion_status_t dion_plan_set_hparams(dion_plan* plan, int32_t idx, float eta, float beta) {
+  if (!plan) return fail(DION_ERR_INVALID_ARG, "NULL plan");
+  if (idx < 0 || idx >= plan->count) return fail(DION_ERR_INVALID_ARG, "index %d outside the plan", idx);
+  if (!std::isfinite(eta) || !std::isfinite(beta)) return fail(DION_ERR_INVALID_ARG, "non-finite eta / beta");
+  plan->descs[idx].eta = eta;
+  plan->descs[idx].beta = beta;
+  plan->dirty = true;
+  return ok();
+}
+
+dion_status_t dion_plan_upload(dion_plan* plan, void* workspace, size_t ws_bytes, void* stream) {
+  dion_status_t st = check_ws(plan, workspace, ws_bytes);
+  if (st) return st;
+  unsigned char* base = static_cast<unsigned char*>(workspace);
+  build_image(plan, base);
+  if (cudaMemcpyAsync(base + plan->off_tables, plan->image.data(), plan->image.size(),
+                      cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_check("table upload");
+  plan->uploaded_ws = workspace;
+  plan->dirty = false;
+  return ok();
+}
+
+dion_status_t dion_step_batched(dion_plan* plan, void* workspace, size_t ws_bytes, void* stream) {
+  return run_phases(plan, workspace, ws_bytes, 0, 4, stream);
+}
+
+dion_status_t dion_step_phases(dion_plan* plan, void* workspace, size_t ws_bytes, int32_t first,
+                               int32_t last, void* stream) {
+  return run_phases(plan, workspace, ws_bytes, first, last, stream);
+}
+
+dion_status_t dion_plan_buffer(const dion_plan* plan, int32_t idx, int32_t which, size_t* byte_offset,
+                               int64_t* rows, int64_t* cols, int64_t* ld) {
+  if (!plan || !byte_offset || !rows || !cols || !ld) return fail(DION_ERR_INVALID_ARG, "NULL argument");
+  if (idx < 0 || idx >= plan->count) return fail(DION_ERR_INVALID_ARG, "index %d outside the plan", idx);
+  const auto& d = plan->descs[idx];
+  *cols = d.r;
+  *ld = plan->rp[idx];
+  switch (which) {
+    case DION_BUF_P: *byte_offset = plan->off_P[idx]; *rows = d.m; break;
+    case DION_BUF_U: *byte_offset = plan->off_U[idx]; *rows = d.m; break;
+    case DION_BUF_W: *byte_offset = plan->off_W[idx]; *rows = d.n; break;
+    default: return fail(DION_ERR_INVALID_ARG, "unknown buffer %d", which);
+  }
+  return ok();
+}
+
+dion_status_t dion_plan_get_status(dion_plan* plan, const void* workspace, size_t ws_bytes,
+                                   uint32_t* per_matrix, void* stream) {
+  dion_status_t st = check_ws(plan, workspace, ws_bytes);
+  if (st) return st;
+  if (!per_matrix) return fail(DION_ERR_INVALID_ARG, "NULL output");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const unsigned char* base = static_cast<const unsigned char*>(workspace);
+  if (cudaMemcpyAsync(per_matrix, base + plan->off_status, 4 * (size_t)plan->count,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return cuda_check("status copy");
+  if (cudaStreamSynchronize(s) != cudaSuccess) return cuda_check("status sync");
+  return ok();
+}
+
+int32_t dion_plan_launches_per_step(const dion_plan* plan) {
+  if (!plan) return -1;
+  int n = 1;                                   // phase (a)
+  n += 6;                                      // phase (b): two CholeskyQR rounds
+  n += 1 + (plan->any_split ? 1 : 0);          // phase (c)
+  n += plan->orth_idx.empty() ? 0 : 6;         // phase (d), Orth-Dion matrices
+  n += plan->dion_idx.empty() ? 0 : 1;         // phase (d), Dion matrices
+  n += 1;                                      // phase (e)
+  return n;
+}
+
+}  // extern "C"

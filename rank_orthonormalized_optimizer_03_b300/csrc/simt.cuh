@@ -1,0 +1,403 @@
+// CUDA-core (FFMA) kernels of the step: every phase as a grouped launch over
+// all matrices (or orth jobs) of a plan.  fp32 storage, fp32 accumulation in a
+// fixed order, so results are bitwise reproducible run to run.
+//
+// Phase map (junaidaliop.github.io "Orth-Dion", update equations):
+//   k_mv        P = (G + R) V                          equations 1-2 (argument of orth)
+//   k_gram      partial Grams A^T A of a row chunk     orth(), CholeskyQR2 Gram
+//   k_chol_inv  Gram reduce, Cholesky, inverse         orth(), positive diagonal
+//   k_trmm      Q = A T  (T upper triangular)          orth(), triangular solve
+//   k_mtu       W = (G + R)^T U  (split over rows)     equation 3
+//   k_wreduce   W = sum of the split partials          equation 3
+//   k_colnorm   Vbar = W diag(1/||w_j||)               Dion right factor
+//   k_epilogue  X -= eta s U Vbar^T; R = beta (M - U W^T)   equations 5-6
+#pragma once
+
+#include "common.cuh"
+
+namespace dion {
+namespace simt {
+
+constexpr int TM = 64, TN = 64, TK = 16, NT = 256;
+constexpr int LDS = TM + 4;  // padded shared row
+
+// acc[u][v] += sum_{k in [kb, ke)} A(i0 + ty*4 + u, k) * B(k, j0 + tx*4 + v)
+// A_KC: consecutive threads walk k when loading A (A is k-contiguous in memory);
+// B_JC: consecutive threads walk j when loading B.
+template <bool A_KC, bool B_JC, class LA, class LB>
+__device__ __forceinline__ void tile_acc(const LA& la, const LB& lb, long long i0, long long j0,
+                                         long long kb, long long ke, float (&acc)[4][4],
+                                         float* As, float* Bs) {
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  for (long long k0 = kb; k0 < ke; k0 += TK) {
+#pragma unroll
+    for (int e = 0; e < (TM * TK) / NT; ++e) {
+      const int idx = tid + e * NT;
+      const int ii = A_KC ? idx / TK : idx % TM;
+      const int kk = A_KC ? idx % TK : idx / TM;
+      const long long k = k0 + kk;
+      As[kk * LDS + ii] = (k < ke) ? la(i0 + ii, k) : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < (TN * TK) / NT; ++e) {
+      const int idx = tid + e * NT;
+      const int jj = B_JC ? idx % TN : idx / TK;
+      const int kk = B_JC ? idx / TN : idx % TK;
+      const long long k = k0 + kk;
+      Bs[kk * LDS + jj] = (k < ke) ? lb(k, j0 + jj) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < TK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = As[kk * LDS + ty * 4 + u];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) b[v] = Bs[kk * LDS + tx * 4 + v];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(a[u], b[v], acc[u][v]);
+    }
+    __syncthreads();
+  }
+}
+
+// Row-major fp32 loader with bounds: element (i, k) of a rows x cols array.
+struct LoadRM {
+  const float* p; long long ld, rows, cols;
+  __device__ float operator()(long long i, long long k) const {
+    return (i < rows && k < cols) ? p[i * ld + k] : 0.f;
+  }
+};
+// Transposed view: element (i, k) = p[k][i].
+struct LoadRMT {
+  const float* p; long long ld, rows, cols;  // rows/cols of the stored array
+  __device__ float operator()(long long i, long long k) const {
+    return (k < rows && i < cols) ? p[k * ld + i] : 0.f;
+  }
+};
+struct LoadM {
+  const MatDev* d;
+  __device__ float operator()(long long i, long long k) const { return load_m(*d, i, k); }
+};
+// M^T: element (j, i) = M[i][j]
+struct LoadMT {
+  const MatDev* d;
+  __device__ float operator()(long long j, long long i) const { return load_m(*d, i, j); }
+};
+
+__device__ __forceinline__ void zero(float (&acc)[4][4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
+}
+
+// ---------------------------------------------------------------- phase (a)
+__global__ void __launch_bounds__(NT) k_mv(const MatDev* __restrict__ mats,
+                                           const int* __restrict__ tstart, int nmat) {
+  __shared__ float As[TK * LDS], Bs[TK * LDS];
+  const int j = find_job(tstart, nmat, blockIdx.x);
+  const MatDev& d = mats[j];
+  const int local = blockIdx.x - tstart[j];
+  const int ntc = (int)((d.rp + TN - 1) / TN);
+  const long long i0 = (long long)(local / ntc) * TM, c0 = (long long)(local % ntc) * TN;
+  float acc[4][4];
+  zero(acc);
+  LoadM la{&d};
+  LoadRM lb{d.V, d.r, d.n, d.r};
+  tile_acc<true, true>(la, lb, i0, c0, 0, d.n, acc, As, Bs);
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const long long i = i0 + ty * 4 + u;
+    if (i >= d.m) continue;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const long long c = c0 + tx * 4 + v;
+      if (c < d.rp) d.P[i * d.rp + c] = acc[u][v];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- orth()
+// Partial Gram of one row chunk: gpart[chunk][a][b] = sum_i A[i][a] A[i][b].
+// pass 0 reads the job's input A, pass 1 its first-pass factor Q.
+__global__ void __launch_bounds__(NT) k_gram(const OrthJob* __restrict__ jobs,
+                                             const int* __restrict__ tstart, int njob, int pass) {
+  __shared__ float As[TK * LDS], Bs[TK * LDS];
+  const int j = find_job(tstart, njob, blockIdx.x);
+  const OrthJob& o = jobs[j];
+  if (pass == 1 && *o.status) return;
+  const int local = blockIdx.x - tstart[j];
+  const int nt = (int)((o.rp + TN - 1) / TN);
+  const int chunk = local / (nt * nt), rem = local % (nt * nt);
+  const long long a0 = (long long)(rem / nt) * TM, b0 = (long long)(rem % nt) * TN;
+  const float* A = pass == 0 ? o.A : o.Q;
+  const long long lda = pass == 0 ? o.lda : o.rp;
+  const long long ib = (long long)chunk * o.chunk;
+  const long long ie = ib + o.chunk < o.rows ? ib + o.chunk : o.rows;
+  float acc[4][4];
+  zero(acc);
+  LoadRMT la{A, lda, o.rows, o.r};   // (a, i) = A[i][a]
+  LoadRM lb{A, lda, o.rows, o.r};    // (i, b) = A[i][b]
+  tile_acc<false, true>(la, lb, a0, b0, ib, ie, acc, As, Bs);
+  float* out = o.gpart + (long long)chunk * o.rp * o.rp;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const long long a = a0 + ty * 4 + u;
+    if (a >= o.rp) continue;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const long long b = b0 + tx * 4 + v;
+      if (b < o.rp) out[a * o.rp + b] = acc[u][v];
+    }
+  }
+}
+
+// One CTA per job: S = sum of the Gram partials (fixed order); upper Cholesky
+// S = Rc^T Rc with a positive diagonal (stored in the upper triangle of S);
+// T = Rc^{-1} (upper triangular, zero elsewhere, padded to rp x rp).
+// A non-positive or non-finite pivot sets the status bits and stops the job.
+constexpr int CHOL_NT = 512;
+__global__ void __launch_bounds__(CHOL_NT) k_chol_inv(const OrthJob* __restrict__ jobs) {
+  const OrthJob& o = jobs[blockIdx.x];
+  __shared__ int s_bad;
+  __shared__ float s_piv;
+  if (*o.status) return;
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const long long r = o.r, rp = o.rp;
+  float* S = o.S;
+  float* T = o.T;
+  for (long long e = tid; e < r * r; e += nth) {
+    const long long a = e / r, b = e % r;
+    float s = 0.f;
+    for (int c = 0; c < o.nchunk; ++c) s += o.gpart[(long long)c * rp * rp + a * rp + b];
+    S[a * rp + b] = s;
+  }
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  for (long long jj = 0; jj < r; ++jj) {
+    if (tid == 0) {
+      const float dd = S[jj * rp + jj];
+      if (!isfinite(dd)) s_bad = (int)(ST_BREAKDOWN | ST_NONFINITE);
+      else if (!(dd > 0.f)) s_bad = (int)ST_BREAKDOWN;
+      else { s_piv = sqrtf(dd); S[jj * rp + jj] = s_piv; }
+    }
+    __syncthreads();
+    if (s_bad) break;
+    const float inv = 1.f / s_piv;
+    for (long long c = jj + 1 + tid; c < r; c += nth) S[jj * rp + c] *= inv;
+    __syncthreads();
+    {
+      const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
+      for (long long a = jj + 1 + warp; a < r; a += nwarp) {
+        const float sa = S[jj * rp + a];
+        for (long long c = a + lane; c < r; c += 32) S[a * rp + c] -= sa * S[jj * rp + c];
+      }
+    }
+    __syncthreads();
+  }
+  if (s_bad) {
+    if (tid == 0) atomicOr(o.status, (unsigned)s_bad);
+    return;
+  }
+  // T = Rc^{-1}: row a from the bottom up, T[a][c] = -(sum_{k=a+1..c} Rc[a][k] T[k][c]) / Rc[a][a]
+  for (long long e = tid; e < rp * rp; e += nth) T[e] = 0.f;
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
+  for (long long a = r - 1; a >= 0; --a) {
+    const float raa = S[a * rp + a];
+    for (long long c = a + warp; c < r; c += nwarp) {
+      float s = 0.f;
+      for (long long k = a + 1 + lane; k <= c; k += 32) s = fmaf(S[a * rp + k], T[k * rp + c], s);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (lane == 0) T[a * rp + c] = (c == a) ? 1.f / raa : -s / raa;
+    }
+    __syncthreads();
+  }
+}
+
+// out = A T with T upper triangular (rp x rp): pass 0 writes Q = A T1, pass 1
+// writes the job's result = Q T2.
+__global__ void __launch_bounds__(NT) k_trmm(const OrthJob* __restrict__ jobs,
+                                             const int* __restrict__ tstart, int njob, int pass) {
+  __shared__ float As[TK * LDS], Bs[TK * LDS];
+  const int j = find_job(tstart, njob, blockIdx.x);
+  const OrthJob& o = jobs[j];
+  if (*o.status) return;
+  const int local = blockIdx.x - tstart[j];
+  const int ntc = (int)((o.rp + TN - 1) / TN);
+  const long long i0 = (long long)(local / ntc) * TM, c0 = (long long)(local % ntc) * TN;
+  const float* A = pass == 0 ? o.A : o.Q;
+  const long long lda = pass == 0 ? o.lda : o.rp;
+  float acc[4][4];
+  zero(acc);
+  LoadRM la{A, lda, o.rows, o.r};
+  LoadRM lb{o.T, o.rp, o.rp, o.rp};
+  const long long ke = (c0 + TN < o.r) ? c0 + TN : o.r;
+  tile_acc<true, true>(la, lb, i0, c0, 0, ke, acc, As, Bs);
+  float* out = pass == 0 ? o.Q : o.out;
+  const long long ldo = pass == 0 ? o.rp : o.ldo;
+  const long long ncol = pass == 0 ? o.rp : o.out_cols;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const long long i = i0 + ty * 4 + u;
+    if (i >= o.rows) continue;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const long long c = c0 + tx * 4 + v;
+      if (c < ncol) out[i * ldo + c] = acc[u][v];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- phase (c)
+__global__ void __launch_bounds__(NT) k_mtu(const MatDev* __restrict__ mats,
+                                            const int* __restrict__ tstart, int nmat) {
+  __shared__ float As[TK * LDS], Bs[TK * LDS];
+  const int j = find_job(tstart, nmat, blockIdx.x);
+  const MatDev& d = mats[j];
+  if (*d.status) return;
+  const int local = blockIdx.x - tstart[j];
+  const int ntc = (int)((d.rp + TN - 1) / TN);
+  const int ntn = (int)((d.n + TM - 1) / TM);
+  const int split = local / (ntn * ntc), rem = local % (ntn * ntc);
+  const long long j0 = (long long)(rem / ntc) * TM, c0 = (long long)(rem % ntc) * TN;
+  const long long ib = (long long)split * d.kchunk;
+  const long long ie = ib + d.kchunk < d.m ? ib + d.kchunk : d.m;
+  float acc[4][4];
+  zero(acc);
+  LoadMT la{&d};
+  LoadRM lb{d.U, d.rp, d.m, d.rp};
+  tile_acc<false, true>(la, lb, j0, c0, ib, ie, acc, As, Bs);
+  float* out = d.ksplit > 1 ? d.Wpart + (long long)split * d.n * d.rp : d.W;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const long long jr = j0 + ty * 4 + u;
+    if (jr >= d.n) continue;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const long long c = c0 + tx * 4 + v;
+      if (c < d.rp) out[jr * d.rp + c] = acc[u][v];
+    }
+  }
+}
+
+// W = sum over splits (fixed order); one CTA covers 1024 elements.
+__global__ void __launch_bounds__(NT) k_wreduce(const MatDev* __restrict__ mats,
+                                                const int* __restrict__ tstart, int nmat) {
+  const int j = find_job(tstart, nmat, blockIdx.x);
+  const MatDev& d = mats[j];
+  if (*d.status || d.ksplit <= 1) return;
+  const long long base = (long long)(blockIdx.x - tstart[j]) * 1024;
+  const long long tot = d.n * d.rp;
+  for (int e = threadIdx.x; e < 1024; e += NT) {
+    const long long idx = base + e;
+    if (idx >= tot) break;
+    float s = 0.f;
+    for (int sp = 0; sp < d.ksplit; ++sp) s += d.Wpart[(long long)sp * tot + idx];
+    d.W[idx] = s;
+  }
+}
+
+// ---------------------------------------------------------------- phase (d), Dion
+// Vbar[:, c] = W[:, c] / ||W[:, c]||, 32 columns per CTA; a zero column stays zero.
+__global__ void __launch_bounds__(NT) k_colnorm(const MatDev* __restrict__ mats,
+                                                const int* __restrict__ tstart,
+                                                const int* __restrict__ idx, int nidx) {
+  __shared__ float part[NT / 32][33];
+  __shared__ float scale[32];
+  const int jj = find_job(tstart, nidx, blockIdx.x);
+  const MatDev& d = mats[idx[jj]];
+  if (*d.status) return;
+  const long long c = (long long)(blockIdx.x - tstart[jj]) * 32 + (threadIdx.x & 31);
+  const int w = threadIdx.x >> 5;
+  float s = 0.f;
+  if (c < d.r)
+    for (long long row = w; row < d.n; row += NT / 32) {
+      const float x = d.W[row * d.rp + c];
+      s = fmaf(x, x, s);
+    }
+  part[w][threadIdx.x & 31] = s;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = 0.f;
+    for (int k = 0; k < NT / 32; ++k) t += part[k][threadIdx.x];
+    scale[threadIdx.x] = t > 0.f ? 1.f / sqrtf(t) : 0.f;
+  }
+  __syncthreads();
+  if (c < d.r) {
+    const float sc = scale[threadIdx.x & 31];
+    for (long long row = w; row < d.n; row += NT / 32) d.V[row * d.r + c] = d.W[row * d.rp + c] * sc;
+  }
+}
+
+// ---------------------------------------------------------------- phase (e)
+// Per 64 x 64 tile of the m x n state: T1 = U Vbar^T, T2 = U W^T (K = r),
+// X -= eta s T1, R = beta (G + R - T2).
+__global__ void __launch_bounds__(NT) k_epilogue(const MatDev* __restrict__ mats,
+                                                 const int* __restrict__ tstart, int nmat) {
+  __shared__ float As[TK * LDS], B1[TK * LDS], B2[TK * LDS];
+  const int j = find_job(tstart, nmat, blockIdx.x);
+  const MatDev& d = mats[j];
+  if (*d.status) return;
+  const int local = blockIdx.x - tstart[j];
+  const int ntn = (int)((d.n + TN - 1) / TN);
+  const long long i0 = (long long)(local / ntn) * TM, j0 = (long long)(local % ntn) * TN;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  float t1[4][4], t2[4][4];
+  zero(t1);
+  zero(t2);
+  for (long long k0 = 0; k0 < d.r; k0 += TK) {
+#pragma unroll
+    for (int e = 0; e < (TM * TK) / NT; ++e) {
+      const int idx = tid + e * NT;
+      const int ii = idx / TK, kk = idx % TK;
+      const long long i = i0 + ii, k = k0 + kk;
+      As[kk * LDS + ii] = (i < d.m && k < d.r) ? d.U[i * d.rp + k] : 0.f;
+      const long long jr = j0 + ii;  // B tiles share the (row, k) walk
+      const bool ok = jr < d.n && k < d.r;
+      B1[kk * LDS + ii] = ok ? d.V[jr * d.r + k] : 0.f;
+      B2[kk * LDS + ii] = ok ? d.W[jr * d.rp + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < TK; ++kk) {
+      float a[4], b1[4], b2[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = As[kk * LDS + ty * 4 + u];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) { b1[v] = B1[kk * LDS + tx * 4 + v]; b2[v] = B2[kk * LDS + tx * 4 + v]; }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          t1[u][v] = fmaf(a[u], b1[v], t1[u][v]);
+          t2[u][v] = fmaf(a[u], b2[v], t2[u][v]);
+        }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const long long i = i0 + ty * 4 + u;
+    if (i >= d.m) continue;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const long long jc = j0 + tx * 4 + v;
+      if (jc >= d.n) continue;
+      const float mm = load_g(d, i, jc) + d.R[i * d.ldr + jc];
+      d.X[i * d.ldx + jc] = fmaf(-d.eta_s, t1[u][v], d.X[i * d.ldx + jc]);
+      d.R[i * d.ldr + jc] = d.beta * (mm - t2[u][v]);
+    }
+  }
+}
+
+}  // namespace simt
+}  // namespace dion

@@ -1,0 +1,198 @@
+"""ctypes binding of libdion.so (declared in include/dion.h).
+
+Argument marshalling only: every step of the optimizer runs in the library's
+CUDA kernels.  PyTorch provides device memory (the caller's tensors and the
+workspace) and the current CUDA stream.  There is no fallback: if the shared
+library is missing or cannot be loaded, importing :func:`lib` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import List, Optional, Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libdion.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "dion.h")
+
+DION_OK, DION_ERR_INVALID_ARG, DION_ERR_CUDA, DION_ERR_WORKSPACE, DION_ERR_UNSUPPORTED = range(5)
+DION_MAT_OK, DION_MAT_CHOL_BREAKDOWN, DION_MAT_NONFINITE = 0, 1, 2
+VARIANT = {"dion": 0, "orth": 1}
+DTYPE_F32, DTYPE_BF16 = 0, 1
+BUF_P, BUF_U, BUF_W = 0, 1, 2
+
+
+class MatrixDesc(ctypes.Structure):
+    _fields_ = [
+        ("X", ctypes.c_void_p), ("G", ctypes.c_void_p), ("R", ctypes.c_void_p), ("V", ctypes.c_void_p),
+        ("m", ctypes.c_int64), ("n", ctypes.c_int64), ("r", ctypes.c_int64),
+        ("ld_x", ctypes.c_int64), ("ld_g", ctypes.c_int64), ("ld_r", ctypes.c_int64),
+        ("g_dtype", ctypes.c_int32), ("variant", ctypes.c_int32),
+        ("eta", ctypes.c_float), ("beta", ctypes.c_float), ("scale", ctypes.c_float),
+        ("reserved", ctypes.c_float),
+    ]
+
+
+class DionError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}: {detail}")
+        self.code = code
+
+
+STATUS_NAMES = {0: "DION_OK", 1: "DION_ERR_INVALID_ARG", 2: "DION_ERR_CUDA",
+                3: "DION_ERR_WORKSPACE", 4: "DION_ERR_UNSUPPORTED"}
+
+_lib = None
+
+
+def _declare(L):
+    P, I32, I64, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    sig = {
+        "dion_abi_version": (I32, []),
+        "dion_status_string": (ctypes.c_char_p, [I32]),
+        "dion_last_error": (ctypes.c_char_p, []),
+        "dion_plan_create": (I32, [ctypes.POINTER(MatrixDesc), I32, ctypes.POINTER(SZ), ctypes.POINTER(P)]),
+        "dion_plan_destroy": (None, [P]),
+        "dion_plan_count": (I32, [P]),
+        "dion_plan_set_hparams": (I32, [P, I32, F, F]),
+        "dion_plan_upload": (I32, [P, P, SZ, P]),
+        "dion_step_batched": (I32, [P, P, SZ, P]),
+        "dion_step_phases": (I32, [P, P, SZ, I32, I32, P]),
+        "dion_plan_buffer": (I32, [P, I32, I32, ctypes.POINTER(SZ), ctypes.POINTER(I64),
+                                   ctypes.POINTER(I64), ctypes.POINTER(I64)]),
+        "dion_plan_get_status": (I32, [P, P, SZ, ctypes.POINTER(ctypes.c_uint32), P]),
+        "dion_plan_launches_per_step": (I32, [P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
+def lib():
+    """The loaded libdion.so (raises if it is not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libdion.so is not built ({LIB_PATH}); run "
+                               "python -m rank_orthonormalized_optimizer_03_b300.build")
+        _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def header_functions() -> List[str]:
+    """Names of the functions declared in include/dion.h."""
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"DION_API\s+[\w\s\*]+?\b(dion_\w+)\s*\(", txt)))
+
+
+def check(code: int, where: str):
+    if code != DION_OK:
+        raise DionError(code, where, lib().dion_last_error().decode())
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return int(getattr(stream, "cuda_stream", stream)) or None
+
+
+def make_desc(X, G, R, V, eta, beta, variant="orth", scale=0.0) -> MatrixDesc:
+    """Descriptor for one matrix from torch tensors (row-major, unit column stride)."""
+    import torch
+    m, n = X.shape
+    r = V.shape[1]
+    for t, nm in ((X, "X"), (G, "G"), (R, "R")):
+        if t.dim() != 2 or t.shape != (m, n) or t.stride(1) != 1:
+            raise ValueError(f"{nm} must be an m x n row-major view")
+    if X.dtype != torch.float32 or R.dtype != torch.float32 or V.dtype != torch.float32:
+        raise ValueError("X, R, V must be float32")
+    if G.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("G must be float32 or bfloat16")
+    if V.shape != (n, r) or not V.is_contiguous():
+        raise ValueError("V must be a contiguous n x r tensor")
+    return MatrixDesc(
+        X.data_ptr(), G.data_ptr(), R.data_ptr(), V.data_ptr(), m, n, r,
+        X.stride(0), G.stride(0), R.stride(0),
+        DTYPE_BF16 if G.dtype == torch.bfloat16 else DTYPE_F32, VARIANT[variant],
+        float(eta), float(beta), float(scale), 0.0)
+
+
+class Plan:
+    """A batch of matrices stepped together (one grouped launch per phase).
+
+    ``mats`` is a sequence of dicts with keys X, G, R, V (CUDA tensors owned by
+    the caller and updated in place) and eta, beta, variant ("orth" | "dion"),
+    optional scale (<= 0 or missing: sqrt(m/n)).  The workspace is a torch
+    uint8 tensor allocated here unless one is passed in.
+    """
+
+    def __init__(self, mats: Sequence[dict], workspace=None, device=None):
+        import torch
+        L = lib()
+        self._keep = [(d["X"], d["G"], d["R"], d["V"]) for d in mats]
+        descs = (MatrixDesc * len(mats))(*[
+            make_desc(d["X"], d["G"], d["R"], d["V"], d["eta"], d["beta"], d.get("variant", "orth"),
+                      d.get("scale", 0.0)) for d in mats])
+        self._descs = descs
+        ws = ctypes.c_size_t(0)
+        plan = ctypes.c_void_p()
+        check(L.dion_plan_create(descs, len(mats), ctypes.byref(ws), ctypes.byref(plan)), "dion_plan_create")
+        self._plan = plan
+        self.count = len(mats)
+        self.ws_bytes = ws.value
+        if workspace is None:
+            dev = device if device is not None else mats[0]["X"].device
+            workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        if workspace.numel() < self.ws_bytes:
+            raise ValueError("workspace too small")
+        self.workspace = workspace
+
+    def close(self):
+        if getattr(self, "_plan", None):
+            lib().dion_plan_destroy(self._plan)
+            self._plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def launches_per_step(self) -> int:
+        return lib().dion_plan_launches_per_step(self._plan)
+
+    def upload(self, stream=None):
+        check(lib().dion_plan_upload(self._plan, self.workspace.data_ptr(), self.ws_bytes,
+                                     _stream_ptr(stream)), "dion_plan_upload")
+
+    def step(self, stream=None):
+        check(lib().dion_step_batched(self._plan, self.workspace.data_ptr(), self.ws_bytes,
+                                      _stream_ptr(stream)), "dion_step_batched")
+
+    def phases(self, first: int, last: int, stream=None):
+        check(lib().dion_step_phases(self._plan, self.workspace.data_ptr(), self.ws_bytes, first, last,
+                                     _stream_ptr(stream)), "dion_step_phases")
+
+    def set_hparams(self, idx: int, eta: float, beta: float):
+        check(lib().dion_plan_set_hparams(self._plan, idx, eta, beta), "dion_plan_set_hparams")
+
+    def status(self, stream=None) -> List[int]:
+        out = (ctypes.c_uint32 * self.count)()
+        check(lib().dion_plan_get_status(self._plan, self.workspace.data_ptr(), self.ws_bytes, out,
+                                         _stream_ptr(stream)), "dion_plan_get_status")
+        return list(out)
+
+    def buffer(self, idx: int, which: int):
+        """A float32 view (rows x r) of intermediate P, U or W of matrix idx."""
+        import torch
+        off, rows, cols, ld = ctypes.c_size_t(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        check(lib().dion_plan_buffer(self._plan, idx, which, ctypes.byref(off), ctypes.byref(rows),
+                                     ctypes.byref(cols), ctypes.byref(ld)), "dion_plan_buffer")
+        nbytes = rows.value * ld.value * 4
+        raw = self.workspace[off.value: off.value + nbytes]
+        return raw.view(torch.float32).view(rows.value, ld.value)[:, : cols.value]

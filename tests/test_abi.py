@@ -1,0 +1,132 @@
+"""Host-side checks of the C ABI (no GPU needed: nothing here launches work).
+
+plan creation, validation, workspace layout and status strings are host
+logic; the descriptors carry fake (never dereferenced) device addresses.
+"""
+import ctypes
+
+import pytest
+
+from rank_orthonormalized_optimizer_03_b300 import build, dion
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return dion.lib()
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = dion.header_functions()
+    assert len(names) >= 13
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", dion.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(L, n)
+    assert L.dion_abi_version() == 1
+
+
+BASE = 0x7F0000000000
+SLOT = 1 << 32   # every buffer gets its own 4 GiB slot of fake address space
+
+
+def fake_desc(k, m=64, n=32, r=8, **kw):
+    d = dict(X=BASE + (4 * k) * SLOT, G=BASE + (4 * k + 1) * SLOT, R=BASE + (4 * k + 2) * SLOT,
+             V=BASE + (4 * k + 3) * SLOT, m=m, n=n, r=r, ld_x=n, ld_g=n, ld_r=n, g_dtype=dion.DTYPE_BF16,
+             variant=1, eta=0.01, beta=0.95, scale=0.0, reserved=0.0)
+    d.update(kw)
+    return dion.MatrixDesc(**d)
+
+
+def create(L, descs):
+    arr = (dion.MatrixDesc * len(descs))(*descs)
+    ws = ctypes.c_size_t(0)
+    plan = ctypes.c_void_p()
+    code = L.dion_plan_create(arr, len(descs), ctypes.byref(ws), ctypes.byref(plan))
+    return code, ws.value, plan
+
+
+def test_valid_plan_and_layout(L):
+    descs = [fake_desc(0), fake_desc(1, m=100, n=40, r=40), fake_desc(2, variant=0, r=1)]
+    code, ws, plan = create(L, descs)
+    assert code == dion.DION_OK, L.dion_last_error()
+    assert ws > 0 and L.dion_plan_count(plan) == 3
+    assert L.dion_plan_launches_per_step(plan) >= 10
+    off, rows, cols, ld = ctypes.c_size_t(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    seen = []
+    for i, d in enumerate(descs):
+        for which, nrow in ((dion.BUF_P, d.m), (dion.BUF_U, d.m), (dion.BUF_W, d.n)):
+            assert L.dion_plan_buffer(plan, i, which, ctypes.byref(off), ctypes.byref(rows),
+                                      ctypes.byref(cols), ctypes.byref(ld)) == 0
+            assert rows.value == nrow and cols.value == d.r and ld.value >= d.r and ld.value % 16 == 0
+            assert off.value % 256 == 0 and off.value + rows.value * ld.value * 4 <= ws
+            seen.append((off.value, off.value + rows.value * ld.value * 4))
+    seen.sort()
+    for a, b in zip(seen, seen[1:]):
+        assert a[1] <= b[0], "workspace buffers overlap"
+    assert L.dion_plan_buffer(plan, 3, 0, ctypes.byref(off), ctypes.byref(rows), ctypes.byref(cols),
+                              ctypes.byref(ld)) == dion.DION_ERR_INVALID_ARG
+    assert L.dion_plan_set_hparams(plan, 1, 0.5, 0.5) == 0
+    assert L.dion_plan_set_hparams(plan, 7, 0.5, 0.5) == dion.DION_ERR_INVALID_ARG
+    assert L.dion_plan_set_hparams(plan, 0, float("nan"), 0.5) == dion.DION_ERR_INVALID_ARG
+    L.dion_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("bad, code", [
+    (dict(r=0), dion.DION_ERR_INVALID_ARG),
+    (dict(r=33), dion.DION_ERR_INVALID_ARG),            # r > min(m, n)
+    (dict(m=0), dion.DION_ERR_INVALID_ARG),
+    (dict(ld_x=16), dion.DION_ERR_INVALID_ARG),         # ld < n
+    (dict(g_dtype=7), dion.DION_ERR_INVALID_ARG),
+    (dict(variant=2), dion.DION_ERR_INVALID_ARG),
+    (dict(eta=float("inf")), dion.DION_ERR_INVALID_ARG),
+    (dict(reserved=1.0), dion.DION_ERR_INVALID_ARG),
+    (dict(X=0), dion.DION_ERR_INVALID_ARG),
+    (dict(X=BASE + 4), dion.DION_ERR_UNSUPPORTED),       # misaligned pointer
+    (dict(ld_x=33), dion.DION_ERR_UNSUPPORTED),          # row pitch not 16-byte multiple
+    (dict(ld_g=36), dion.DION_ERR_UNSUPPORTED),          # bf16 pitch 72 bytes
+])
+def test_invalid_descriptors_rejected(L, bad, code):
+    got, _, plan = create(L, [fake_desc(0, **bad)])
+    assert got == code, (bad, L.dion_last_error())
+    assert not plan.value
+    assert L.dion_last_error().decode() != ""
+
+
+def test_overlapping_buffers_rejected(L):
+    a = fake_desc(0)
+    b = fake_desc(1, X=a.R + 128)          # X of matrix 1 inside R of matrix 0
+    assert create(L, [a, b])[0] == dion.DION_ERR_INVALID_ARG
+    c = fake_desc(1, G=a.G)                 # two matrices may share a read-only gradient
+    assert create(L, [a, c])[0] == dion.DION_OK
+    d = fake_desc(1, G=a.V)                 # but a gradient may not alias writable state
+    assert create(L, [a, d])[0] == dion.DION_ERR_INVALID_ARG
+
+
+def test_null_and_count_arguments(L):
+    ws = ctypes.c_size_t(0)
+    plan = ctypes.c_void_p()
+    arr = (dion.MatrixDesc * 1)(fake_desc(0))
+    assert L.dion_plan_create(None, 1, ctypes.byref(ws), ctypes.byref(plan)) == dion.DION_ERR_INVALID_ARG
+    assert L.dion_plan_create(arr, 0, ctypes.byref(ws), ctypes.byref(plan)) == dion.DION_ERR_INVALID_ARG
+    assert L.dion_plan_count(None) == -1
+    L.dion_plan_destroy(None)
+
+
+def test_launching_calls_check_workspace_before_touching_cuda(L):
+    code, ws, plan = create(L, [fake_desc(0)])
+    assert code == 0
+    assert L.dion_step_batched(plan, None, ws, None) == dion.DION_ERR_WORKSPACE
+    assert L.dion_step_batched(plan, 0x10000, ws - 1, None) == dion.DION_ERR_WORKSPACE
+    assert L.dion_step_batched(plan, 0x10010, ws, None) == dion.DION_ERR_WORKSPACE   # misaligned
+    assert L.dion_step_phases(plan, 0x10000, ws, 3, 1, None) == dion.DION_ERR_INVALID_ARG
+    L.dion_plan_destroy(plan)
+
+
+def test_status_strings(L):
+    for code, name in dion.STATUS_NAMES.items():
+        assert L.dion_status_string(code).decode() == name
+    assert L.dion_status_string(99).decode() == "DION_ERR_UNKNOWN"

@@ -1,0 +1,269 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Every case draws seeded inputs (rank_orthonormalized_optimizer_03_b300.synth),
+hands the same stored fp32 / bf16 values to both sides and compares
+element-wise (relative Frobenius norms) with the tolerances of parity_util.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import dion_oracle as O
+from parity_util import (TOL_CHAIN, TOL_ORTH, TOL_STEP, check_step, f64, grad_f64, grad_to_device,
+                         orth_v0, padded, rel, state_snapshot)
+from rank_orthonormalized_optimizer_03_b300 import build, dion, synth, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    dion.lib()
+    return torch.device("cuda:0")
+
+
+def to_dev(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+
+
+def host_matrix(hi, dev, variant):
+    import torch
+    s = hi.spec
+    return dict(X=to_dev(hi.X0, dev), G=grad_to_device(hi.grads[0], dev),
+                R=torch.zeros((s.m, s.n), dtype=torch.float32, device=dev),
+                V=to_dev(orth_v0(hi.V0_raw), dev), eta=s.eta, beta=s.beta, variant=variant,
+                scale=s.scale)
+
+
+# ---------------------------------------------------------------- single matrices, chains
+@pytest.mark.parametrize("variant", ["orth", "dion"])
+@pytest.mark.parametrize("wname", ["single_256x128_r16", "square_1024_r256"])
+def test_chain_single_matrix(dev, wname, variant):
+    import torch
+    wl = workloads.by_name(wname)
+    hi = synth.host_inputs(wl, seed=0)
+    s = hi.spec
+    d = host_matrix(hi, dev, variant)
+    plan = dion.Plan([d])
+    # the oracle's own float64 trajectory from the same initial state
+    traj = dict(X=f64(d["X"]), R=f64(d["R"]), V=f64(d["V"]))
+    worst = {}
+    for t in range(wl.steps):
+        d["G"].copy_(grad_to_device(hi.grads[t], dev))
+        before = state_snapshot(d)
+        plan.step()
+        torch.cuda.synchronize()
+        assert plan.status() == [0]
+        G64 = hi.grad_f64(t)
+        _, errs = check_step(before, G64, d, s.eta, s.beta, variant, s.scale,
+                             U_gpu=plan.buffer(0, dion.BUF_U))
+        for k, v in errs.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+        ref = O.oracle_step(traj["X"], G64, traj["R"], traj["V"], s.eta, s.beta, variant, s.scale)
+        traj = dict(X=ref["X"], R=ref["R"], V=ref["V"])
+    after = state_snapshot(d)
+    assert rel(after["X"], traj["X"]) <= TOL_CHAIN
+    assert rel(after["R"], traj["R"]) <= TOL_CHAIN
+    print(wname, variant, "worst single-step errors", worst)
+
+
+# ---------------------------------------------------------------- batched models
+def device_plan(wl, dev, variants=("orth",), indices=None, seed=0):
+    mats = []
+    for k, spec in enumerate(wl.mats):
+        X0, V0_raw, G = synth.device_matrix_inputs(spec, wl, k, seed=seed, device=dev)
+        import torch
+        V0 = to_dev(orth_v0(f64(V0_raw)), dev)
+        mats.append(dict(X=X0, G=G, R=torch.zeros_like(X0), V=V0, eta=spec.eta, beta=spec.beta,
+                         variant=variants[k % len(variants)], scale=spec.scale))
+    return mats
+
+
+def check_batched(wl, dev, check_idx, variants=("orth", "dion")):
+    import torch
+    mats = device_plan(wl, dev, variants)
+    plan = dion.Plan(mats)
+    before = {i: state_snapshot(mats[i]) for i in check_idx}
+    G64 = {i: grad_f64(mats[i]["G"]) for i in check_idx}
+    plan.step()
+    torch.cuda.synchronize()
+    st = plan.status()
+    assert all(v == 0 for v in st), st
+    worst = {}
+    for i in check_idx:
+        spec = wl.mats[i]
+        _, errs = check_step(before[i], G64[i], mats[i], spec.eta, spec.beta, mats[i]["variant"],
+                             spec.scale, U_gpu=plan.buffer(i, dion.BUF_U))
+        for k, v in errs.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+    print(wl.name, "worst", worst)
+    return plan, mats
+
+
+def test_gpt160m_all_matrices(dev):
+    wl = workloads.gpt_160m(4)
+    check_batched(wl, dev, list(range(len(wl.mats))))
+
+
+@pytest.mark.slow
+def test_llama3b_rdiv16_layers_0_and_27(dev):
+    wl = workloads.llama_3b(16)
+    idx = list(range(0, 7)) + list(range(27 * 7, 28 * 7))
+    check_batched(wl, dev, idx)
+
+
+# ---------------------------------------------------------------- per-phase intermediates
+PHASE_CASES = [(100, 36, 1), (100, 36, 3), (36, 100, 17), (200, 64, 16), (64, 64, 64),
+               (130, 260, 33), (257, 129, 2), (33, 48, 33)]
+
+
+@pytest.mark.parametrize("m,n,r", PHASE_CASES)
+@pytest.mark.parametrize("variant", ["orth", "dion"])
+def test_phase_intermediates(dev, m, n, r, variant):
+    import torch
+    g = np.random.Generator(np.random.PCG64(m * 1000 + n * 10 + r))
+    ld = ((n + 7) // 8) * 8 + 8           # padded row pitch, exercises ld > n
+    X = padded(to_dev(g.normal(0, 0.02, (m, n)), dev), ld)
+    R = padded(to_dev(0.05 * g.standard_normal((m, n)), dev), ld)
+    Gn = (g.standard_normal((m, 4)) @ g.standard_normal((4, n)) + 0.1 * g.standard_normal((m, n)))
+    G = padded(grad_to_device(synth.f32_to_bf16_bits(Gn.astype(np.float32)), dev), ld)
+    V = to_dev(g.standard_normal((n, r)), dev)            # warm start need not be orthonormal
+    d = dict(X=X, G=G, R=R, V=V, eta=0.03, beta=0.9, variant=variant)
+    plan = dion.Plan([d])
+    before = state_snapshot(d)
+    G64 = grad_f64(G)
+    ref = O.oracle_step(before["X"], G64, before["R"], before["V"], 0.03, 0.9, variant)
+    plan.phases(0, 0)
+    torch.cuda.synchronize()
+    assert rel(f64(plan.buffer(0, dion.BUF_P)), ref["P"]) < 1e-5
+    plan.phases(1, 1)
+    U = f64(plan.buffer(0, dion.BUF_U))
+    assert np.abs(U.T @ U - np.eye(r)).max() < TOL_ORTH
+    assert rel(U, ref["U"]) < 1e-4
+    plan.phases(2, 2)
+    assert rel(f64(plan.buffer(0, dion.BUF_W)), ref["W"]) < 1e-4
+    plan.phases(3, 3)
+    assert rel(f64(d["V"]), ref["Vbar"]) < 1e-4
+    plan.phases(4, 4)
+    torch.cuda.synchronize()
+    assert plan.status() == [0]
+    assert rel(f64(d["X"]), ref["X"]) < TOL_STEP
+    if r == min(m, n):
+        # full rank: U U^T M = M, the residual vanishes; only fp32 rounding residue is left
+        assert np.linalg.norm(f64(d["R"])) <= 1e-5 * 0.9 * np.linalg.norm(ref["M"])
+    else:
+        assert rel(f64(d["R"]), ref["R"]) < TOL_STEP
+    assert rel(f64(d["X"]) - before["X"], ref["X"] - before["X"]) < 1e-3
+
+
+def test_mixed_batch_dtypes_variants_shapes(dev):
+    import torch
+    g = np.random.Generator(np.random.PCG64(7))
+    mats, refs, befores = [], [], []
+    for k, (m, n, r, gdt, var) in enumerate([(96, 64, 8, "f32", "orth"), (64, 96, 8, "bf16", "dion"),
+                                             (128, 128, 32, "bf16", "orth"), (48, 40, 1, "f32", "dion")]):
+        X = to_dev(g.normal(0, 0.02, (m, n)), dev)
+        R = to_dev(0.02 * g.standard_normal((m, n)), dev)
+        Gn = (g.standard_normal((m, n)) * 0.1 + g.standard_normal((m, 2)) @ g.standard_normal((2, n)))
+        G = grad_to_device(synth.f32_to_bf16_bits(Gn.astype(np.float32)) if gdt == "bf16"
+                           else Gn.astype(np.float32), dev)
+        V = to_dev(orth_v0(g.standard_normal((n, r))), dev)
+        d = dict(X=X, G=G, R=R, V=V, eta=0.01 * (k + 1), beta=0.9, variant=var, scale=1.5 if k == 2 else 0.0)
+        mats.append(d)
+    plan = dion.Plan(mats)
+    befores = [state_snapshot(d) for d in mats]
+    plan.step()
+    torch.cuda.synchronize()
+    assert plan.status() == [0, 0, 0, 0]
+    for k, d in enumerate(mats):
+        sc = 1.5 if k == 2 else None
+        check_step(befores[k], grad_f64(d["G"]), d, d["eta"], d["beta"], d["variant"], sc,
+                   U_gpu=plan.buffer(k, dion.BUF_U))
+
+
+# ---------------------------------------------------------------- failure handling
+def test_rank_deficient_sets_status_and_leaves_state(dev):
+    import torch
+    m, n, r = 64, 32, 4
+    X = torch.randn(m, n, device=dev)
+    R = torch.zeros(m, n, device=dev)
+    G = torch.zeros(m, n, device=dev)
+    V = torch.randn(n, r, device=dev)
+    ok = dict(X=torch.randn(m, n, device=dev), G=torch.randn(m, n, device=dev), R=torch.zeros(m, n, device=dev),
+              V=torch.randn(n, r, device=dev), eta=0.1, beta=0.9)
+    snap = [t.clone() for t in (X, R, V)]
+    plan = dion.Plan([dict(X=X, G=G, R=R, V=V, eta=0.1, beta=0.9), ok])
+    plan.step()
+    torch.cuda.synchronize()
+    st = plan.status()
+    assert st[0] & dion.DION_MAT_CHOL_BREAKDOWN and st[1] == 0
+    for a, b in zip((X, R, V), snap):
+        assert torch.equal(a, b)
+
+
+def test_nonfinite_gradient_sets_status(dev):
+    import torch
+    m, n, r = 64, 32, 4
+    G = torch.randn(m, n, device=dev)
+    G[3, 5] = float("nan")
+    X = torch.randn(m, n, device=dev)
+    R = torch.zeros(m, n, device=dev)
+    V = torch.randn(n, r, device=dev)
+    snap = [t.clone() for t in (X, R, V)]
+    plan = dion.Plan([dict(X=X, G=G, R=R, V=V, eta=0.1, beta=0.9)])
+    plan.step()
+    torch.cuda.synchronize()
+    st = plan.status()
+    assert st[0] & dion.DION_MAT_NONFINITE
+    for a, b in zip((X, R, V), snap):
+        assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------- determinism, resume
+def test_bitwise_deterministic_and_resumable(dev):
+    import torch
+    wl = workloads.gpt_160m(4)
+    sub = workloads.Workload("gpt_sub", wl.mats[:6], wl.g_dtype, wl.grad, wl.grad_rank, wl.grad_noise,
+                             wl.grad_signal)
+    a = device_plan(sub, dev, ("orth", "dion"))
+    b = [{k: (v.clone() if hasattr(v, "clone") else v) for k, v in d.items()} for d in a]
+    pa, pb = dion.Plan(a), dion.Plan(b)
+    for _ in range(3):
+        pa.step()
+        pb.step()
+    torch.cuda.synchronize()
+    for da, db in zip(a, b):
+        for k in ("X", "R", "V"):
+            assert torch.equal(da[k], db[k])
+    # checkpoint after 3 steps, resume with a fresh plan on the saved state, 2 more steps
+    c = [{k: (v.clone() if hasattr(v, "clone") else v) for k, v in d.items()} for d in a]
+    for _ in range(2):
+        pa.step()
+    pc = dion.Plan(c)
+    for _ in range(2):
+        pc.step()
+    torch.cuda.synchronize()
+    for da, dc in zip(a, c):
+        for k in ("X", "R", "V"):
+            assert torch.equal(da[k], dc[k])
+
+
+def test_set_hparams_takes_effect(dev):
+    import torch
+    g = np.random.Generator(np.random.PCG64(3))
+    m, n, r = 64, 48, 4
+    d = dict(X=to_dev(g.normal(0, 0.02, (m, n)), dev), G=to_dev(g.standard_normal((m, n)), dev),
+             R=torch.zeros(m, n, device=dev), V=to_dev(orth_v0(g.standard_normal((n, r))), dev),
+             eta=0.01, beta=0.9)
+    plan = dion.Plan([d])
+    plan.set_hparams(0, 0.2, 0.5)
+    before = state_snapshot(d)
+    plan.step()
+    torch.cuda.synchronize()
+    check_step(before, grad_f64(d["G"]), d, 0.2, 0.5, "orth")
