@@ -142,7 +142,9 @@ DION_API dion_status_t dion_step_batched(dion_plan* plan, void* workspace, size_
 
 /*
  * Run phases first..last (inclusive) of a step, for tests and profiling:
- *   0 (a): reset status, P = (G + R) V                    (P in the workspace)
+ *   0 (a): reset status, P = (G + R) V                    (P in the workspace;
+ *          for Dion matrices V is first replaced by orth(V), which leaves
+ *          orth(P) unchanged and keeps P well conditioned)
  *   1 (b): U = orth(P)                                     (U in the workspace)
  *   2 (c): W = (G + R)^T U                                 (W in the workspace)
  *   3 (d): Vbar = orth(W) or colnorm(W), written into V

@@ -20,6 +20,8 @@ struct MatDev {
   const void* G;       // m x n, ld ldg, fp32 or bf16
   float* R;            // m x n, ld ldr
   float* V;            // n x r dense: V_prev in, Vbar out
+  const float* Vin;    // warm start read by phase (a): V itself (Orth-Dion) or orth(V) (Dion)
+  long long ldvin;     // its leading dimension (r or rp)
   long long m, n, r, rp;       // rp = r rounded up to the tile granule
   long long ldx, ldg, ldr;
   int g_bf16;          // 1: G is bf16
@@ -34,6 +36,9 @@ struct MatDev {
   int kchunk;          // rows of M per split
   unsigned* status;    // per-matrix status word
 };
+
+// Status bits that stop the rest of a matrix's step.
+constexpr unsigned ST_FATAL = ST_BREAKDOWN | ST_NONFINITE;
 
 // One orth() problem: A (rows x r, lda) -> out (rows x r, ldo), by CholeskyQR2.
 struct OrthJob {

@@ -55,13 +55,14 @@ struct dion_plan {
   // workspace layout (byte offsets from the workspace base)
   size_t ws_bytes = 0;
   size_t off_tables = 0, tables_bytes = 0, off_status = 0;
-  std::vector<size_t> off_P, off_Q, off_U, off_W, off_Wpart, off_gpart, off_S, off_T;
+  std::vector<size_t> off_P, off_Q, off_U, off_W, off_Wpart, off_gpart, off_S, off_T, off_Vo;
 
   // table image layout (byte offsets inside the tables region)
-  size_t t_mats = 0, t_jobs_p = 0, t_jobs_w = 0;
+  size_t t_mats = 0, t_jobs_p = 0, t_jobs_w = 0, t_jobs_v = 0, t_ts_gram_v = 0, t_ts_trmm_v = 0;
   size_t t_ts_mv = 0, t_ts_gram_p = 0, t_ts_trmm_p = 0, t_ts_mtu = 0, t_ts_wred = 0,
          t_ts_epi = 0, t_ts_gram_w = 0, t_ts_trmm_w = 0, t_ts_coln = 0, t_coln_idx = 0;
   std::vector<int> ts_mv, ts_gram_p, ts_trmm_p, ts_mtu, ts_wred, ts_epi, ts_gram_w, ts_trmm_w, ts_coln;
+  std::vector<int> ts_gram_v, ts_trmm_v;   // orth(V) of the Dion matrices
   bool any_split = false;
 
   std::vector<unsigned char> image;
@@ -177,6 +178,8 @@ void layout(dion_plan* p) {
   prefix(p->ts_gram_w, p->orth_idx, [&](int i) { long long t = cdiv(p->rp[i], simt::TN); return p->nchunk_w[i] * t * t; });
   prefix(p->ts_trmm_w, p->orth_idx, [&](int i) { return cdiv(D(i).n, simt::TM) * cdiv(p->rp[i], simt::TN); });
   prefix(p->ts_coln, p->dion_idx, [&](int i) { return cdiv(D(i).r, 32); });
+  prefix(p->ts_gram_v, p->dion_idx, [&](int i) { long long t = cdiv(p->rp[i], simt::TN); return p->nchunk_w[i] * t * t; });
+  prefix(p->ts_trmm_v, p->dion_idx, [&](int i) { return cdiv(D(i).n, simt::TM) * cdiv(p->rp[i], simt::TN); });
 
   // ---- tables region
   size_t off = 0;
@@ -184,6 +187,9 @@ void layout(dion_plan* p) {
   p->t_mats = take(sizeof(MatDev) * cnt);
   p->t_jobs_p = take(sizeof(OrthJob) * cnt);
   p->t_jobs_w = take(sizeof(OrthJob) * std::max<size_t>(1, p->orth_idx.size()));
+  p->t_jobs_v = take(sizeof(OrthJob) * std::max<size_t>(1, p->dion_idx.size()));
+  p->t_ts_gram_v = take(4 * p->ts_gram_v.size());
+  p->t_ts_trmm_v = take(4 * p->ts_trmm_v.size());
   p->t_ts_mv = take(4 * p->ts_mv.size());
   p->t_ts_gram_p = take(4 * p->ts_gram_p.size());
   p->t_ts_trmm_p = take(4 * p->ts_trmm_p.size());
@@ -203,6 +209,7 @@ void layout(dion_plan* p) {
   p->off_status = region(4 * (size_t)cnt);
   p->off_P.resize(cnt); p->off_Q.resize(cnt); p->off_U.resize(cnt); p->off_W.resize(cnt);
   p->off_Wpart.resize(cnt); p->off_gpart.resize(cnt); p->off_S.resize(cnt); p->off_T.resize(cnt);
+  p->off_Vo.resize(cnt);
   for (int i = 0; i < cnt; ++i) {
     const long long m = D(i).m, n = D(i).n, rp = p->rp[i];
     p->off_P[i] = region(4 * (size_t)(m * rp));
@@ -213,6 +220,7 @@ void layout(dion_plan* p) {
     p->off_gpart[i] = region(4 * (size_t)std::max(p->nchunk_p[i], p->nchunk_w[i]) * (size_t)(rp * rp));
     p->off_S[i] = region(4 * (size_t)(rp * rp));
     p->off_T[i] = region(4 * (size_t)(rp * rp));
+    p->off_Vo[i] = region(D(i).variant == DION_VARIANT_DION ? 4 * (size_t)(n * rp) : 4);
   }
   p->ws_bytes = ws;
 }
@@ -221,12 +229,19 @@ void build_image(dion_plan* p, unsigned char* base) {
   const int cnt = p->count;
   p->image.assign(p->tables_bytes, 0);
   std::vector<MatDev> mats(cnt);
-  std::vector<OrthJob> jp(cnt), jw(std::max<size_t>(1, p->orth_idx.size()));
+  std::vector<OrthJob> jp(cnt), jw(std::max<size_t>(1, p->orth_idx.size())),
+      jv(std::max<size_t>(1, p->dion_idx.size()));
   unsigned* status = reinterpret_cast<unsigned*>(base + p->off_status);
   for (int i = 0; i < cnt; ++i) {
     const auto& d = p->descs[i];
     MatDev& x = mats[i];
     x.X = d.X; x.G = d.G; x.R = d.R; x.V = d.V;
+    // Dion's warm start Vbar = W diag(1/|w_j|) can be far from orthonormal; phase (a)
+    // then reads orth(V) instead, which leaves U = orth(M V) unchanged (orth(A T) = orth(A)
+    // for T upper triangular with a positive diagonal) and keeps M V well conditioned.
+    const bool dn = d.variant == DION_VARIANT_DION;
+    x.Vin = dn ? reinterpret_cast<const float*>(base + p->off_Vo[i]) : d.V;
+    x.ldvin = dn ? p->rp[i] : d.r;
     x.m = d.m; x.n = d.n; x.r = d.r; x.rp = p->rp[i];
     x.ldx = d.ld_x; x.ldg = d.ld_g; x.ldr = d.ld_r;
     x.g_bf16 = d.g_dtype == DION_DTYPE_BF16;
@@ -264,7 +279,19 @@ void build_image(dion_plan* p, unsigned char* base) {
     o.out = x.V; o.ldo = x.r; o.out_cols = x.r;
     o.nchunk = p->nchunk_w[i]; o.chunk = p->chunk_w[i];
   }
+  for (size_t k = 0; k < p->dion_idx.size(); ++k) {
+    const int i = p->dion_idx[k];
+    const MatDev& x = mats[i];
+    OrthJob& o = jv[k];
+    o = jp[i];
+    o.A = x.V; o.lda = x.r; o.rows = x.n;
+    o.out = const_cast<float*>(x.Vin); o.ldo = x.rp; o.out_cols = x.rp;
+    o.nchunk = p->nchunk_w[i]; o.chunk = p->chunk_w[i];
+  }
   put(p->image, p->t_mats, mats.data(), mats.size());
+  put(p->image, p->t_jobs_v, jv.data(), jv.size());
+  put(p->image, p->t_ts_gram_v, p->ts_gram_v.data(), p->ts_gram_v.size());
+  put(p->image, p->t_ts_trmm_v, p->ts_trmm_v.data(), p->ts_trmm_v.size());
   put(p->image, p->t_jobs_p, jp.data(), jp.size());
   put(p->image, p->t_jobs_w, jw.data(), jw.size());
   put(p->image, p->t_ts_mv, p->ts_mv.data(), p->ts_mv.size());
@@ -335,6 +362,9 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
       case 0:
         if (cudaMemsetAsync(base + p->off_status, 0, 4 * (size_t)cnt, s) != cudaSuccess)
           return cuda_check("status reset");
+        st = launch_orth(p, base, s, p->t_jobs_v, p->t_ts_gram_v, p->t_ts_trmm_v, p->ts_gram_v,
+                         p->ts_trmm_v, (int)p->dion_idx.size());
+        if (st) return st;
         simt::k_mv<<<p->ts_mv[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_mv), cnt);
         break;
       case 1:
@@ -477,6 +507,7 @@ dion_status_t dion_plan_get_status(dion_plan* plan, const void* workspace, size_
 int32_t dion_plan_launches_per_step(const dion_plan* plan) {
   if (!plan) return -1;
   int n = 1;                                   // phase (a)
+  n += plan->dion_idx.empty() ? 0 : 6;         // phase (a), orth(V) of the Dion matrices
   n += 6;                                      // phase (b): two CholeskyQR rounds
   n += 1 + (plan->any_split ? 1 : 0);          // phase (c)
   n += plan->orth_idx.empty() ? 0 : 6;         // phase (d), Orth-Dion matrices

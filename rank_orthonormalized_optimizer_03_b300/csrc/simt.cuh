@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(NT) k_mv(const MatDev* __restrict__ mats,
   float acc[4][4];
   zero(acc);
   LoadM la{&d};
-  LoadRM lb{d.V, d.r, d.n, d.r};
+  LoadRM lb{d.Vin, d.ldvin, d.n, d.r};
   tile_acc<true, true>(la, lb, i0, c0, 0, d.n, acc, As, Bs);
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
 #pragma unroll
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(NT) k_gram(const OrthJob* __restrict__ jobs,
   __shared__ float As[TK * LDS], Bs[TK * LDS];
   const int j = find_job(tstart, njob, blockIdx.x);
   const OrthJob& o = jobs[j];
-  if (pass == 1 && *o.status) return;
+  if (*o.status & ST_FATAL) return;
   const int local = blockIdx.x - tstart[j];
   const int nt = (int)((o.rp + TN - 1) / TN);
   const int chunk = local / (nt * nt), rem = local % (nt * nt);
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(CHOL_NT) k_chol_inv(const OrthJob* __restrict_
   const OrthJob& o = jobs[blockIdx.x];
   __shared__ int s_bad;
   __shared__ float s_piv;
-  if (*o.status) return;
+  if (*o.status & ST_FATAL) return;
   const int tid = threadIdx.x, nth = blockDim.x;
   const long long r = o.r, rp = o.rp;
   float* S = o.S;
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(NT) k_trmm(const OrthJob* __restrict__ jobs,
   __shared__ float As[TK * LDS], Bs[TK * LDS];
   const int j = find_job(tstart, njob, blockIdx.x);
   const OrthJob& o = jobs[j];
-  if (*o.status) return;
+  if (*o.status & ST_FATAL) return;
   const int local = blockIdx.x - tstart[j];
   const int ntc = (int)((o.rp + TN - 1) / TN);
   const long long i0 = (long long)(local / ntc) * TM, c0 = (long long)(local % ntc) * TN;
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(NT) k_mtu(const MatDev* __restrict__ mats,
   __shared__ float As[TK * LDS], Bs[TK * LDS];
   const int j = find_job(tstart, nmat, blockIdx.x);
   const MatDev& d = mats[j];
-  if (*d.status) return;
+  if (*d.status & ST_FATAL) return;
   const int local = blockIdx.x - tstart[j];
   const int ntc = (int)((d.rp + TN - 1) / TN);
   const int ntn = (int)((d.n + TM - 1) / TM);
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(NT) k_wreduce(const MatDev* __restrict__ mats,
                                                 const int* __restrict__ tstart, int nmat) {
   const int j = find_job(tstart, nmat, blockIdx.x);
   const MatDev& d = mats[j];
-  if (*d.status || d.ksplit <= 1) return;
+  if ((*d.status & ST_FATAL) || d.ksplit <= 1) return;
   const long long base = (long long)(blockIdx.x - tstart[j]) * 1024;
   const long long tot = d.n * d.rp;
   for (int e = threadIdx.x; e < 1024; e += NT) {
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(NT) k_colnorm(const MatDev* __restrict__ mats,
   __shared__ float scale[32];
   const int jj = find_job(tstart, nidx, blockIdx.x);
   const MatDev& d = mats[idx[jj]];
-  if (*d.status) return;
+  if (*d.status & ST_FATAL) return;
   const long long c = (long long)(blockIdx.x - tstart[jj]) * 32 + (threadIdx.x & 31);
   const int w = threadIdx.x >> 5;
   float s = 0.f;
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(NT) k_epilogue(const MatDev* __restrict__ mats
   __shared__ float As[TK * LDS], B1[TK * LDS], B2[TK * LDS];
   const int j = find_job(tstart, nmat, blockIdx.x);
   const MatDev& d = mats[j];
-  if (*d.status) return;
+  if (*d.status & ST_FATAL) return;
   const int local = blockIdx.x - tstart[j];
   const int ntn = (int)((d.n + TN - 1) / TN);
   const long long i0 = (long long)(local / ntn) * TM, j0 = (long long)(local % ntn) * TN;

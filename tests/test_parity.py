@@ -141,7 +141,9 @@ def test_phase_intermediates(dev, m, n, r, variant):
     ref = O.oracle_step(before["X"], G64, before["R"], before["V"], 0.03, 0.9, variant)
     plan.phases(0, 0)
     torch.cuda.synchronize()
-    assert rel(f64(plan.buffer(0, dion.BUF_P)), ref["P"]) < 1e-5
+    # Dion: phase (a) forms M orth(V), which has the same orth() as M V
+    P_ref = ref["P"] if variant == "orth" else ref["M"] @ O.orth(before["V"])[0]
+    assert rel(f64(plan.buffer(0, dion.BUF_P)), P_ref) < 1e-5
     plan.phases(1, 1)
     U = f64(plan.buffer(0, dion.BUF_U))
     assert np.abs(U.T @ U - np.eye(r)).max() < TOL_ORTH
@@ -267,3 +269,24 @@ def test_set_hparams_takes_effect(dev):
     plan.step()
     torch.cuda.synchronize()
     check_step(before, grad_f64(d["G"]), d, 0.2, 0.5, "orth")
+
+
+@pytest.mark.parametrize("variant", ["dion", "orth"])
+def test_consecutive_steps_from_random_warm_start(dev, variant):
+    """Step 2 of Dion starts from Vbar = colnorm(W), whose condition number is ~2e2 here;
+    with a strong low-rank gradient M Vbar then has condition ~1e4, beyond fp32 CholeskyQR.
+    The step must still match the oracle (the library orthonormalises V first)."""
+    import torch
+    wl = workloads.gpt_160m(4)
+    spec = wl.mats[4]                                   # 3072 x 768, r = 192
+    X0, V0_raw, G = synth.device_matrix_inputs(spec, wl, 4, seed=1, device=dev)
+    d = dict(X=X0, G=G, R=torch.zeros_like(X0), V=to_dev(orth_v0(f64(V0_raw)), dev), eta=spec.eta,
+             beta=spec.beta, variant=variant, scale=spec.scale)
+    plan = dion.Plan([d])
+    G64 = grad_f64(G)
+    for _ in range(3):
+        before = state_snapshot(d)
+        plan.step()
+        torch.cuda.synchronize()
+        assert plan.status() == [0]
+        check_step(before, G64, d, spec.eta, spec.beta, variant, spec.scale, U_gpu=plan.buffer(0, dion.BUF_U))
