@@ -181,8 +181,10 @@ def run_cuda(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
+    from rank_orthonormalized_optimizer_03_b300.dion import DION_MAT_SHIFTED, FATAL
     status = plan.status()
-    bad = sum(1 for v in status if v)
+    bad = sum(1 for v in status if v & FATAL)
+    shifted = sum(1 for v in status if v & DION_MAT_SHIFTED)
 
     step_bytes = cost["step"].bytes
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
@@ -227,7 +229,7 @@ def run_cuda(args):
         "roofline": roof,
         "clocks": clk.summary(),
         "gpu_launches": plan.launches_per_step * args.steps,
-        "status_nonzero": bad,
+        "status_failed": bad, "status_shifted": shifted,
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -34,7 +34,8 @@
  *  - Return values are host-side status codes (dion_status_t).  Numerical
  *    trouble inside a step never traps or hangs: it sets per-matrix bits in
  *    device status words, read with dion_plan_get_status().  A matrix whose
- *    status is not DION_MAT_OK after a step was left unchanged (X, R, V).
+ *    status has any bit other than DION_MAT_SHIFTED set after a step was left
+ *    unchanged (X, R, V), except after DION_MAT_TIMEOUT (update incomplete).
  *  - Thread safety: a plan may be used by one host thread at a time.
  *    dion_last_error() is per host thread.
  */
@@ -68,7 +69,11 @@ typedef enum {
 enum {
   DION_MAT_OK = 0,
   DION_MAT_CHOL_BREAKDOWN = 1,  /* orth(): non-positive Cholesky pivot (rank-deficient argument) */
-  DION_MAT_NONFINITE = 2        /* orth(): non-finite value met (NaN / Inf in the inputs)        */
+  DION_MAT_NONFINITE = 2,       /* orth(): non-finite value met (NaN / Inf in the inputs)        */
+  DION_MAT_TIMEOUT = 4,         /* a pipeline wait inside a tensor-core kernel gave up after 2 s;
+                                   the kernel returned early and this matrix's update is incomplete */
+  DION_MAT_SHIFTED = 8          /* informational: an orth() of this matrix was ill conditioned
+                                   (kappa > ~1e3) and took shifted CholeskyQR3; the update is complete */
 };
 
 typedef enum { DION_VARIANT_DION = 0, DION_VARIANT_ORTH = 1 } dion_variant_t;

@@ -13,6 +13,8 @@ namespace dion {
 // Per-matrix status bits (same values as DION_MAT_* in dion.h).
 constexpr unsigned ST_BREAKDOWN = 1u;
 constexpr unsigned ST_NONFINITE = 2u;
+constexpr unsigned ST_TIMEOUT = 4u;     // a bounded wait inside a tensor-core kernel gave up
+constexpr unsigned ST_SHIFTED = 8u;     // informational: an orth() of this matrix needed the shifted pass
 
 // One weight matrix of the batch, with the workspace buffers of its step.
 struct MatDev {
@@ -40,11 +42,14 @@ struct MatDev {
 // Status bits that stop the rest of a matrix's step.
 constexpr unsigned ST_FATAL = ST_BREAKDOWN | ST_NONFINITE;
 
-// One orth() problem: A (rows x r, lda) -> out (rows x r, ldo), by CholeskyQR2.
+// One orth() problem: A (rows x r, lda) -> out (rows x r, ldo), by CholeskyQR2,
+// or shifted CholeskyQR3 when the first Cholesky shows A is ill conditioned.
 struct OrthJob {
   const float* A;      // input, rows x r (ld lda)
   long long lda;
   float* Q;            // first-pass factor, rows x rp (ld rp)
+  float* Q2;           // second-pass factor of a shifted (three-pass) job, rows x rp
+  unsigned* flag;      // 1: this job took the shifted first pass and needs a third
   float* out;          // result, rows x out_cols (ld ldo)
   long long ldo;
   long long out_cols;  // columns written to out (rp in the workspace, r into V)

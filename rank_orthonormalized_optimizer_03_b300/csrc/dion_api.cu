@@ -13,6 +13,9 @@
 
 #include "common.cuh"
 #include "simt.cuh"
+#include "tc_epilogue.cuh"
+#include "tc_split.cuh"
+#include "tc_stream.cuh"
 
 using namespace dion;
 
@@ -39,8 +42,8 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
-// rank padding granule: the tensor-core tiles take N in multiples of 16
-constexpr long long kRankGranule = 16;
+// rank padding granule: one 128-byte row of fp32 operands (the tensor-core K step)
+constexpr long long kRankGranule = 32;
 
 }  // namespace
 
@@ -55,7 +58,7 @@ struct dion_plan {
   // workspace layout (byte offsets from the workspace base)
   size_t ws_bytes = 0;
   size_t off_tables = 0, tables_bytes = 0, off_status = 0;
-  std::vector<size_t> off_P, off_Q, off_U, off_W, off_Wpart, off_gpart, off_S, off_T, off_Vo;
+  std::vector<size_t> off_P, off_Q, off_Q2, off_U, off_W, off_Wpart, off_gpart, off_S, off_T, off_Vo;
 
   // table image layout (byte offsets inside the tables region)
   size_t t_mats = 0, t_jobs_p = 0, t_jobs_w = 0, t_jobs_v = 0, t_ts_gram_v = 0, t_ts_trmm_v = 0;
@@ -64,6 +67,19 @@ struct dion_plan {
   std::vector<int> ts_mv, ts_gram_p, ts_trmm_p, ts_mtu, ts_wred, ts_epi, ts_gram_w, ts_trmm_w, ts_coln;
   std::vector<int> ts_gram_v, ts_trmm_v;   // orth(V) of the Dion matrices
   bool any_split = false;
+
+  // tensor-core path: split (hi/lo tf32) operand copies and the phase (e) tables
+  std::vector<size_t> off_Uh, off_Ul, off_Vh, off_Vl, off_Wh, off_Wl;
+  size_t t_epi = 0, t_ts_epi_tc = 0, t_split = 0, t_ts_split = 0;
+  std::vector<int> ts_epi_tc, ts_split;
+  int n_split = 0;
+  int num_sms = 0;
+  // phases (a) and (c): streaming jobs, transposed split copies V^T, U^T
+  std::vector<int> ncb, bn;
+  std::vector<long long> ldt_n, ldt_m;
+  std::vector<size_t> off_VTh, off_VTl, off_UTh, off_UTl;
+  size_t t_sj_a = 0, t_sj_c = 0, t_ts_sa = 0, t_ts_sc = 0, t_tj_v = 0, t_tj_u = 0, t_ts_tv = 0, t_ts_tu = 0;
+  std::vector<int> ts_sa, ts_sc, ts_tv, ts_tu;
 
   std::vector<unsigned char> image;
   const void* uploaded_ws = nullptr;
@@ -135,16 +151,25 @@ void layout(dion_plan* p) {
     p->rp[i] = cdiv(d.r, kRankGranule) * kRankGranule;
     (d.variant == DION_VARIANT_ORTH ? p->orth_idx : p->dion_idx).push_back(i);
   }
-  // split of the row range in phase (c) so that a lone matrix still fills the GPU
-  long long tiles_c = 0;
-  for (int i = 0; i < cnt; ++i)
-    tiles_c += cdiv(p->descs[i].n, simt::TM) * cdiv(p->rp[i], simt::TN);
-  const long long want = 4LL * 148;
-  const long long split = tiles_c >= want ? 1 : cdiv(want, tiles_c);
+  // column blocks of the streaming kernels (TMEM holds two slices of bn <= 192 columns)
+  p->ncb.resize(cnt); p->bn.resize(cnt); p->ldt_n.resize(cnt); p->ldt_m.resize(cnt);
+  for (int i = 0; i < cnt; ++i) {
+    p->ncb[i] = (int)cdiv(p->rp[i], tcstream::BN_MAX);
+    p->bn[i] = (int)(cdiv(cdiv(p->rp[i], p->ncb[i]), 32) * 32);
+    p->ldt_n[i] = cdiv(p->descs[i].n, 32) * 32;
+    p->ldt_m[i] = cdiv(p->descs[i].m, 32) * 32;
+  }
+  // phase (c) splits the rows of M (its K) into ranges of at most 2048 (8 TMEM
+  // slices), smaller when the batch has too few items to fill the GPU
+  long long items_c = 0;
+  for (int i = 0; i < cnt; ++i) items_c += cdiv(p->descs[i].n, tcstream::BM) * p->ncb[i];
+  const long long want = 2LL * 148;
+  const long long split = items_c >= want ? 1 : cdiv(want, items_c);
   for (int i = 0; i < cnt; ++i) {
     const long long m = p->descs[i].m;
-    long long s = std::min<long long>(split, std::max<long long>(1, m / 256));
-    long long ch = cdiv(cdiv(m, s), 16) * 16;
+    long long ch = cdiv(cdiv(m, split), 256) * 256;
+    ch = std::min<long long>(ch, 2048);
+    ch = std::min<long long>(ch, cdiv(m, 32) * 32);
     p->kchunk[i] = (int)ch;
     p->ksplit[i] = (int)cdiv(m, ch);
     if (p->ksplit[i] > 1) p->any_split = true;
@@ -183,7 +208,35 @@ void layout(dion_plan* p) {
 
   // ---- tables region
   size_t off = 0;
-  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 16); return o; };
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 128); return o; };
+  // tensor-core tables first: they hold CUtensorMaps (64-byte alignment)
+  prefix(p->ts_epi_tc, all, [&](int i) { return cdiv(D(i).m, tcepi::BM) * cdiv(D(i).n, tcepi::BNJ); });
+  p->n_split = 3 * cnt;
+  {
+    std::vector<int> jobs(p->n_split);
+    for (int k = 0; k < p->n_split; ++k) jobs[k] = k;
+    prefix(p->ts_split, jobs, [&](int k) {
+      const int i = k / 3;
+      const long long rows = (k % 3 == 0) ? D(i).m : D(i).n;
+      return cdiv(rows * p->rp[i], tcsplit::ELEMS_PER_CTA);
+    });
+  }
+  prefix(p->ts_sa, all, [&](int i) { return cdiv(D(i).m, tcstream::BM) * p->ncb[i]; });
+  prefix(p->ts_sc, all, [&](int i) { return cdiv(D(i).n, tcstream::BM) * (long long)p->ksplit[i] * p->ncb[i]; });
+  prefix(p->ts_tv, all, [&](int i) { return cdiv(D(i).n, 32) * cdiv(p->rp[i], 32); });
+  prefix(p->ts_tu, all, [&](int i) { return cdiv(D(i).m, 32) * cdiv(p->rp[i], 32); });
+  p->t_sj_a = take(sizeof(tcstream::SJob) * cnt);
+  p->t_sj_c = take(sizeof(tcstream::SJob) * cnt);
+  p->t_epi = take(sizeof(tcepi::EpiMat) * cnt);
+  p->t_split = take(sizeof(tcsplit::SplitJob) * p->n_split);
+  p->t_ts_epi_tc = take(4 * p->ts_epi_tc.size());
+  p->t_ts_split = take(4 * p->ts_split.size());
+  p->t_ts_sa = take(4 * p->ts_sa.size());
+  p->t_ts_sc = take(4 * p->ts_sc.size());
+  p->t_tj_v = take(sizeof(tcsplit::TJob) * cnt);
+  p->t_tj_u = take(sizeof(tcsplit::TJob) * cnt);
+  p->t_ts_tv = take(4 * p->ts_tv.size());
+  p->t_ts_tu = take(4 * p->ts_tu.size());
   p->t_mats = take(sizeof(MatDev) * cnt);
   p->t_jobs_p = take(sizeof(OrthJob) * cnt);
   p->t_jobs_w = take(sizeof(OrthJob) * std::max<size_t>(1, p->orth_idx.size()));
@@ -206,7 +259,9 @@ void layout(dion_plan* p) {
   size_t ws = 0;
   auto region = [&](size_t bytes) { size_t o = ws; ws = align_up(ws + std::max<size_t>(bytes, 4), kAlign); return o; };
   p->off_tables = region(p->tables_bytes);
-  p->off_status = region(4 * (size_t)cnt);
+  // status words, then the three-pass flags of the orth() of P, W and V
+  p->off_status = region(16 * (size_t)cnt);
+  p->off_Q2.resize(cnt);
   p->off_P.resize(cnt); p->off_Q.resize(cnt); p->off_U.resize(cnt); p->off_W.resize(cnt);
   p->off_Wpart.resize(cnt); p->off_gpart.resize(cnt); p->off_S.resize(cnt); p->off_T.resize(cnt);
   p->off_Vo.resize(cnt);
@@ -214,6 +269,7 @@ void layout(dion_plan* p) {
     const long long m = D(i).m, n = D(i).n, rp = p->rp[i];
     p->off_P[i] = region(4 * (size_t)(m * rp));
     p->off_Q[i] = region(4 * (size_t)(std::max(m, n) * rp));
+    p->off_Q2[i] = region(4 * (size_t)(std::max(m, n) * rp));
     p->off_U[i] = region(4 * (size_t)(m * rp));
     p->off_W[i] = region(4 * (size_t)(n * rp));
     p->off_Wpart[i] = region(p->ksplit[i] > 1 ? 4 * (size_t)p->ksplit[i] * (size_t)(n * rp) : 4);
@@ -222,10 +278,61 @@ void layout(dion_plan* p) {
     p->off_T[i] = region(4 * (size_t)(rp * rp));
     p->off_Vo[i] = region(D(i).variant == DION_VARIANT_DION ? 4 * (size_t)(n * rp) : 4);
   }
+  p->off_VTh.resize(cnt); p->off_VTl.resize(cnt); p->off_UTh.resize(cnt); p->off_UTl.resize(cnt);
+  for (int i = 0; i < cnt; ++i) {
+    const long long rp = p->rp[i];
+    p->off_VTh[i] = region(4 * (size_t)(rp * p->ldt_n[i]));
+    p->off_VTl[i] = region(4 * (size_t)(rp * p->ldt_n[i]));
+    p->off_UTh[i] = region(4 * (size_t)(rp * p->ldt_m[i]));
+    p->off_UTl[i] = region(4 * (size_t)(rp * p->ldt_m[i]));
+  }
+  p->off_Uh.resize(cnt); p->off_Ul.resize(cnt); p->off_Vh.resize(cnt); p->off_Vl.resize(cnt);
+  p->off_Wh.resize(cnt); p->off_Wl.resize(cnt);
+  for (int i = 0; i < cnt; ++i) {
+    const long long m = D(i).m, n = D(i).n, rp = p->rp[i];
+    p->off_Uh[i] = region(4 * (size_t)(m * rp));
+    p->off_Ul[i] = region(4 * (size_t)(m * rp));
+    p->off_Vh[i] = region(4 * (size_t)(n * rp));
+    p->off_Vl[i] = region(4 * (size_t)(n * rp));
+    p->off_Wh[i] = region(4 * (size_t)(n * rp));
+    p->off_Wl[i] = region(4 * (size_t)(n * rp));
+  }
   p->ws_bytes = ws;
 }
 
-void build_image(dion_plan* p, unsigned char* base) {
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// 2-D row-major tensor map: `cols` elements per row (the contiguous dimension),
+// `rows` rows `pitch_bytes` apart; box of box_cols x box_rows elements.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, long long cols, long long rows,
+              long long pitch_bytes, int box_cols, int box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)pitch_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+dion_status_t build_image(dion_plan* p, unsigned char* base) {
   const int cnt = p->count;
   p->image.assign(p->tables_bytes, 0);
   std::vector<MatDev> mats(cnt);
@@ -260,6 +367,7 @@ void build_image(dion_plan* p, unsigned char* base) {
                    long long ocols, int nch, int ch) {
       o.A = A; o.lda = x.rp;
       o.Q = reinterpret_cast<float*>(base + p->off_Q[i]);
+      o.Q2 = reinterpret_cast<float*>(base + p->off_Q2[i]);
       o.out = out; o.ldo = ldo; o.out_cols = ocols;
       o.gpart = reinterpret_cast<float*>(base + p->off_gpart[i]);
       o.S = reinterpret_cast<float*>(base + p->off_S[i]);
@@ -269,6 +377,7 @@ void build_image(dion_plan* p, unsigned char* base) {
       o.status = x.status;
     };
     job(jp[i], x.P, x.m, x.U, x.rp, x.rp, p->nchunk_p[i], p->chunk_p[i]);
+    jp[i].flag = status + cnt + i;
   }
   for (size_t k = 0; k < p->orth_idx.size(); ++k) {
     const int i = p->orth_idx[k];
@@ -278,6 +387,7 @@ void build_image(dion_plan* p, unsigned char* base) {
     o.A = x.W; o.lda = x.rp; o.rows = x.n;
     o.out = x.V; o.ldo = x.r; o.out_cols = x.r;
     o.nchunk = p->nchunk_w[i]; o.chunk = p->chunk_w[i];
+    o.flag = status + 2 * cnt + i;
   }
   for (size_t k = 0; k < p->dion_idx.size(); ++k) {
     const int i = p->dion_idx[k];
@@ -287,6 +397,7 @@ void build_image(dion_plan* p, unsigned char* base) {
     o.A = x.V; o.lda = x.r; o.rows = x.n;
     o.out = const_cast<float*>(x.Vin); o.ldo = x.rp; o.out_cols = x.rp;
     o.nchunk = p->nchunk_w[i]; o.chunk = p->chunk_w[i];
+    o.flag = status + 3 * cnt + i;
   }
   put(p->image, p->t_mats, mats.data(), mats.size());
   put(p->image, p->t_jobs_v, jv.data(), jv.size());
@@ -304,6 +415,97 @@ void build_image(dion_plan* p, unsigned char* base) {
   put(p->image, p->t_ts_trmm_w, p->ts_trmm_w.data(), p->ts_trmm_w.size());
   put(p->image, p->t_ts_coln, p->ts_coln.data(), p->ts_coln.size());
   if (!p->dion_idx.empty()) put(p->image, p->t_coln_idx, p->dion_idx.data(), p->dion_idx.size());
+
+  // ---- tensor-core phase (e): operand maps (split copies in the workspace) and state maps
+  std::vector<tcepi::EpiMat> epi(cnt);
+  std::vector<tcsplit::SplitJob> sj(p->n_split);
+  const CUtensorMapDataType F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  for (int i = 0; i < cnt; ++i) {
+    const auto& d = p->descs[i];
+    const MatDev& x = mats[i];
+    const long long rp = p->rp[i];
+    float* Uh = reinterpret_cast<float*>(base + p->off_Uh[i]);
+    float* Ul = reinterpret_cast<float*>(base + p->off_Ul[i]);
+    float* Vh = reinterpret_cast<float*>(base + p->off_Vh[i]);
+    float* Vl = reinterpret_cast<float*>(base + p->off_Vl[i]);
+    float* Wh = reinterpret_cast<float*>(base + p->off_Wh[i]);
+    float* Wl = reinterpret_cast<float*>(base + p->off_Wl[i]);
+    tcepi::EpiMat& e = epi[i];
+    std::memset(&e, 0, sizeof e);
+    bool okm = true;
+    okm &= make_map(&e.map[tcepi::MAP_UH], F32, Uh, rp, d.m, rp * 4, tcepi::BK, tcepi::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&e.map[tcepi::MAP_UL], F32, Ul, rp, d.m, rp * 4, tcepi::BK, tcepi::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&e.map[tcepi::MAP_VH], F32, Vh, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&e.map[tcepi::MAP_VL], F32, Vl, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&e.map[tcepi::MAP_WH], F32, Wh, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&e.map[tcepi::MAP_WL], F32, Wl, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (d.g_dtype == DION_DTYPE_BF16)
+      okm &= make_map(&e.map[tcepi::MAP_G], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.G, d.n, d.m, d.ld_g * 2, tcepi::SUB,
+                      tcepi::BM, CU_TENSOR_MAP_SWIZZLE_32B);
+    else
+      okm &= make_map(&e.map[tcepi::MAP_G], F32, d.G, d.n, d.m, d.ld_g * 4, tcepi::SUB, tcepi::BM,
+                      CU_TENSOR_MAP_SWIZZLE_64B);
+    okm &= make_map(&e.map[tcepi::MAP_R], F32, d.R, d.n, d.m, d.ld_r * 4, tcepi::SUB, tcepi::BM, CU_TENSOR_MAP_SWIZZLE_64B);
+    okm &= make_map(&e.map[tcepi::MAP_X], F32, d.X, d.n, d.m, d.ld_x * 4, tcepi::SUB, tcepi::BM, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!okm) return fail(DION_ERR_CUDA, "matrix %d: cuTensorMapEncodeTiled failed", i);
+    e.m = (int)d.m; e.n = (int)d.n; e.rp = (int)rp; e.g_bf16 = x.g_bf16;
+    e.eta_s = x.eta_s; e.beta = x.beta; e.status = x.status;
+    // split jobs: U (workspace, ld rp), Vbar (= V after phase (d), ld r), W (workspace, ld rp)
+    sj[3 * i + 0] = tcsplit::SplitJob{x.U, rp, Uh, Ul, rp, d.m, d.r, x.status};
+    sj[3 * i + 1] = tcsplit::SplitJob{d.V, d.r, Vh, Vl, rp, d.n, d.r, x.status};
+    sj[3 * i + 2] = tcsplit::SplitJob{x.W, rp, Wh, Wl, rp, d.n, d.r, x.status};
+  }
+  // ---- tensor-core phases (a) and (c)
+  std::vector<tcstream::SJob> sa(cnt), sc(cnt);
+  std::vector<tcsplit::TJob> tv(cnt), tu(cnt);
+  for (int i = 0; i < cnt; ++i) {
+    const auto& d = p->descs[i];
+    const MatDev& x = mats[i];
+    const long long rp = p->rp[i];
+    const bool gb = d.g_dtype == DION_DTYPE_BF16;
+    const CUtensorMapDataType gdt = gb ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : F32;
+    const long long gpitch = d.ld_g * (gb ? 2 : 4);
+    float* VTh = reinterpret_cast<float*>(base + p->off_VTh[i]);
+    float* VTl = reinterpret_cast<float*>(base + p->off_VTl[i]);
+    float* UTh = reinterpret_cast<float*>(base + p->off_UTh[i]);
+    float* UTl = reinterpret_cast<float*>(base + p->off_UTl[i]);
+    tcstream::SJob& a = sa[i];
+    std::memset(&a, 0, sizeof a);
+    bool okm = true;
+    okm &= make_map(&a.mG, gdt, d.G, d.n, d.m, gpitch, tcstream::BK, tcstream::BM,
+                    gb ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&a.mR, F32, d.R, d.n, d.m, d.ld_r * 4, tcstream::BK, tcstream::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&a.mBh, F32, VTh, d.n, rp, p->ldt_n[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&a.mBl, F32, VTl, d.n, rp, p->ldt_n[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
+    a.out = x.P; a.ld_out = rp; a.split_stride = 0; a.rows = (int)d.m; a.kdim = (int)d.n;
+    a.ksplit = 1; a.kchunk = (int)(cdiv(d.n, 32) * 32); a.ncb = p->ncb[i]; a.bn = p->bn[i];
+    a.rp = (int)rp; a.g_bf16 = x.g_bf16; a.status = x.status;
+    tcstream::SJob& c = sc[i];
+    std::memset(&c, 0, sizeof c);
+    okm &= make_map(&c.mG, gdt, d.G, d.n, d.m, gpitch, gb ? 64 : 32, tcstream::BK, CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&c.mR, F32, d.R, d.n, d.m, d.ld_r * 4, 32, tcstream::BK, CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&c.mBh, F32, UTh, d.m, rp, p->ldt_m[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&c.mBl, F32, UTl, d.m, rp, p->ldt_m[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!okm) return fail(DION_ERR_CUDA, "matrix %d: cuTensorMapEncodeTiled failed (streaming maps)", i);
+    c.out = p->ksplit[i] > 1 ? x.Wpart : x.W; c.ld_out = rp; c.split_stride = d.n * rp;
+    c.rows = (int)d.n; c.kdim = (int)d.m; c.ksplit = p->ksplit[i]; c.kchunk = p->kchunk[i];
+    c.ncb = p->ncb[i]; c.bn = p->bn[i]; c.rp = (int)rp; c.g_bf16 = x.g_bf16; c.status = x.status;
+    tv[i] = tcsplit::TJob{x.Vin, x.ldvin, VTh, VTl, p->ldt_n[i], d.n, d.r, rp, x.status};
+    tu[i] = tcsplit::TJob{x.U, rp, UTh, UTl, p->ldt_m[i], d.m, d.r, rp, x.status};
+  }
+  put(p->image, p->t_sj_a, sa.data(), sa.size());
+  put(p->image, p->t_sj_c, sc.data(), sc.size());
+  put(p->image, p->t_ts_sa, p->ts_sa.data(), p->ts_sa.size());
+  put(p->image, p->t_ts_sc, p->ts_sc.data(), p->ts_sc.size());
+  put(p->image, p->t_tj_v, tv.data(), tv.size());
+  put(p->image, p->t_tj_u, tu.data(), tu.size());
+  put(p->image, p->t_ts_tv, p->ts_tv.data(), p->ts_tv.size());
+  put(p->image, p->t_ts_tu, p->ts_tu.data(), p->ts_tu.size());
+  put(p->image, p->t_epi, epi.data(), epi.size());
+  put(p->image, p->t_split, sj.data(), sj.size());
+  put(p->image, p->t_ts_epi_tc, p->ts_epi_tc.data(), p->ts_epi_tc.size());
+  put(p->image, p->t_ts_split, p->ts_split.data(), p->ts_split.size());
+  return DION_OK;
 }
 
 dion_status_t check_ws(const dion_plan* p, const void* ws, size_t bytes) {
@@ -335,9 +537,14 @@ dion_status_t launch_orth(const dion_plan* p, unsigned char* base, cudaStream_t 
   const OrthJob* jobs = tab<OrthJob>(p, base, t_jobs);
   const int* tg = tab<int>(p, base, t_ts_gram);
   const int* tt = tab<int>(p, base, t_ts_trmm);
-  for (int pass = 0; pass < 2; ++pass) {
+  // the largest rank of the list decides whether the Cholesky works in shared memory
+  long long rmax = 0;
+  for (int i = 0; i < p->count; ++i) rmax = std::max<long long>(rmax, p->descs[i].r);
+  const size_t chol_smem = (size_t)(rmax * (rmax + 1) * 4);
+  const int use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
+  for (int pass = 0; pass < 3; ++pass) {
     simt::k_gram<<<ts_gram[njob], simt::NT, 0, s>>>(jobs, tg, njob, pass);
-    simt::k_chol_inv<<<njob, simt::CHOL_NT, 0, s>>>(jobs);
+    simt::k_chol_inv<<<njob, simt::CHOL_NT, use_smem ? chol_smem : 0, s>>>(jobs, pass, use_smem);
     simt::k_trmm<<<ts_trmm[njob], simt::NT, 0, s>>>(jobs, tt, njob, pass);
   }
   return cuda_check("orth launch");
@@ -360,12 +567,16 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
   for (int ph = first; ph <= last; ++ph) {
     switch (ph) {
       case 0:
-        if (cudaMemsetAsync(base + p->off_status, 0, 4 * (size_t)cnt, s) != cudaSuccess)
+        if (cudaMemsetAsync(base + p->off_status, 0, 16 * (size_t)cnt, s) != cudaSuccess)
           return cuda_check("status reset");
         st = launch_orth(p, base, s, p->t_jobs_v, p->t_ts_gram_v, p->t_ts_trmm_v, p->ts_gram_v,
                          p->ts_trmm_v, (int)p->dion_idx.size());
         if (st) return st;
-        simt::k_mv<<<p->ts_mv[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_mv), cnt);
+        tcsplit::k_tsplit<<<p->ts_tv[cnt], tcsplit::NT, 0, s>>>(
+            tab<tcsplit::TJob>(p, base, p->t_tj_v), tab<int>(p, base, p->t_ts_tv), cnt);
+        tcstream::k_stream<false><<<std::min(p->ts_sa[cnt], p->num_sms), tcstream::NTHREADS,
+                                    tcstream::SMEM_BYTES, s>>>(tab<tcstream::SJob>(p, base, p->t_sj_a),
+                                                               tab<int>(p, base, p->t_ts_sa), cnt, p->ts_sa[cnt]);
         break;
       case 1:
         st = launch_orth(p, base, s, p->t_jobs_p, p->t_ts_gram_p, p->t_ts_trmm_p, p->ts_gram_p,
@@ -373,7 +584,11 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
         if (st) return st;
         break;
       case 2:
-        simt::k_mtu<<<p->ts_mtu[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_mtu), cnt);
+        tcsplit::k_tsplit<<<p->ts_tu[cnt], tcsplit::NT, 0, s>>>(
+            tab<tcsplit::TJob>(p, base, p->t_tj_u), tab<int>(p, base, p->t_ts_tu), cnt);
+        tcstream::k_stream<true><<<std::min(p->ts_sc[cnt], p->num_sms), tcstream::NTHREADS,
+                                   tcstream::SMEM_BYTES, s>>>(tab<tcstream::SJob>(p, base, p->t_sj_c),
+                                                              tab<int>(p, base, p->t_ts_sc), cnt, p->ts_sc[cnt]);
         if (p->any_split)
           simt::k_wreduce<<<p->ts_wred[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_wred), cnt);
         break;
@@ -386,9 +601,15 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
               mats, tab<int>(p, base, p->t_ts_coln), tab<int>(p, base, p->t_coln_idx),
               (int)p->dion_idx.size());
         break;
-      case 4:
-        simt::k_epilogue<<<p->ts_epi[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_epi), cnt);
+      case 4: {
+        tcsplit::k_split<<<p->ts_split[p->n_split], tcsplit::NT, 0, s>>>(
+            tab<tcsplit::SplitJob>(p, base, p->t_split), tab<int>(p, base, p->t_ts_split), p->n_split);
+        const int tiles = p->ts_epi_tc[cnt];
+        const int grid = std::min(tiles, p->num_sms);
+        tcepi::k_epi<<<grid, tcepi::NTHREADS, tcepi::SMEM_BYTES, s>>>(
+            tab<tcepi::EpiMat>(p, base, p->t_epi), tab<int>(p, base, p->t_ts_epi_tc), cnt, tiles);
         break;
+      }
     }
     st = cuda_check("phase launch");
     if (st) return st;
@@ -456,7 +677,23 @@ dion_status_t dion_plan_upload(dion_plan* plan, void* workspace, size_t ws_bytes
   dion_status_t st = check_ws(plan, workspace, ws_bytes);
   if (st) return st;
   unsigned char* base = static_cast<unsigned char*>(workspace);
-  build_image(plan, base);
+  if (plan->num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&plan->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cuda_check("device query");
+    if (cudaFuncSetAttribute(tcepi::k_epi, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tcepi::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(tcstream::k_stream<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tcstream::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(tcstream::k_stream<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tcstream::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(simt::k_chol_inv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             simt::CHOL_SMEM_MAX) != cudaSuccess)
+      return cuda_check("kernel attributes");
+  }
+  st = build_image(plan, base);
+  if (st) return st;
   if (cudaMemcpyAsync(base + plan->off_tables, plan->image.data(), plan->image.size(),
                       cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return cuda_check("table upload");
@@ -506,13 +743,13 @@ dion_status_t dion_plan_get_status(dion_plan* plan, const void* workspace, size_
 
 int32_t dion_plan_launches_per_step(const dion_plan* plan) {
   if (!plan) return -1;
-  int n = 1;                                   // phase (a)
-  n += plan->dion_idx.empty() ? 0 : 6;         // phase (a), orth(V) of the Dion matrices
-  n += 6;                                      // phase (b): two CholeskyQR rounds
-  n += 1 + (plan->any_split ? 1 : 0);          // phase (c)
-  n += plan->orth_idx.empty() ? 0 : 6;         // phase (d), Orth-Dion matrices
+  int n = 2;                                   // phase (a): V^T split + tensor-core P = M V
+  n += plan->dion_idx.empty() ? 0 : 9;         // phase (a), orth(V) of the Dion matrices
+  n += 9;                                      // phase (b): up to three CholeskyQR rounds
+  n += 2 + (plan->any_split ? 1 : 0);          // phase (c): U^T split, tensor-core W = M^T U, reduce
+  n += plan->orth_idx.empty() ? 0 : 9;         // phase (d), Orth-Dion matrices
   n += plan->dion_idx.empty() ? 0 : 1;         // phase (d), Dion matrices
-  n += 1;                                      // phase (e)
+  n += 2;                                      // phase (e): operand split + tensor-core update
   return n;
 }
 

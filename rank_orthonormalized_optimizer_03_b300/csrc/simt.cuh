@@ -130,11 +130,12 @@ __global__ void __launch_bounds__(NT) k_gram(const OrthJob* __restrict__ jobs,
   const int j = find_job(tstart, njob, blockIdx.x);
   const OrthJob& o = jobs[j];
   if (*o.status & ST_FATAL) return;
+  if (pass == 2 && !*o.flag) return;
   const int local = blockIdx.x - tstart[j];
   const int nt = (int)((o.rp + TN - 1) / TN);
   const int chunk = local / (nt * nt), rem = local % (nt * nt);
   const long long a0 = (long long)(rem / nt) * TM, b0 = (long long)(rem % nt) * TN;
-  const float* A = pass == 0 ? o.A : o.Q;
+  const float* A = pass == 0 ? o.A : (pass == 1 ? o.Q : o.Q2);
   const long long lda = pass == 0 ? o.lda : o.rp;
   const long long ib = (long long)chunk * o.chunk;
   const long long ie = ib + o.chunk < o.rows ? ib + o.chunk : o.rows;
@@ -157,82 +158,128 @@ __global__ void __launch_bounds__(NT) k_gram(const OrthJob* __restrict__ jobs,
   }
 }
 
-// One CTA per job: S = sum of the Gram partials (fixed order); upper Cholesky
-// S = Rc^T Rc with a positive diagonal (stored in the upper triangle of S);
-// T = Rc^{-1} (upper triangular, zero elsewhere, padded to rp x rp).
-// A non-positive or non-finite pivot sets the status bits and stops the job.
+// One CTA per job: S = sum of the Gram partials (fixed order), upper Cholesky
+// S = Rc^T Rc with a positive diagonal, T = Rc^{-1} (upper triangular, zero
+// elsewhere, rp x rp).  S lives in shared memory when it fits (sm != 0), else
+// in the job's global scratch.
+//
+// Pass 0 is where conditioning is decided.  CholeskyQR2 in fp32 needs
+// kappa(A) well below u^{-1/2} ~ 4e3; when the unshifted factorisation breaks
+// down or its pivots imply kappa(A) > ~1e3 (min pivot^2 < 1e-6 max diagonal),
+// the Gram is rebuilt with the shift s = 11 (rows r + r (r + 1)) u ||A||_F^2 of
+// shifted CholeskyQR (Fukaya, Kannan, Nakatsukasa, Zhang, Yamamoto 2020) and
+// the job is flagged for a third pass.  Every factor stays upper triangular
+// with a positive diagonal, so the final Q is still the unique thin-QR factor.
+// A failure in pass 1 or 2 (or of the shifted pass) marks the matrix and
+// leaves it unchanged.
 constexpr int CHOL_NT = 512;
-__global__ void __launch_bounds__(CHOL_NT) k_chol_inv(const OrthJob* __restrict__ jobs) {
-  const OrthJob& o = jobs[blockIdx.x];
-  __shared__ int s_bad;
-  __shared__ float s_piv;
-  if (*o.status & ST_FATAL) return;
+constexpr int CHOL_SMEM_MAX = 200 * 1024;
+
+__device__ void chol_load(const OrthJob& o, float* S, long long lds, float shift, float* s_trace) {
   const int tid = threadIdx.x, nth = blockDim.x;
   const long long r = o.r, rp = o.rp;
-  float* S = o.S;
-  float* T = o.T;
+  float tr = 0.f;
   for (long long e = tid; e < r * r; e += nth) {
     const long long a = e / r, b = e % r;
-    float s = 0.f;
-    for (int c = 0; c < o.nchunk; ++c) s += o.gpart[(long long)c * rp * rp + a * rp + b];
-    S[a * rp + b] = s;
+    float v = 0.f;
+    for (int c = 0; c < o.nchunk; ++c) v += o.gpart[(long long)c * rp * rp + a * rp + b];
+    if (a == b) { tr += v; v += shift; }
+    S[a * lds + b] = v;
   }
-  if (tid == 0) s_bad = 0;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) tr += __shfl_xor_sync(0xffffffffu, tr, off);
+  if ((tid & 31) == 0) s_trace[tid >> 5] = tr;
+  __syncthreads();
+}
+
+// In-place upper Cholesky; returns 0, or the status bits of a failure.
+// *min_piv2 / *max_diag receive the smallest squared pivot and largest diagonal.
+__device__ int chol_factor(float* S, long long lds, long long r, float* s_piv, int* s_bad, float* s_min, float* s_max) {
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
+  if (tid == 0) { *s_bad = 0; *s_min = INFINITY; *s_max = 0.f; }
+  if (tid == 0)
+    for (long long j = 0; j < r; ++j) *s_max = fmaxf(*s_max, S[j * lds + j]);
   __syncthreads();
   for (long long jj = 0; jj < r; ++jj) {
     if (tid == 0) {
-      const float dd = S[jj * rp + jj];
-      if (!isfinite(dd)) s_bad = (int)(ST_BREAKDOWN | ST_NONFINITE);
-      else if (!(dd > 0.f)) s_bad = (int)ST_BREAKDOWN;
-      else { s_piv = sqrtf(dd); S[jj * rp + jj] = s_piv; }
+      const float dd = S[jj * lds + jj];
+      if (!isfinite(dd)) *s_bad = (int)(ST_BREAKDOWN | ST_NONFINITE);
+      else if (!(dd > 0.f)) *s_bad = (int)ST_BREAKDOWN;
+      else { *s_min = fminf(*s_min, dd); *s_piv = sqrtf(dd); S[jj * lds + jj] = *s_piv; }
     }
     __syncthreads();
-    if (s_bad) break;
-    const float inv = 1.f / s_piv;
-    for (long long c = jj + 1 + tid; c < r; c += nth) S[jj * rp + c] *= inv;
+    if (*s_bad) return *s_bad;
+    const float inv = 1.f / *s_piv;
+    for (long long c = jj + 1 + tid; c < r; c += nth) S[jj * lds + c] *= inv;
     __syncthreads();
-    {
-      const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
-      for (long long a = jj + 1 + warp; a < r; a += nwarp) {
-        const float sa = S[jj * rp + a];
-        for (long long c = a + lane; c < r; c += 32) S[a * rp + c] -= sa * S[jj * rp + c];
-      }
+    for (long long a = jj + 1 + warp; a < r; a += nwarp) {
+      const float sa = S[jj * lds + a];
+      for (long long c = a + lane; c < r; c += 32) S[a * lds + c] -= sa * S[jj * lds + c];
     }
     __syncthreads();
   }
-  if (s_bad) {
-    if (tid == 0) atomicOr(o.status, (unsigned)s_bad);
+  return 0;
+}
+
+__global__ void __launch_bounds__(CHOL_NT) k_chol_inv(const OrthJob* __restrict__ jobs, int pass, int use_smem) {
+  extern __shared__ float sm_dyn[];
+  const OrthJob& o = jobs[blockIdx.x];
+  __shared__ int s_bad;
+  __shared__ float s_piv, s_min, s_max;
+  __shared__ float s_trace[CHOL_NT / 32];
+  if (*o.status & ST_FATAL) return;
+  if (pass == 2 && !*o.flag) return;
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const long long r = o.r, rp = o.rp;
+  float* S = use_smem ? sm_dyn : o.S;
+  const long long lds = use_smem ? r + 1 : rp;
+  chol_load(o, S, lds, 0.f, s_trace);
+  int bad = chol_factor(S, lds, r, &s_piv, &s_bad, &s_min, &s_max);
+  if (pass == 0 && (bad || s_min < 1e-6f * s_max)) {
+    float trace = 0.f;
+    for (int w = 0; w < nth / 32; ++w) trace += s_trace[w];
+    const float shift = 11.f * ((float)o.rows * (float)r + (float)r * (float)(r + 1)) * 5.9604645e-8f * trace;
+    __syncthreads();
+    chol_load(o, S, lds, shift, s_trace);
+    bad = chol_factor(S, lds, r, &s_piv, &s_bad, &s_min, &s_max);
+    if (!bad && tid == 0) { *o.flag = 1u; atomicOr(o.status, ST_SHIFTED); }
+  }
+  if (bad) {
+    if (tid == 0) atomicOr(o.status, (unsigned)bad);
     return;
   }
   // T = Rc^{-1}: row a from the bottom up, T[a][c] = -(sum_{k=a+1..c} Rc[a][k] T[k][c]) / Rc[a][a]
+  float* T = o.T;
   for (long long e = tid; e < rp * rp; e += nth) T[e] = 0.f;
   __syncthreads();
   const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
   for (long long a = r - 1; a >= 0; --a) {
-    const float raa = S[a * rp + a];
+    const float raa = S[a * lds + a];
     for (long long c = a + warp; c < r; c += nwarp) {
-      float s = 0.f;
-      for (long long k = a + 1 + lane; k <= c; k += 32) s = fmaf(S[a * rp + k], T[k * rp + c], s);
+      float sum = 0.f;
+      for (long long k = a + 1 + lane; k <= c; k += 32) sum = fmaf(S[a * lds + k], T[k * rp + c], sum);
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (lane == 0) T[a * rp + c] = (c == a) ? 1.f / raa : -s / raa;
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (lane == 0) T[a * rp + c] = (c == a) ? 1.f / raa : -sum / raa;
     }
     __syncthreads();
   }
 }
 
-// out = A T with T upper triangular (rp x rp): pass 0 writes Q = A T1, pass 1
-// writes the job's result = Q T2.
+// out = A T with T upper triangular (rp x rp), one CholeskyQR pass.
 __global__ void __launch_bounds__(NT) k_trmm(const OrthJob* __restrict__ jobs,
                                              const int* __restrict__ tstart, int njob, int pass) {
   __shared__ float As[TK * LDS], Bs[TK * LDS];
   const int j = find_job(tstart, njob, blockIdx.x);
   const OrthJob& o = jobs[j];
   if (*o.status & ST_FATAL) return;
+  const bool three = *o.flag != 0;
+  if (pass == 2 && !three) return;
   const int local = blockIdx.x - tstart[j];
   const int ntc = (int)((o.rp + TN - 1) / TN);
   const long long i0 = (long long)(local / ntc) * TM, c0 = (long long)(local % ntc) * TN;
-  const float* A = pass == 0 ? o.A : o.Q;
+  const float* A = pass == 0 ? o.A : (pass == 1 ? o.Q : o.Q2);
   const long long lda = pass == 0 ? o.lda : o.rp;
   float acc[4][4];
   zero(acc);
@@ -240,9 +287,11 @@ __global__ void __launch_bounds__(NT) k_trmm(const OrthJob* __restrict__ jobs,
   LoadRM lb{o.T, o.rp, o.rp, o.rp};
   const long long ke = (c0 + TN < o.r) ? c0 + TN : o.r;
   tile_acc<true, true>(la, lb, i0, c0, 0, ke, acc, As, Bs);
-  float* out = pass == 0 ? o.Q : o.out;
-  const long long ldo = pass == 0 ? o.rp : o.ldo;
-  const long long ncol = pass == 0 ? o.rp : o.out_cols;
+  // pass 0 -> Q; pass 1 -> the result, or Q2 when a third pass follows; pass 2 -> the result
+  const bool final_pass = pass == 2 || (pass == 1 && !three);
+  float* out = final_pass ? o.out : (pass == 0 ? o.Q : o.Q2);
+  const long long ldo = final_pass ? o.ldo : o.rp;
+  const long long ncol = final_pass ? o.out_cols : o.rp;
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
 #pragma unroll
   for (int u = 0; u < 4; ++u) {

@@ -1,0 +1,373 @@
+// Phases (a) and (c) on the 5th-generation tensor core: the two streaming
+// contractions with the error-feedback buffer M = G + R (junaidaliop.github.io
+// "Orth-Dion", update equations for U and W):
+//
+//     (a)  P = M V       rows i of M, K = n      (TRANS = false)
+//     (c)  W = M^T U     rows j of M^T, K = m    (TRANS = true, K split over CTAs)
+//
+// M is never stored: every CTA streams G and R tiles by TMA into a staging
+// ring, and 8 converter warps form M = G + R in fp32, split it into the two
+// tf32 halves of a 3xTF32 product and write them into the 128-byte-swizzled
+// K-major operand layout the MMA reads (transposing on the way for M^T).  The
+// second operand (V^T or U^T, already split) comes in by TMA.
+//
+// The tensor core's fp32 accumulation truncates: its bias grows with the
+// number of accumulation steps (measured -1e-5 relative per 1024 of K).  So a
+// tile accumulates at most 256 of K in TMEM (a "slice", 2 TMEM buffers) and the
+// converter warps, between conversions, add finished slices into registers in
+// round-to-nearest fp32; the bias then stays near 2e-6.
+//
+// Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..9 converter and
+// slice drain.  One CTA per SM, persistent over (row tile, K range, column
+// block) items of every matrix.
+#pragma once
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace dion {
+namespace tcstream {
+
+using namespace dion::tc;
+
+constexpr int BM = 128;              // output rows per tile (TMEM lanes)
+constexpr int BK = 32;               // K per chunk
+constexpr int SLICE = 8;             // chunks per TMEM slice (256 of K)
+constexpr int OSTAGES = 2;
+constexpr int SSTAGES = 2;
+constexpr int NCONV = 8;             // converter / drain warps
+constexpr int NTHREADS = (2 + NCONV) * 32;
+constexpr int BN_MAX = 192;          // widest column block (TMEM: 2 x 192 <= 512)
+constexpr int HALF_MAX = BN_MAX / 2; // accumulator columns per converter thread
+constexpr uint32_t TMEM_COLS = 512;
+
+constexpr uint32_t A_BYTES = BM * BK * 4;                // 16 KB
+constexpr uint32_t B_BYTES_MAX = BN_MAX * BK * 4;        // 24 KB
+constexpr uint32_t OST_BYTES = 2 * A_BYTES + 2 * B_BYTES_MAX;   // 80 KB
+constexpr uint32_t SST_BYTES = 32768;                    // G (<= 16 KB) | R (16 KB)
+constexpr uint32_t SMEM_BYTES = 1024 + OSTAGES * OST_BYTES + SSTAGES * SST_BYTES + 512;
+
+struct SJob {
+  CUtensorMap mG, mR, mBh, mBl;   // G, R (staging boxes); B operand hi / lo (box 32 x bn)
+  float* out;                     // P (a) or W partials (c)
+  long long ld_out;               // leading dimension of out (rp)
+  long long split_stride;         // elements between the K-range partials of out
+  int rows;                       // output rows: m (a) or n (c)
+  int kdim;                       // K extent: n (a) or m (c)
+  int ksplit, kchunk;             // K ranges (multiple of BK)
+  int ncb, bn;                    // column blocks of width bn (multiple of 32, <= BN_MAX)
+  int rp, g_bf16;
+  unsigned* status;
+  int pad[4];
+};
+static_assert(sizeof(SJob) % 64 == 0, "SJob must keep 64-byte alignment of its maps");
+
+struct Item {
+  int job, row0, ks, c0, k0, nk;
+};
+
+__device__ __forceinline__ Item item_of(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob,
+                                        int t) {
+  Item it;
+  it.job = find_job(tstart, njob, t);
+  const SJob& j = jobs[it.job];
+  int local = t - tstart[it.job];
+  const int cb = local % j.ncb;
+  local /= j.ncb;
+  it.ks = local % j.ksplit;
+  it.row0 = (local / j.ksplit) * BM;
+  it.c0 = cb * j.bn;
+  it.k0 = it.ks * j.kchunk;
+  const int k1 = min(j.kdim, it.k0 + j.kchunk);
+  it.nk = (k1 - it.k0 + BK - 1) / BK;
+  return it;
+}
+
+__device__ __forceinline__ bool skip(const SJob& j) { return (*j.status & ST_FATAL) != 0; }
+
+// Drain one finished TMEM slice (columns [col0, col0 + half) of this thread's
+// lane) into the register accumulator.
+__device__ __forceinline__ void drain_add(uint32_t taddr, int half, float (&acc)[HALF_MAX]) {
+#pragma unroll
+  for (int cb = 0; cb < HALF_MAX / 16; ++cb) {
+    if (cb * 16 < half) {
+      float v[16];
+      tmem_ld16(taddr + cb * 16, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc[cb * 16 + k] += v[k];
+    }
+  }
+}
+
+template <bool TRANS>
+__global__ void __launch_bounds__(NTHREADS, 1)
+k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob, int nitems) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* ost = smem;
+  unsigned char* sst = smem + OSTAGES * OST_BYTES;
+  uint64_t* bars = (uint64_t*)(sst + SSTAGES * SST_BYTES);
+  uint64_t* o_full = bars;                 // B bytes (TMA) + NCONV converter arrivals
+  uint64_t* o_empty = o_full + OSTAGES;    // MMA commit
+  uint64_t* s_full = o_empty + OSTAGES;    // staging bytes (TMA)
+  uint64_t* s_empty = s_full + SSTAGES;    // NCONV converter arrivals
+  uint64_t* acc_full = s_empty + SSTAGES;  // MMA commit per slice
+  uint64_t* acc_empty = acc_full + 2;      // NCONV drain arrivals
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tslot = (uint32_t*)(drain + 1);
+  volatile int* abort_flag = (volatile int*)(tslot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < OSTAGES; ++i) { mbar_init(&o_full[i], 1 + NCONV); mbar_init(&o_empty[i], 1); }
+    for (int i = 0; i < SSTAGES; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], NCONV); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], NCONV); }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) { tmem_alloc(tslot, TMEM_COLS); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  int failed = -1;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int os = 0, ss = 0; uint32_t oph = 0, sph = 0;
+    uint32_t olast[OSTAGES] = {0, 0}, slast[SSTAGES] = {0, 0};
+    bool oused[OSTAGES] = {false, false}, sused[SSTAGES] = {false, false};
+    for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
+      const Item it = item_of(jobs, tstart, njob, t);
+      const SJob& j = jobs[it.job];
+      if (skip(j)) continue;
+      const uint32_t gbytes = BM * BK * (j.g_bf16 ? 2 : 4);
+      const uint32_t bbytes = j.bn * BK * 4;
+      for (int kc = 0; kc < it.nk; ++kc) {
+        const int k = it.k0 + kc * BK;
+        // staging: G and R tiles of M
+        if (!mbar_wait(&s_empty[ss], sph ^ 1, abort_flag)) { failed = it.job; goto prod_done; }
+        mbar_arrive_expect_tx(&s_full[ss], gbytes + BM * BK * 4);
+        {
+          unsigned char* gdst = sst + ss * SST_BYTES;
+          unsigned char* rdst = gdst + 16384;
+          if (!TRANS) {
+            tma_load_2d(gdst, &j.mG, &s_full[ss], k, it.row0);
+            tma_load_2d(rdst, &j.mR, &s_full[ss], k, it.row0);
+          } else {
+            // rows k..k+31 of M, columns row0..row0+127 (boxes of 128 bytes per row)
+            const int gbox = j.g_bf16 ? 64 : 32;
+            for (int b = 0; b < BM / gbox; ++b)
+              tma_load_2d(gdst + b * 4096, &j.mG, &s_full[ss], it.row0 + b * gbox, k);
+            for (int b = 0; b < BM / 32; ++b)
+              tma_load_2d(rdst + b * 4096, &j.mR, &s_full[ss], it.row0 + b * 32, k);
+          }
+        }
+        sused[ss] = true; slast[ss] = sph;
+        if (++ss == SSTAGES) { ss = 0; sph ^= 1; }
+        // operand stage: the B half (already split), bn rows
+        if (!mbar_wait(&o_empty[os], oph ^ 1, abort_flag)) { failed = it.job; goto prod_done; }
+        mbar_arrive_expect_tx(&o_full[os], 2 * bbytes);
+        {
+          unsigned char* b = ost + os * OST_BYTES + 2 * A_BYTES;
+          tma_load_2d(b, &j.mBh, &o_full[os], k, it.c0);
+          tma_load_2d(b + B_BYTES_MAX, &j.mBl, &o_full[os], k, it.c0);
+        }
+        oused[os] = true; olast[os] = oph;
+        if (++os == OSTAGES) { os = 0; oph ^= 1; }
+      }
+    }
+  prod_done:
+    if (*abort_flag) {
+      for (int i = 0; i < SSTAGES; ++i) if (sused[i]) mbar_wait_drain(&s_full[i], slast[i]);
+      for (int i = 0; i < OSTAGES; ++i) if (oused[i]) mbar_wait_drain(&o_full[i], olast[i]);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    int os = 0; uint32_t oph = 0; int b = 0; uint32_t aph[2] = {0, 0};
+    bool issued = false;
+    for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
+      const Item it = item_of(jobs, tstart, njob, t);
+      const SJob& j = jobs[it.job];
+      if (skip(j)) continue;
+      const uint32_t idesc = idesc_tf32(BM, j.bn);
+      for (int kc = 0; kc < it.nk; ++kc) {
+        if (kc % SLICE == 0) {
+          if (!mbar_wait(&acc_empty[b], aph[b] ^ 1, abort_flag)) { failed = it.job; goto mma_done; }
+          tc_fence_after();
+        }
+        if (!mbar_wait(&o_full[os], oph, abort_flag)) { failed = it.job; goto mma_done; }
+        tc_fence_after();
+        const uint32_t d = tmem + b * BN_MAX;
+        const uint32_t ah = smem_u32(ost + os * OST_BYTES), al = ah + A_BYTES;
+        const uint32_t bh = ah + 2 * A_BYTES, bl = bh + B_BYTES_MAX;
+#pragma unroll
+        for (int kk = 0; kk < BK / 8; ++kk) {
+          const uint32_t o = kk * 32;
+          mma_tf32(d, sdesc_k_sw128(al + o), sdesc_k_sw128(bh + o), idesc, ((kc % SLICE) | kk) != 0);
+          mma_tf32(d, sdesc_k_sw128(ah + o), sdesc_k_sw128(bl + o), idesc, 1);
+          mma_tf32(d, sdesc_k_sw128(ah + o), sdesc_k_sw128(bh + o), idesc, 1);
+        }
+        issued = true;
+        mma_commit(&o_empty[os]);
+        if (++os == OSTAGES) { os = 0; oph ^= 1; }
+        if (kc % SLICE == SLICE - 1 || kc == it.nk - 1) {
+          mma_commit(&acc_full[b]);
+          aph[b] ^= 1; b ^= 1;
+        }
+      }
+    }
+  mma_done:
+    if (*abort_flag && issued) { mma_commit(drain); mbar_wait_drain(drain, 0); }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ converters + slice drain
+    const int cw = warp - 2;                 // 0..7
+    const int quarter = warp & 3;            // TMEM lane quarter of this warp
+    const int h = cw >> 2;                   // K half (conversion) and column half (drain)
+    const int row = quarter * 32 + lane;     // output row within the tile (TMEM lane)
+    int os = 0, ss = 0; uint32_t oph = 0, sph = 0;
+    int b = 0; uint32_t aph[2] = {0, 0};
+    float acc[HALF_MAX];
+    for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
+      const Item it = item_of(jobs, tstart, njob, t);
+      const SJob& j = jobs[it.job];
+      if (skip(j)) continue;
+      const int half = j.bn >> 1;
+      const int nslices = (it.nk + SLICE - 1) / SLICE;
+      int drained = 0;
+#pragma unroll
+      for (int k = 0; k < HALF_MAX; ++k) acc[k] = 0.f;
+      bool ok = true;
+      for (int kc = 0; kc < it.nk && ok; ++kc) {
+        // before the first chunk of slice s + 2, fold slice s into the registers
+        if (kc % SLICE == 0 && kc / SLICE >= 2) {
+          if (!mbar_wait_warp(&acc_full[b], aph[b], abort_flag)) { failed = it.job; ok = false; break; }
+          tc_fence_after();
+          drain_add(tmem + ((uint32_t)(quarter * 32) << 16) + b * BN_MAX + h * half, half, acc);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[b]);
+          aph[b] ^= 1; b ^= 1; ++drained;
+        }
+        if (!mbar_wait_warp(&s_full[ss], sph, abort_flag)) { failed = it.job; ok = false; break; }
+        if (!mbar_wait_warp(&o_empty[os], oph ^ 1, abort_flag)) { failed = it.job; ok = false; break; }
+        const unsigned char* gsrc = sst + ss * SST_BYTES;
+        const unsigned char* rsrc = gsrc + 16384;
+        unsigned char* ahp = ost + os * OST_BYTES;
+        unsigned char* alp = ahp + A_BYTES;
+        if (!TRANS) {
+          // row `row` of M, K elements [16h, 16h + 16) of this chunk
+          float mv[16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int ch = 4 * h + c;
+            const float4 r = *reinterpret_cast<const float4*>(rsrc + row * 128 + (((ch ^ row) & 7) << 4));
+            mv[4 * c] = r.x; mv[4 * c + 1] = r.y; mv[4 * c + 2] = r.z; mv[4 * c + 3] = r.w;
+          }
+          if (j.g_bf16) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int ch = 2 * h + c;   // 64-byte rows, 64-byte swizzle
+              const uint4 v = *reinterpret_cast<const uint4*>(gsrc + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4));
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                mv[c * 8 + 2 * k] += __uint_as_float(w[k] << 16);
+                mv[c * 8 + 2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int ch = 4 * h + c;
+              const float4 g = *reinterpret_cast<const float4*>(gsrc + row * 128 + (((ch ^ row) & 7) << 4));
+              mv[4 * c] += g.x; mv[4 * c + 1] += g.y; mv[4 * c + 2] += g.z; mv[4 * c + 3] += g.w;
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float4 hi, lo;
+            split_tf32(mv[4 * c], hi.x, lo.x);
+            split_tf32(mv[4 * c + 1], hi.y, lo.y);
+            split_tf32(mv[4 * c + 2], hi.z, lo.z);
+            split_tf32(mv[4 * c + 3], hi.w, lo.w);
+            const uint32_t off = sw128_off(row, 16 * h + 4 * c);
+            *reinterpret_cast<float4*>(ahp + off) = hi;
+            *reinterpret_cast<float4*>(alp + off) = lo;
+          }
+        } else {
+          // column `row` of M (row of M^T), K = rows [16h, 16h + 16) of this chunk
+          const int jb = row >> 5, jj = row & 31;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float mv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = 16 * h + 4 * c + e;
+              float v = *reinterpret_cast<const float*>(rsrc + jb * 4096 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4) +
+                                                        ((jj & 3) << 2));
+              if (j.g_bf16) {
+                const int gb = row >> 6, gj = row & 63;
+                const uint16_t gv = *reinterpret_cast<const uint16_t*>(
+                    gsrc + gb * 4096 + i * 128 + ((((gj >> 3) ^ i) & 7) << 4) + ((gj & 7) << 1));
+                v += __uint_as_float((uint32_t)gv << 16);
+              } else {
+                v += *reinterpret_cast<const float*>(gsrc + jb * 4096 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4) +
+                                                     ((jj & 3) << 2));
+              }
+              mv[e] = v;
+            }
+            float4 hi, lo;
+            split_tf32(mv[0], hi.x, lo.x);
+            split_tf32(mv[1], hi.y, lo.y);
+            split_tf32(mv[2], hi.z, lo.z);
+            split_tf32(mv[3], hi.w, lo.w);
+            const uint32_t off = sw128_off(row, 16 * h + 4 * c);
+            *reinterpret_cast<float4*>(ahp + off) = hi;
+            *reinterpret_cast<float4*>(alp + off) = lo;
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&s_empty[ss]);
+          mbar_arrive(&o_full[os]);
+        }
+        if (++ss == SSTAGES) { ss = 0; sph ^= 1; }
+        if (++os == OSTAGES) { os = 0; oph ^= 1; }
+      }
+      // the last (up to two) slices
+      while (ok && drained < nslices) {
+        if (!mbar_wait_warp(&acc_full[b], aph[b], abort_flag)) { failed = it.job; ok = false; break; }
+        tc_fence_after();
+        drain_add(tmem + ((uint32_t)(quarter * 32) << 16) + b * BN_MAX + h * half, half, acc);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[b]);
+        aph[b] ^= 1; b ^= 1; ++drained;
+      }
+      if (!ok) break;
+      const int grow = it.row0 + row;
+      if (grow < j.rows) {
+        float* dst = j.out + (long long)it.ks * j.split_stride + (long long)grow * j.ld_out + it.c0 + h * half;
+#pragma unroll
+        for (int cb = 0; cb < HALF_MAX / 16; ++cb)
+          if (cb * 16 < half && it.c0 + h * half + cb * 16 < j.rp) {
+#pragma unroll
+            for (int k = 0; k < 16; k += 4)
+              *reinterpret_cast<float4*>(dst + cb * 16 + k) =
+                  make_float4(acc[cb * 16 + k], acc[cb * 16 + k + 1], acc[cb * 16 + k + 2], acc[cb * 16 + k + 3]);
+          }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, TMEM_COLS); }
+  if (failed >= 0) atomicOr(jobs[failed].status, ST_TIMEOUT);
+}
+
+}  // namespace tcstream
+}  // namespace dion

@@ -17,7 +17,9 @@ LIB_PATH = os.path.join(PKG, "libdion.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "dion.h")
 
 DION_OK, DION_ERR_INVALID_ARG, DION_ERR_CUDA, DION_ERR_WORKSPACE, DION_ERR_UNSUPPORTED = range(5)
-DION_MAT_OK, DION_MAT_CHOL_BREAKDOWN, DION_MAT_NONFINITE = 0, 1, 2
+DION_MAT_OK, DION_MAT_CHOL_BREAKDOWN, DION_MAT_NONFINITE, DION_MAT_TIMEOUT, DION_MAT_SHIFTED = 0, 1, 2, 4, 8
+# bits that mean the matrix was not updated (DION_MAT_SHIFTED is informational)
+FATAL = DION_MAT_CHOL_BREAKDOWN | DION_MAT_NONFINITE | DION_MAT_TIMEOUT
 VARIANT = {"dion": 0, "orth": 1}
 DTYPE_F32, DTYPE_BF16 = 0, 1
 BUF_P, BUF_U, BUF_W = 0, 1, 2
@@ -180,6 +182,10 @@ class Plan:
 
     def set_hparams(self, idx: int, eta: float, beta: float):
         check(lib().dion_plan_set_hparams(self._plan, idx, eta, beta), "dion_plan_set_hparams")
+
+    def failures(self, stream=None) -> List[int]:
+        """Per-matrix status words restricted to the bits that mean "not updated"."""
+        return [v & FATAL for v in self.status(stream)]
 
     def status(self, stream=None) -> List[int]:
         out = (ctypes.c_uint32 * self.count)()
