@@ -56,6 +56,8 @@ struct OrthJob {
   float* gpart;        // nchunk x rp x rp Gram partial sums
   float* S;            // rp x rp Gram / Cholesky factor
   float* T;            // rp x rp inverse of the Cholesky factor
+  float* Tt_hi;        // rp x rp: T^T split into tf32 halves (B operand of the tensor-core A T)
+  float* Tt_lo;
   long long rows, r, rp;
   int nchunk;          // row chunks of the Gram reduction
   int chunk;           // rows per chunk

@@ -16,6 +16,7 @@
 #include "tc_epilogue.cuh"
 #include "tc_split.cuh"
 #include "tc_stream.cuh"
+#include "tc_gram.cuh"
 
 using namespace dion;
 
@@ -80,6 +81,14 @@ struct dion_plan {
   std::vector<size_t> off_VTh, off_VTl, off_UTh, off_UTl;
   size_t t_sj_a = 0, t_sj_c = 0, t_ts_sa = 0, t_ts_sc = 0, t_tj_v = 0, t_tj_u = 0, t_ts_tv = 0, t_ts_tu = 0;
   std::vector<int> ts_sa, ts_sc, ts_tv, ts_tu;
+  // tensor-core orth(): per list (0 = P, 1 = W, 2 = V) and pass, Gram and A T jobs
+  bool tc_orth = false;
+  std::vector<size_t> off_Tth, off_Ttl;
+  size_t t_gj[3][3] = {}, t_tj[3][3] = {}, t_ts_g[3] = {}, t_ts_t[3] = {};
+  std::vector<int> ts_g[3], ts_t[3], ts_gred[3];
+  size_t t_ts_gred[3] = {};
+  size_t t_vcopy = 0, t_ts_vcopy = 0;
+  std::vector<int> ts_vcopy;
 
   std::vector<unsigned char> image;
   const void* uploaded_ws = nullptr;
@@ -180,9 +189,18 @@ void layout(dion_plan* p) {
     *ch = (int)c;
     *nch = (int)cdiv(rows, c);
   };
+  p->tc_orth = true;
+  for (int i = 0; i < cnt; ++i) p->tc_orth = p->tc_orth && p->rp[i] <= tcgram::RP_MAX;
   for (int i = 0; i < cnt; ++i) {
-    chunks(p->descs[i].m, &p->nchunk_p[i], &p->chunk_p[i]);
-    chunks(p->descs[i].n, &p->nchunk_w[i], &p->chunk_w[i]);
+    if (p->tc_orth) {
+      // tensor-core Gram: one partial per 256 rows
+      p->chunk_p[i] = p->chunk_w[i] = tcgram::CHUNK_ROWS;
+      p->nchunk_p[i] = (int)cdiv(p->descs[i].m, tcgram::CHUNK_ROWS);
+      p->nchunk_w[i] = (int)cdiv(p->descs[i].n, tcgram::CHUNK_ROWS);
+    } else {
+      chunks(p->descs[i].m, &p->nchunk_p[i], &p->chunk_p[i]);
+      chunks(p->descs[i].n, &p->nchunk_w[i], &p->chunk_w[i]);
+    }
   }
 
   // ---- tile prefix sums
@@ -225,6 +243,28 @@ void layout(dion_plan* p) {
   prefix(p->ts_sc, all, [&](int i) { return cdiv(D(i).n, tcstream::BM) * (long long)p->ksplit[i] * p->ncb[i]; });
   prefix(p->ts_tv, all, [&](int i) { return cdiv(D(i).n, 32) * cdiv(p->rp[i], 32); });
   prefix(p->ts_tu, all, [&](int i) { return cdiv(D(i).m, 32) * cdiv(p->rp[i], 32); });
+  {
+    const std::vector<int>* lists[3] = {&all, &p->orth_idx, &p->dion_idx};
+    for (int L = 0; L < 3; ++L) {
+      const size_t nj = std::max<size_t>(1, lists[L]->size());
+      prefix(p->ts_g[L], *lists[L], [&](int i) { return cdiv(L == 0 ? D(i).m : D(i).n, tcgram::CHUNK_ROWS); });
+      prefix(p->ts_t[L], *lists[L], [&](int i) {
+        return cdiv(L == 0 ? D(i).m : D(i).n, tcstream::BM) * p->ncb[i]; });
+      prefix(p->ts_gred[L], *lists[L], [&](int i) { return cdiv(p->rp[i] * p->rp[i], simt::GRED_ELEMS); });
+      for (int ps = 0; ps < 3; ++ps) {
+        p->t_gj[L][ps] = take(sizeof(tcgram::GJob) * nj);
+        p->t_tj[L][ps] = take(sizeof(tcstream::SJob) * nj);
+      }
+    }
+    prefix(p->ts_vcopy, p->dion_idx, [&](int i) { return cdiv(D(i).n * p->rp[i], tcsplit::ELEMS_PER_CTA); });
+    p->t_vcopy = take(sizeof(tcsplit::SplitJob) * std::max<size_t>(1, p->dion_idx.size()));
+    for (int L = 0; L < 3; ++L) {
+      p->t_ts_gred[L] = take(4 * p->ts_gred[L].size());
+      p->t_ts_g[L] = take(4 * p->ts_g[L].size());
+      p->t_ts_t[L] = take(4 * p->ts_t[L].size());
+    }
+    p->t_ts_vcopy = take(4 * p->ts_vcopy.size());
+  }
   p->t_sj_a = take(sizeof(tcstream::SJob) * cnt);
   p->t_sj_c = take(sizeof(tcstream::SJob) * cnt);
   p->t_epi = take(sizeof(tcepi::EpiMat) * cnt);
@@ -277,6 +317,11 @@ void layout(dion_plan* p) {
     p->off_S[i] = region(4 * (size_t)(rp * rp));
     p->off_T[i] = region(4 * (size_t)(rp * rp));
     p->off_Vo[i] = region(D(i).variant == DION_VARIANT_DION ? 4 * (size_t)(n * rp) : 4);
+  }
+  p->off_Tth.resize(cnt); p->off_Ttl.resize(cnt);
+  for (int i = 0; i < cnt; ++i) {
+    p->off_Tth[i] = region(4 * (size_t)(p->rp[i] * p->rp[i]));
+    p->off_Ttl[i] = region(4 * (size_t)(p->rp[i] * p->rp[i]));
   }
   p->off_VTh.resize(cnt); p->off_VTl.resize(cnt); p->off_UTh.resize(cnt); p->off_UTl.resize(cnt);
   for (int i = 0; i < cnt; ++i) {
@@ -372,6 +417,8 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
       o.gpart = reinterpret_cast<float*>(base + p->off_gpart[i]);
       o.S = reinterpret_cast<float*>(base + p->off_S[i]);
       o.T = reinterpret_cast<float*>(base + p->off_T[i]);
+      o.Tt_hi = p->tc_orth ? reinterpret_cast<float*>(base + p->off_Tth[i]) : nullptr;
+      o.Tt_lo = p->tc_orth ? reinterpret_cast<float*>(base + p->off_Ttl[i]) : nullptr;
       o.rows = rows; o.r = x.r; o.rp = x.rp;
       o.nchunk = nch; o.chunk = ch;
       o.status = x.status;
@@ -394,7 +441,7 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     const MatDev& x = mats[i];
     OrthJob& o = jv[k];
     o = jp[i];
-    o.A = x.V; o.lda = x.r; o.rows = x.n;
+    o.A = p->tc_orth ? x.Vin : x.V; o.lda = p->tc_orth ? x.rp : x.r; o.rows = x.n;
     o.out = const_cast<float*>(x.Vin); o.ldo = x.rp; o.out_cols = x.rp;
     o.nchunk = p->nchunk_w[i]; o.chunk = p->chunk_w[i];
     o.flag = status + 3 * cnt + i;
@@ -479,7 +526,8 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     okm &= make_map(&a.mBl, F32, VTl, d.n, rp, p->ldt_n[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
     a.out = x.P; a.ld_out = rp; a.split_stride = 0; a.rows = (int)d.m; a.kdim = (int)d.n;
     a.ksplit = 1; a.kchunk = (int)(cdiv(d.n, 32) * 32); a.ncb = p->ncb[i]; a.bn = p->bn[i];
-    a.rp = (int)rp; a.g_bf16 = x.g_bf16; a.status = x.status;
+    a.rp = (int)rp; a.gmode = gb ? tcstream::G_BF16 : tcstream::G_F32; a.status = x.status;
+    a.pass = -1; a.out_cols = (int)rp;
     tcstream::SJob& c = sc[i];
     std::memset(&c, 0, sizeof c);
     okm &= make_map(&c.mG, gdt, d.G, d.n, d.m, gpitch, gb ? 64 : 32, tcstream::BK, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -489,9 +537,57 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     if (!okm) return fail(DION_ERR_CUDA, "matrix %d: cuTensorMapEncodeTiled failed (streaming maps)", i);
     c.out = p->ksplit[i] > 1 ? x.Wpart : x.W; c.ld_out = rp; c.split_stride = d.n * rp;
     c.rows = (int)d.n; c.kdim = (int)d.m; c.ksplit = p->ksplit[i]; c.kchunk = p->kchunk[i];
-    c.ncb = p->ncb[i]; c.bn = p->bn[i]; c.rp = (int)rp; c.g_bf16 = x.g_bf16; c.status = x.status;
+    c.ncb = p->ncb[i]; c.bn = p->bn[i]; c.rp = (int)rp; c.gmode = gb ? tcstream::G_BF16 : tcstream::G_F32;
+    c.status = x.status; c.pass = -1; c.out_cols = (int)rp;
     tv[i] = tcsplit::TJob{x.Vin, x.ldvin, VTh, VTl, p->ldt_n[i], d.n, d.r, rp, x.status};
     tu[i] = tcsplit::TJob{x.U, rp, UTh, UTl, p->ldt_m[i], d.m, d.r, rp, x.status};
+  }
+  // ---- tensor-core orth(): Gram and A T jobs per list and pass
+  if (p->tc_orth) {
+    const std::vector<OrthJob>* ojs[3] = {&jp, &jw, &jv};
+    const std::vector<int>* lists[3] = {nullptr, &p->orth_idx, &p->dion_idx};
+    for (int L = 0; L < 3; ++L) {
+      const size_t nj = L == 0 ? (size_t)cnt : lists[L]->size();
+      for (int ps = 0; ps < 3; ++ps) {
+        std::vector<tcgram::GJob> gj(std::max<size_t>(1, nj));
+        std::vector<tcstream::SJob> tj(std::max<size_t>(1, nj));
+        for (size_t k = 0; k < nj; ++k) {
+          const int i = L == 0 ? (int)k : (*lists[L])[k];
+          const OrthJob& o = (*ojs[L])[k];
+          const long long rp = p->rp[i];
+          const float* src = ps == 0 ? o.A : (ps == 1 ? o.Q : o.Q2);
+          const long long lds = ps == 0 ? o.lda : rp;
+          tcgram::GJob& g = gj[k];
+          std::memset(&g, 0, sizeof g);
+          bool okm = make_map(&g.mA, F32, src, rp, o.rows, lds * 4, 32, tcgram::BK, CU_TENSOR_MAP_SWIZZLE_128B);
+          g.gpart = o.gpart; g.rows = (int)o.rows; g.rp = (int)rp;
+          g.nchunk = (int)cdiv(o.rows, tcgram::CHUNK_ROWS); g.pass = ps; g.flag = o.flag; g.status = o.status;
+          tcstream::SJob& t = tj[k];
+          std::memset(&t, 0, sizeof t);
+          okm &= make_map(&t.mR, F32, src, rp, o.rows, lds * 4, tcstream::BK, tcstream::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+          okm &= make_map(&t.mBh, F32, o.Tt_hi, rp, rp, rp * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
+          okm &= make_map(&t.mBl, F32, o.Tt_lo, rp, rp, rp * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
+          if (!okm) return fail(DION_ERR_CUDA, "matrix %d: cuTensorMapEncodeTiled failed (orth maps)", i);
+          t.out = o.out; t.ld_out = o.ldo; t.split_stride = 0; t.q1 = o.Q; t.q2 = o.Q2; t.flag = o.flag;
+          t.pass = ps; t.out_cols = (int)o.out_cols; t.rows = (int)o.rows; t.kdim = (int)rp;
+          t.ksplit = 1; t.kchunk = (int)rp; t.ncb = p->ncb[i]; t.bn = p->bn[i]; t.rp = (int)rp;
+          t.gmode = tcstream::G_NONE; t.status = o.status;
+        }
+        put(p->image, p->t_gj[L][ps], gj.data(), gj.size());
+        put(p->image, p->t_tj[L][ps], tj.data(), tj.size());
+      }
+      put(p->image, p->t_ts_g[L], p->ts_g[L].data(), p->ts_g[L].size());
+      put(p->image, p->t_ts_gred[L], p->ts_gred[L].data(), p->ts_gred[L].size());
+      put(p->image, p->t_ts_t[L], p->ts_t[L].data(), p->ts_t[L].size());
+    }
+    std::vector<tcsplit::SplitJob> vc(std::max<size_t>(1, p->dion_idx.size()));
+    for (size_t k = 0; k < p->dion_idx.size(); ++k) {
+      const int i = p->dion_idx[k];
+      vc[k] = tcsplit::SplitJob{mats[i].V, p->descs[i].r, const_cast<float*>(mats[i].Vin), nullptr, p->rp[i],
+                                p->descs[i].n, p->descs[i].r, mats[i].status};
+    }
+    put(p->image, p->t_vcopy, vc.data(), vc.size());
+    put(p->image, p->t_ts_vcopy, p->ts_vcopy.data(), p->ts_vcopy.size());
   }
   put(p->image, p->t_sj_a, sa.data(), sa.size());
   put(p->image, p->t_sj_c, sc.data(), sc.size());
@@ -544,8 +640,29 @@ dion_status_t launch_orth(const dion_plan* p, unsigned char* base, cudaStream_t 
   const int use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
   for (int pass = 0; pass < 3; ++pass) {
     simt::k_gram<<<ts_gram[njob], simt::NT, 0, s>>>(jobs, tg, njob, pass);
-    simt::k_chol_inv<<<njob, simt::CHOL_NT, use_smem ? chol_smem : 0, s>>>(jobs, pass, use_smem);
+    simt::k_chol_inv<<<njob, simt::CHOL_NT, use_smem ? chol_smem : 0, s>>>(jobs, pass, use_smem, 0);
     simt::k_trmm<<<ts_trmm[njob], simt::NT, 0, s>>>(jobs, tt, njob, pass);
+  }
+  return cuda_check("orth launch");
+}
+
+// orth() of list L (0: P, 1: W, 2: V) on the tensor core: up to three CholeskyQR
+// passes of (Gram partials, Cholesky + inverse, A T).
+dion_status_t launch_orth_tc(const dion_plan* p, unsigned char* base, cudaStream_t s, int L, size_t t_jobs, int njob) {
+  if (njob == 0) return DION_OK;
+  const OrthJob* jobs = tab<OrthJob>(p, base, t_jobs);
+  long long rmax = 0;
+  for (int i = 0; i < p->count; ++i) rmax = std::max<long long>(rmax, p->descs[i].r);
+  const size_t chol_smem = (size_t)(rmax * (rmax + 1) * 4);
+  const int use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
+  const int ng = p->ts_g[L][njob], nt = p->ts_t[L][njob];
+  for (int ps = 0; ps < 3; ++ps) {
+    tcgram::k_gram<<<std::min(ng, p->num_sms), tcgram::NTHREADS, tcgram::SMEM_BYTES, s>>>(
+        tab<tcgram::GJob>(p, base, p->t_gj[L][ps]), tab<int>(p, base, p->t_ts_g[L]), njob, ng);
+    simt::k_gram_reduce<<<p->ts_gred[L][njob], 256, 0, s>>>(jobs, tab<int>(p, base, p->t_ts_gred[L]), njob, ps);
+    simt::k_chol_inv<<<njob, simt::CHOL_NT, use_smem ? chol_smem : 0, s>>>(jobs, ps, use_smem, 1);
+    tcstream::k_stream<false><<<std::min(nt, p->num_sms), tcstream::NTHREADS, tcstream::SMEM_BYTES, s>>>(
+        tab<tcstream::SJob>(p, base, p->t_tj[L][ps]), tab<int>(p, base, p->t_ts_t[L]), njob, nt);
   }
   return cuda_check("orth launch");
 }
@@ -569,8 +686,17 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
       case 0:
         if (cudaMemsetAsync(base + p->off_status, 0, 16 * (size_t)cnt, s) != cudaSuccess)
           return cuda_check("status reset");
-        st = launch_orth(p, base, s, p->t_jobs_v, p->t_ts_gram_v, p->t_ts_trmm_v, p->ts_gram_v,
-                         p->ts_trmm_v, (int)p->dion_idx.size());
+        if (p->tc_orth) {
+          if (!p->dion_idx.empty()) {
+            tcsplit::k_split<<<p->ts_vcopy[p->dion_idx.size()], tcsplit::NT, 0, s>>>(
+                tab<tcsplit::SplitJob>(p, base, p->t_vcopy), tab<int>(p, base, p->t_ts_vcopy),
+                (int)p->dion_idx.size());
+          }
+          st = launch_orth_tc(p, base, s, 2, p->t_jobs_v, (int)p->dion_idx.size());
+        } else {
+          st = launch_orth(p, base, s, p->t_jobs_v, p->t_ts_gram_v, p->t_ts_trmm_v, p->ts_gram_v,
+                           p->ts_trmm_v, (int)p->dion_idx.size());
+        }
         if (st) return st;
         tcsplit::k_tsplit<<<p->ts_tv[cnt], tcsplit::NT, 0, s>>>(
             tab<tcsplit::TJob>(p, base, p->t_tj_v), tab<int>(p, base, p->t_ts_tv), cnt);
@@ -579,8 +705,9 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
                                                                tab<int>(p, base, p->t_ts_sa), cnt, p->ts_sa[cnt]);
         break;
       case 1:
-        st = launch_orth(p, base, s, p->t_jobs_p, p->t_ts_gram_p, p->t_ts_trmm_p, p->ts_gram_p,
-                         p->ts_trmm_p, cnt);
+        st = p->tc_orth ? launch_orth_tc(p, base, s, 0, p->t_jobs_p, cnt)
+                        : launch_orth(p, base, s, p->t_jobs_p, p->t_ts_gram_p, p->t_ts_trmm_p, p->ts_gram_p,
+                                      p->ts_trmm_p, cnt);
         if (st) return st;
         break;
       case 2:
@@ -593,8 +720,9 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
           simt::k_wreduce<<<p->ts_wred[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_wred), cnt);
         break;
       case 3:
-        st = launch_orth(p, base, s, p->t_jobs_w, p->t_ts_gram_w, p->t_ts_trmm_w, p->ts_gram_w,
-                         p->ts_trmm_w, (int)p->orth_idx.size());
+        st = p->tc_orth ? launch_orth_tc(p, base, s, 1, p->t_jobs_w, (int)p->orth_idx.size())
+                        : launch_orth(p, base, s, p->t_jobs_w, p->t_ts_gram_w, p->t_ts_trmm_w, p->ts_gram_w,
+                                      p->ts_trmm_w, (int)p->orth_idx.size());
         if (st) return st;
         if (!p->dion_idx.empty())
           simt::k_colnorm<<<p->ts_coln[p->dion_idx.size()], simt::NT, 0, s>>>(
@@ -689,7 +817,9 @@ dion_status_t dion_plan_upload(dion_plan* plan, void* workspace, size_t ws_bytes
         cudaFuncSetAttribute(tcstream::k_stream<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)tcstream::SMEM_BYTES) != cudaSuccess ||
         cudaFuncSetAttribute(simt::k_chol_inv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             simt::CHOL_SMEM_MAX) != cudaSuccess)
+                             simt::CHOL_SMEM_MAX) != cudaSuccess ||
+        cudaFuncSetAttribute(tcgram::k_gram, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tcgram::SMEM_BYTES) != cudaSuccess)
       return cuda_check("kernel attributes");
   }
   st = build_image(plan, base);
@@ -744,10 +874,11 @@ dion_status_t dion_plan_get_status(dion_plan* plan, const void* workspace, size_
 int32_t dion_plan_launches_per_step(const dion_plan* plan) {
   if (!plan) return -1;
   int n = 2;                                   // phase (a): V^T split + tensor-core P = M V
-  n += plan->dion_idx.empty() ? 0 : 9;         // phase (a), orth(V) of the Dion matrices
-  n += 9;                                      // phase (b): up to three CholeskyQR rounds
+  const int per_orth = plan->tc_orth ? 12 : 9;  // up to three CholeskyQR rounds (+ partial reduce)
+  n += plan->dion_idx.empty() ? 0 : per_orth + (plan->tc_orth ? 1 : 0);   // phase (a): orth(V) of Dion matrices
+  n += per_orth;                               // phase (b)
   n += 2 + (plan->any_split ? 1 : 0);          // phase (c): U^T split, tensor-core W = M^T U, reduce
-  n += plan->orth_idx.empty() ? 0 : 9;         // phase (d), Orth-Dion matrices
+  n += plan->orth_idx.empty() ? 0 : per_orth;  // phase (d), Orth-Dion matrices
   n += plan->dion_idx.empty() ? 0 : 1;         // phase (d), Dion matrices
   n += 2;                                      // phase (e): operand split + tensor-core update
   return n;

@@ -14,6 +14,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace dion {
 namespace simt {
@@ -175,14 +176,42 @@ __global__ void __launch_bounds__(NT) k_gram(const OrthJob* __restrict__ jobs,
 constexpr int CHOL_NT = 512;
 constexpr int CHOL_SMEM_MAX = 200 * 1024;
 
-__device__ void chol_load(const OrthJob& o, float* S, long long lds, float shift, float* s_trace) {
+// Sum of the Gram partials of every job, in a fixed order, into partial 0
+// (gpart[0] = sum_c gpart[c]); one thread per Gram element over the whole GPU,
+// four partials in flight per thread.
+constexpr int GRED_ELEMS = 1024;
+__global__ void __launch_bounds__(256) k_gram_reduce(const OrthJob* __restrict__ jobs,
+                                                     const int* __restrict__ tstart, int njob, int pass) {
+  const int j = find_job(tstart, njob, blockIdx.x);
+  const OrthJob& o = jobs[j];
+  if (*o.status & ST_FATAL) return;
+  if (pass == 2 && !*o.flag) return;
+  const long long rp2 = o.rp * o.rp;
+  for (int e = threadIdx.x; e < GRED_ELEMS; e += blockDim.x) {
+    const long long idx = (long long)(blockIdx.x - tstart[j]) * GRED_ELEMS + e;
+    if (idx >= rp2) break;
+    const float* g = o.gpart + idx;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    int c = 0;
+    for (; c + 4 <= o.nchunk; c += 4) {
+      s0 += g[(long long)c * rp2];
+      s1 += g[(long long)(c + 1) * rp2];
+      s2 += g[(long long)(c + 2) * rp2];
+      s3 += g[(long long)(c + 3) * rp2];
+    }
+    for (; c < o.nchunk; ++c) s0 += g[(long long)c * rp2];
+    o.gpart[idx] = (s0 + s1) + (s2 + s3);
+  }
+}
+
+__device__ void chol_load(const OrthJob& o, int nchunk, float* S, long long lds, float shift, float* s_trace) {
   const int tid = threadIdx.x, nth = blockDim.x;
   const long long r = o.r, rp = o.rp;
   float tr = 0.f;
   for (long long e = tid; e < r * r; e += nth) {
     const long long a = e / r, b = e % r;
     float v = 0.f;
-    for (int c = 0; c < o.nchunk; ++c) v += o.gpart[(long long)c * rp * rp + a * rp + b];
+    for (int c = 0; c < nchunk; ++c) v += o.gpart[(long long)c * rp * rp + a * rp + b];
     if (a == b) { tr += v; v += shift; }
     S[a * lds + b] = v;
   }
@@ -222,7 +251,9 @@ __device__ int chol_factor(float* S, long long lds, long long r, float* s_piv, i
   return 0;
 }
 
-__global__ void __launch_bounds__(CHOL_NT) k_chol_inv(const OrthJob* __restrict__ jobs, int pass, int use_smem) {
+// reduced != 0: the partials were already summed into partial 0 by k_gram_reduce.
+__global__ void __launch_bounds__(CHOL_NT) k_chol_inv(const OrthJob* __restrict__ jobs, int pass, int use_smem,
+                                                     int reduced) {
   extern __shared__ float sm_dyn[];
   const OrthJob& o = jobs[blockIdx.x];
   __shared__ int s_bad;
@@ -234,14 +265,15 @@ __global__ void __launch_bounds__(CHOL_NT) k_chol_inv(const OrthJob* __restrict_
   const long long r = o.r, rp = o.rp;
   float* S = use_smem ? sm_dyn : o.S;
   const long long lds = use_smem ? r + 1 : rp;
-  chol_load(o, S, lds, 0.f, s_trace);
+  const int nchunk = reduced ? 1 : o.nchunk;
+  chol_load(o, nchunk, S, lds, 0.f, s_trace);
   int bad = chol_factor(S, lds, r, &s_piv, &s_bad, &s_min, &s_max);
   if (pass == 0 && (bad || s_min < 1e-6f * s_max)) {
     float trace = 0.f;
     for (int w = 0; w < nth / 32; ++w) trace += s_trace[w];
     const float shift = 11.f * ((float)o.rows * (float)r + (float)r * (float)(r + 1)) * 5.9604645e-8f * trace;
     __syncthreads();
-    chol_load(o, S, lds, shift, s_trace);
+    chol_load(o, nchunk, S, lds, shift, s_trace);
     bad = chol_factor(S, lds, r, &s_piv, &s_bad, &s_min, &s_max);
     if (!bad && tid == 0) { *o.flag = 1u; atomicOr(o.status, ST_SHIFTED); }
   }
@@ -264,6 +296,15 @@ __global__ void __launch_bounds__(CHOL_NT) k_chol_inv(const OrthJob* __restrict_
       if (lane == 0) T[a * rp + c] = (c == a) ? 1.f / raa : -sum / raa;
     }
     __syncthreads();
+  }
+  if (o.Tt_hi) {
+    for (long long e = tid; e < rp * rp; e += nth) {
+      const long long c = e / rp, a = e % rp;   // Tt[c][a] = T[a][c]
+      float h, l;
+      tc::split_tf32(T[a * rp + c], h, l);
+      o.Tt_hi[e] = h;
+      o.Tt_lo[e] = l;
+    }
   }
 }
 

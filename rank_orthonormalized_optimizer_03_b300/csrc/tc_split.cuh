@@ -2,6 +2,7 @@
 // product: x = hi + lo + O(2^-22 |x|), both stored as fp32 bit patterns whose
 // low 13 mantissa bits are zero.  Columns c >= cols of the padded output are
 // written as zero so that the K padding of the tensor-core kernels adds nothing.
+// A job with lo == nullptr is a plain padded copy (hi = x).
 #pragma once
 
 #include "common.cuh"
@@ -35,6 +36,10 @@ __global__ void __launch_bounds__(NT) k_split(const SplitJob* __restrict__ jobs,
     if (idx >= total) break;
     const long long row = idx / o.ldd, c = idx % o.ldd;
     const float v = c < o.cols ? o.src[row * o.lds + c] : 0.f;
+    if (!o.lo) {
+      o.hi[idx] = v;
+      continue;
+    }
     float h, l;
     tc::split_tf32(v, h, l);
     o.hi[idx] = h;

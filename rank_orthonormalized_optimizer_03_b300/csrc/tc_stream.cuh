@@ -47,18 +47,27 @@ constexpr uint32_t OST_BYTES = 2 * A_BYTES + 2 * B_BYTES_MAX;   // 80 KB
 constexpr uint32_t SST_BYTES = 32768;                    // G (<= 16 KB) | R (16 KB)
 constexpr uint32_t SMEM_BYTES = 1024 + OSTAGES * OST_BYTES + SSTAGES * SST_BYTES + 512;
 
+// gmode: what the staged tiles hold.  G_BF16 / G_F32: M = G + R (phases a, c);
+// G_NONE: a single fp32 matrix in the R slot (the A T product of orth()).
+enum { G_NONE = 0, G_BF16 = 1, G_F32 = 2 };
+
 struct SJob {
   CUtensorMap mG, mR, mBh, mBl;   // G, R (staging boxes); B operand hi / lo (box 32 x bn)
-  float* out;                     // P (a) or W partials (c)
-  long long ld_out;               // leading dimension of out (rp)
+  float* out;                     // P (a), W or its partials (c), or the final result of orth()
+  long long ld_out;               // leading dimension of out
   long long split_stride;         // elements between the K-range partials of out
-  int rows;                       // output rows: m (a) or n (c)
-  int kdim;                       // K extent: n (a) or m (c)
+  float* q1;                      // orth(): pass-0 result (ld rp)
+  float* q2;                      // orth(): pass-1 result of a three-pass job (ld rp)
+  const unsigned* flag;           // orth(): three-pass flag of the job
+  int pass;                       // orth(): CholeskyQR pass 0..2; -1 for phases (a), (c)
+  int out_cols;                   // columns of out to write (rp, or r for Vbar into V)
+  int rows;                       // output rows: m (a) or n (c), rows of A (orth)
+  int kdim;                       // K extent: n (a), m (c), rp (orth)
   int ksplit, kchunk;             // K ranges (multiple of BK)
   int ncb, bn;                    // column blocks of width bn (multiple of 32, <= BN_MAX)
-  int rp, g_bf16;
+  int rp, gmode;
   unsigned* status;
-  int pad[4];
+  int pad[6];
 };
 static_assert(sizeof(SJob) % 64 == 0, "SJob must keep 64-byte alignment of its maps");
 
@@ -83,7 +92,9 @@ __device__ __forceinline__ Item item_of(const SJob* __restrict__ jobs, const int
   return it;
 }
 
-__device__ __forceinline__ bool skip(const SJob& j) { return (*j.status & ST_FATAL) != 0; }
+__device__ __forceinline__ bool skip(const SJob& j) {
+  return (*j.status & ST_FATAL) != 0 || (j.pass == 2 && !*j.flag);
+}
 
 // Drain one finished TMEM slice (columns [col0, col0 + half) of this thread's
 // lane) into the register accumulator.
@@ -143,7 +154,7 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
       const Item it = item_of(jobs, tstart, njob, t);
       const SJob& j = jobs[it.job];
       if (skip(j)) continue;
-      const uint32_t gbytes = BM * BK * (j.g_bf16 ? 2 : 4);
+      const uint32_t gbytes = j.gmode == G_NONE ? 0u : BM * BK * (j.gmode == G_BF16 ? 2 : 4);
       const uint32_t bbytes = j.bn * BK * 4;
       for (int kc = 0; kc < it.nk; ++kc) {
         const int k = it.k0 + kc * BK;
@@ -154,11 +165,11 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
           unsigned char* gdst = sst + ss * SST_BYTES;
           unsigned char* rdst = gdst + 16384;
           if (!TRANS) {
-            tma_load_2d(gdst, &j.mG, &s_full[ss], k, it.row0);
+            if (j.gmode != G_NONE) tma_load_2d(gdst, &j.mG, &s_full[ss], k, it.row0);
             tma_load_2d(rdst, &j.mR, &s_full[ss], k, it.row0);
           } else {
             // rows k..k+31 of M, columns row0..row0+127 (boxes of 128 bytes per row)
-            const int gbox = j.g_bf16 ? 64 : 32;
+            const int gbox = j.gmode == G_BF16 ? 64 : 32;
             for (int b = 0; b < BM / gbox; ++b)
               tma_load_2d(gdst + b * 4096, &j.mG, &s_full[ss], it.row0 + b * gbox, k);
             for (int b = 0; b < BM / 32; ++b)
@@ -266,7 +277,7 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
             const float4 r = *reinterpret_cast<const float4*>(rsrc + row * 128 + (((ch ^ row) & 7) << 4));
             mv[4 * c] = r.x; mv[4 * c + 1] = r.y; mv[4 * c + 2] = r.z; mv[4 * c + 3] = r.w;
           }
-          if (j.g_bf16) {
+          if (j.gmode == G_BF16) {
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
               const int ch = 2 * h + c;   // 64-byte rows, 64-byte swizzle
@@ -278,7 +289,7 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
                 mv[c * 8 + 2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
               }
             }
-          } else {
+          } else if (j.gmode == G_F32) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const int ch = 4 * h + c;
@@ -308,7 +319,7 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
               const int i = 16 * h + 4 * c + e;
               float v = *reinterpret_cast<const float*>(rsrc + jb * 4096 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4) +
                                                         ((jj & 3) << 2));
-              if (j.g_bf16) {
+              if (j.gmode == G_BF16) {
                 const int gb = row >> 6, gj = row & 63;
                 const uint16_t gv = *reinterpret_cast<const uint16_t*>(
                     gsrc + gb * 4096 + i * 128 + ((((gj >> 3) ^ i) & 7) << 4) + ((gj & 7) << 1));
@@ -350,15 +361,25 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
       }
       if (!ok) break;
       const int grow = it.row0 + row;
+      // destination: phases (a) / (c) write out (+ the K-range partial); orth() passes
+      // write their intermediate factor, or the final result after the last pass
+      float* dst = j.out + (long long)it.ks * j.split_stride;
+      long long ld = j.ld_out;
+      int cols = j.out_cols;
+      if (j.pass == 0 || (j.pass == 1 && *j.flag)) {
+        dst = j.pass == 0 ? j.q1 : j.q2;
+        ld = j.rp;
+        cols = j.rp;
+      }
       if (grow < j.rows) {
-        float* dst = j.out + (long long)it.ks * j.split_stride + (long long)grow * j.ld_out + it.c0 + h * half;
+        dst += (long long)grow * ld;
+        const int cbase = it.c0 + h * half;
 #pragma unroll
         for (int cb = 0; cb < HALF_MAX / 16; ++cb)
-          if (cb * 16 < half && it.c0 + h * half + cb * 16 < j.rp) {
+          if (cb * 16 < half) {
 #pragma unroll
-            for (int k = 0; k < 16; k += 4)
-              *reinterpret_cast<float4*>(dst + cb * 16 + k) =
-                  make_float4(acc[cb * 16 + k], acc[cb * 16 + k + 1], acc[cb * 16 + k + 2], acc[cb * 16 + k + 3]);
+            for (int k = 0; k < 16; ++k)
+              if (cbase + cb * 16 + k < cols) dst[cbase + cb * 16 + k] = acc[cb * 16 + k];
           }
       }
     }

@@ -147,11 +147,17 @@ def test_phase_intermediates(dev, m, n, r, variant):
     plan.phases(1, 1)
     U = f64(plan.buffer(0, dion.BUF_U))
     assert np.abs(U.T @ U - np.eye(r)).max() < TOL_ORTH
-    assert rel(U, ref["U"]) < 1e-4
+    # The Q factor of a thin QR moves by up to kappa(P) times the relative
+    # perturbation of P; P itself carries fp32 rounding (2^-24), so an
+    # intermediate's forward error is bounded by a multiple of kappa(P) u,
+    # not by a fixed number.  X and R below keep the fixed tolerances.
+    sv = np.linalg.svd(P_ref, compute_uv=False)
+    tol_mid = max(1e-4, 4.0 * (sv[0] / sv[-1]) * 2.0 ** -24)
+    assert rel(U, ref["U"]) < tol_mid
     plan.phases(2, 2)
-    assert rel(f64(plan.buffer(0, dion.BUF_W)), ref["W"]) < 1e-4
+    assert rel(f64(plan.buffer(0, dion.BUF_W)), ref["W"]) < tol_mid
     plan.phases(3, 3)
-    assert rel(f64(d["V"]), ref["Vbar"]) < 1e-4
+    assert rel(f64(d["V"]), ref["Vbar"]) < tol_mid
     plan.phases(4, 4)
     torch.cuda.synchronize()
     assert plan.failures() == [0]
