@@ -314,7 +314,7 @@ void layout(dion_plan* p) {
     p->off_W[i] = region(4 * (size_t)(n * rp));
     p->off_Wpart[i] = region(p->ksplit[i] > 1 ? 4 * (size_t)p->ksplit[i] * (size_t)(n * rp) : 4);
     p->off_gpart[i] = region(4 * (size_t)std::max(p->nchunk_p[i], p->nchunk_w[i]) * (size_t)(rp * rp));
-    p->off_S[i] = region(4 * (size_t)(rp * rp));
+    p->off_S[i] = region(4 * (size_t)(rp * rp + rp));
     p->off_T[i] = region(4 * (size_t)(rp * rp));
     p->off_Vo[i] = region(D(i).variant == DION_VARIANT_DION ? 4 * (size_t)(n * rp) : 4);
   }
@@ -636,7 +636,7 @@ dion_status_t launch_orth(const dion_plan* p, unsigned char* base, cudaStream_t 
   // the largest rank of the list decides whether the Cholesky works in shared memory
   long long rmax = 0;
   for (int i = 0; i < p->count; ++i) rmax = std::max<long long>(rmax, p->descs[i].r);
-  const size_t chol_smem = (size_t)(rmax * (rmax + 1) * 4);
+  const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax) * 4);
   const int use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
   for (int pass = 0; pass < 3; ++pass) {
     simt::k_gram<<<ts_gram[njob], simt::NT, 0, s>>>(jobs, tg, njob, pass);
@@ -653,7 +653,7 @@ dion_status_t launch_orth_tc(const dion_plan* p, unsigned char* base, cudaStream
   const OrthJob* jobs = tab<OrthJob>(p, base, t_jobs);
   long long rmax = 0;
   for (int i = 0; i < p->count; ++i) rmax = std::max<long long>(rmax, p->descs[i].r);
-  const size_t chol_smem = (size_t)(rmax * (rmax + 1) * 4);
+  const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax) * 4);
   const int use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
   const int ng = p->ts_g[L][njob], nt = p->ts_t[L][njob];
   for (int ps = 0; ps < 3; ++ps) {

@@ -281,29 +281,37 @@ __global__ void __launch_bounds__(CHOL_NT) k_chol_inv(const OrthJob* __restrict_
     if (tid == 0) atomicOr(o.status, (unsigned)bad);
     return;
   }
-  // T = Rc^{-1}: row a from the bottom up, T[a][c] = -(sum_{k=a+1..c} Rc[a][k] T[k][c]) / Rc[a][a]
-  float* T = o.T;
-  for (long long e = tid; e < rp * rp; e += nth) T[e] = 0.f;
-  __syncthreads();
+  // T = Rc^{-1}, one column per warp with no block-wide barrier:
+  //   T[c][c] = 1 / Rc[c][c];  T[a][c] = -(sum_{k=a+1..c} Rc[a][k] T[k][c]) / Rc[a][a],  a = c-1 .. 0.
+  // Column c of T (a < c) is kept in row c of S's lower triangle, its diagonal in tdiag[c].
+  float* tdiag = use_smem ? sm_dyn + r * lds : o.S + rp * rp;   // r floats of scratch
   const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
-  for (long long a = r - 1; a >= 0; --a) {
-    const float raa = S[a * lds + a];
-    for (long long c = a + warp; c < r; c += nwarp) {
+  for (long long c = warp; c < r; c += nwarp) {
+    const float tcc = 1.f / S[c * lds + c];
+    for (long long a = c - 1; a >= 0; --a) {
       float sum = 0.f;
-      for (long long k = a + 1 + lane; k <= c; k += 32) sum = fmaf(S[a * lds + k], T[k * rp + c], sum);
+      for (long long k = a + 1 + lane; k <= c; k += 32)
+        sum = fmaf(S[a * lds + k], k == c ? tcc : S[c * lds + k], sum);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      if (lane == 0) T[a * rp + c] = (c == a) ? 1.f / raa : -sum / raa;
+      if (lane == 0) S[c * lds + a] = -sum / S[a * lds + a];
+      __syncwarp();
     }
-    __syncthreads();
+    if (lane == 0) tdiag[c] = tcc;
   }
-  if (o.Tt_hi) {
-    for (long long e = tid; e < rp * rp; e += nth) {
-      const long long c = e / rp, a = e % rp;   // Tt[c][a] = T[a][c]
+  __syncthreads();
+  // T (row-major rp x rp, zero outside the upper triangle) and T^T split for the tensor core
+  float* T = o.T;
+  for (long long e = tid; e < rp * rp; e += nth) {
+    const long long a = e / rp, c = e % rp;
+    float v = 0.f;
+    if (a < r && c < r) v = a < c ? S[c * lds + a] : (a == c ? tdiag[a] : 0.f);
+    if (!o.Tt_hi) T[e] = v;
+    else {
       float h, l;
-      tc::split_tf32(T[a * rp + c], h, l);
-      o.Tt_hi[e] = h;
-      o.Tt_lo[e] = l;
+      tc::split_tf32(v, h, l);
+      o.Tt_hi[c * rp + a] = h;   // Tt[c][a] = T[a][c]
+      o.Tt_lo[c * rp + a] = l;
     }
   }
 }

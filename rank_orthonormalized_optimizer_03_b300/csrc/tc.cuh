@@ -190,6 +190,25 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for the 64-byte swizzle layout (rows of 64 bytes = 16 fp32, 16-byte
+// chunk index XOR (row / 2) % 4, 8-row groups 512 bytes apart; tile base
+// 512-aligned, K steps of 32 bytes inside the row).
+__device__ __forceinline__ uint64_t sdesc_k_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;                       // layout: 64-byte swizzle
+  return d;
+}
+
+// Byte offset of element (row, k) of a 4-byte K-major operand tile in the 64-byte
+// swizzle layout (k in [0, 16)).
+__device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t k) {
+  return row * 64u + ((((k >> 2) ^ (row >> 1)) & 3u) << 4) + ((k & 3u) << 2);
+}
+
 // Byte offset of element (row, k) of a 4-byte K-major operand tile in the
 // 128-byte swizzle layout (k in [0, 32)).
 __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t k) {

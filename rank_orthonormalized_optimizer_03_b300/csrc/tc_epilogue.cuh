@@ -201,6 +201,7 @@ k_epi(const EpiMat* __restrict__ mats, const int* __restrict__ tstart, int nmat,
     const bool leader = (warp == 4 && lane == 0);
     int b = 0; uint32_t aph[2] = {0, 0};
     int q = 0; uint32_t ph = 0;
+    int prev_q = -1;   // staging slot whose TMA stores are still reading it (leader only)
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile tl = tile_of(mats, tstart, nmat, t);
       const EpiMat& e = mats[tl.mat];
@@ -266,12 +267,15 @@ k_epi(const EpiMat* __restrict__ mats, const int* __restrict__ tstart, int nmat,
         fence_async_smem();
         named_sync(1, 128);
         if (leader) {
+          // stores of this slot go out now; the previous slot is released once
+          // its own stores have read the shared memory (all but the newest group)
           const int x = tl.j0 + sc * SUB;
           tma_store_2d(&e.map[MAP_R], rb, x, tl.i0);
           tma_store_2d(&e.map[MAP_X], xb, x, tl.i0);
           tma_store_commit();
-          tma_store_wait_read<0>();
-          mbar_arrive(&q_empty[q]);
+          tma_store_wait_read<1>();
+          if (prev_q >= 0) mbar_arrive(&q_empty[prev_q]);
+          prev_q = q;
         }
         if (++q == QSTAGES) { q = 0; ph ^= 1; }
       }
@@ -281,7 +285,10 @@ k_epi(const EpiMat* __restrict__ mats, const int* __restrict__ tstart, int nmat,
       if (lane == 0) mbar_arrive(&acc_empty[b]);
       aph[b] ^= 1; b ^= 1;
     }
-    if (leader) tma_store_wait_all<0>();
+    if (leader) {
+      tma_store_wait_all<0>();
+      if (prev_q >= 0) mbar_arrive(&q_empty[prev_q]);
+    }
   }
   tc_fence_before();
   __syncthreads();
