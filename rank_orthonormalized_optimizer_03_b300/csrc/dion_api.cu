@@ -89,6 +89,11 @@ struct dion_plan {
   size_t t_ts_gred[3] = {};
   size_t t_vcopy = 0, t_ts_vcopy = 0;
   std::vector<int> ts_vcopy;
+  // work-item tables of the persistent tensor-core kernels (built on the host, heaviest first)
+  std::vector<tcstream::Item> it_sa, it_sc, it_tr[3];
+  std::vector<tcepi::Tile> it_epi;
+  std::vector<tcgram::GItem> it_g[3];
+  size_t t_it_sa = 0, t_it_sc = 0, t_it_tr[3] = {}, t_it_epi = 0, t_it_g[3] = {};
 
   std::vector<unsigned char> image;
   const void* uploaded_ws = nullptr;
@@ -265,6 +270,64 @@ void layout(dion_plan* p) {
     }
     p->t_ts_vcopy = take(4 * p->ts_vcopy.size());
   }
+  // ---- work-item tables
+  {
+    auto by_cost = [](std::vector<tcstream::Item>& v, const std::vector<int>& bnv, bool job_is_matrix,
+                      const std::vector<int>* list) {
+      std::stable_sort(v.begin(), v.end(), [&](const tcstream::Item& a, const tcstream::Item& b) {
+        const int ia = job_is_matrix ? a.job : (*list)[a.job], ib = job_is_matrix ? b.job : (*list)[b.job];
+        return (long long)a.nk * bnv[ia] > (long long)b.nk * bnv[ib];
+      });
+    };
+    p->it_sa.clear();
+    p->it_sc.clear();
+    for (int i = 0; i < cnt; ++i) {
+      const long long m = D(i).m, n = D(i).n;
+      for (long long r0 = 0; r0 < m; r0 += tcstream::BM)
+        for (int cb = 0; cb < p->ncb[i]; ++cb)
+          p->it_sa.push_back(tcstream::Item{i, (int)r0, 0, cb * p->bn[i], 0, (int)cdiv(n, tcstream::BK), 0, 0});
+      for (long long r0 = 0; r0 < n; r0 += tcstream::BM)
+        for (int ks = 0; ks < p->ksplit[i]; ++ks)
+          for (int cb = 0; cb < p->ncb[i]; ++cb) {
+            const long long k0 = (long long)ks * p->kchunk[i];
+            const long long k1 = std::min<long long>(m, k0 + p->kchunk[i]);
+            p->it_sc.push_back(tcstream::Item{i, (int)r0, ks, cb * p->bn[i], (int)k0,
+                                              (int)cdiv(k1 - k0, tcstream::BK), 0, 0});
+          }
+    }
+    by_cost(p->it_sa, p->bn, true, nullptr);
+    by_cost(p->it_sc, p->bn, true, nullptr);
+    const std::vector<int>* lists[3] = {&all, &p->orth_idx, &p->dion_idx};
+    for (int L = 0; L < 3; ++L) {
+      p->it_tr[L].clear();
+      p->it_g[L].clear();
+      for (size_t k = 0; k < lists[L]->size(); ++k) {
+        const int i = (*lists[L])[k];
+        const long long rows = L == 0 ? D(i).m : D(i).n;
+        for (long long r0 = 0; r0 < rows; r0 += tcstream::BM)
+          for (int cb = 0; cb < p->ncb[i]; ++cb)
+            p->it_tr[L].push_back(tcstream::Item{(int)k, (int)r0, 0, cb * p->bn[i], 0,
+                                                 (int)(p->rp[i] / tcstream::BK), 0, 0});
+        for (long long c = 0; c < cdiv(rows, tcgram::CHUNK_ROWS); ++c)
+          p->it_g[L].push_back(tcgram::GItem{(int)k, (int)c, 0, 0});
+      }
+      by_cost(p->it_tr[L], p->bn, false, lists[L]);
+    }
+    p->it_epi.clear();
+    for (int i = 0; i < cnt; ++i)
+      for (long long i0 = 0; i0 < D(i).m; i0 += tcepi::BM)
+        for (long long j0 = 0; j0 < D(i).n; j0 += tcepi::BNJ)
+          p->it_epi.push_back(tcepi::Tile{i, (int)i0, (int)j0, 0});
+    std::stable_sort(p->it_epi.begin(), p->it_epi.end(), [&](const tcepi::Tile& a, const tcepi::Tile& b) {
+      return p->rp[a.mat] > p->rp[b.mat]; });
+    p->t_it_sa = take(sizeof(tcstream::Item) * std::max<size_t>(1, p->it_sa.size()));
+    p->t_it_sc = take(sizeof(tcstream::Item) * std::max<size_t>(1, p->it_sc.size()));
+    for (int L = 0; L < 3; ++L) {
+      p->t_it_tr[L] = take(sizeof(tcstream::Item) * std::max<size_t>(1, p->it_tr[L].size()));
+      p->t_it_g[L] = take(sizeof(tcgram::GItem) * std::max<size_t>(1, p->it_g[L].size()));
+    }
+    p->t_it_epi = take(sizeof(tcepi::Tile) * std::max<size_t>(1, p->it_epi.size()));
+  }
   p->t_sj_a = take(sizeof(tcstream::SJob) * cnt);
   p->t_sj_c = take(sizeof(tcstream::SJob) * cnt);
   p->t_epi = take(sizeof(tcepi::EpiMat) * cnt);
@@ -314,7 +377,7 @@ void layout(dion_plan* p) {
     p->off_W[i] = region(4 * (size_t)(n * rp));
     p->off_Wpart[i] = region(p->ksplit[i] > 1 ? 4 * (size_t)p->ksplit[i] * (size_t)(n * rp) : 4);
     p->off_gpart[i] = region(4 * (size_t)std::max(p->nchunk_p[i], p->nchunk_w[i]) * (size_t)(rp * rp));
-    p->off_S[i] = region(4 * (size_t)(rp * rp + rp));
+    p->off_S[i] = region(4 * (size_t)(rp * rp + rp + 32 * rp));
     p->off_T[i] = region(4 * (size_t)(rp * rp));
     p->off_Vo[i] = region(D(i).variant == DION_VARIANT_DION ? 4 * (size_t)(n * rp) : 4);
   }
@@ -480,12 +543,13 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     tcepi::EpiMat& e = epi[i];
     std::memset(&e, 0, sizeof e);
     bool okm = true;
-    okm &= make_map(&e.map[tcepi::MAP_UH], F32, Uh, rp, d.m, rp * 4, tcepi::BK, tcepi::BM, CU_TENSOR_MAP_SWIZZLE_128B);
-    okm &= make_map(&e.map[tcepi::MAP_UL], F32, Ul, rp, d.m, rp * 4, tcepi::BK, tcepi::BM, CU_TENSOR_MAP_SWIZZLE_128B);
-    okm &= make_map(&e.map[tcepi::MAP_VH], F32, Vh, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, CU_TENSOR_MAP_SWIZZLE_128B);
-    okm &= make_map(&e.map[tcepi::MAP_VL], F32, Vl, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, CU_TENSOR_MAP_SWIZZLE_128B);
-    okm &= make_map(&e.map[tcepi::MAP_WH], F32, Wh, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, CU_TENSOR_MAP_SWIZZLE_128B);
-    okm &= make_map(&e.map[tcepi::MAP_WL], F32, Wl, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, CU_TENSOR_MAP_SWIZZLE_128B);
+    const CUtensorMapSwizzle OSW = CU_TENSOR_MAP_SWIZZLE_64B;   // operand boxes of 16 along K
+    okm &= make_map(&e.map[tcepi::MAP_UH], F32, Uh, rp, d.m, rp * 4, tcepi::BK, tcepi::BM, OSW);
+    okm &= make_map(&e.map[tcepi::MAP_UL], F32, Ul, rp, d.m, rp * 4, tcepi::BK, tcepi::BM, OSW);
+    okm &= make_map(&e.map[tcepi::MAP_VH], F32, Vh, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, OSW);
+    okm &= make_map(&e.map[tcepi::MAP_VL], F32, Vl, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, OSW);
+    okm &= make_map(&e.map[tcepi::MAP_WH], F32, Wh, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, OSW);
+    okm &= make_map(&e.map[tcepi::MAP_WL], F32, Wl, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, OSW);
     if (d.g_dtype == DION_DTYPE_BF16)
       okm &= make_map(&e.map[tcepi::MAP_G], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.G, d.n, d.m, d.ld_g * 2, tcepi::SUB,
                       tcepi::BM, CU_TENSOR_MAP_SWIZZLE_32B);
@@ -519,11 +583,13 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     tcstream::SJob& a = sa[i];
     std::memset(&a, 0, sizeof a);
     bool okm = true;
+    // staging boxes of 16 columns (64-byte rows for fp32, 32-byte rows for bf16) and
+    // operand boxes of 16 along K (64-byte swizzle)
     okm &= make_map(&a.mG, gdt, d.G, d.n, d.m, gpitch, tcstream::BK, tcstream::BM,
-                    gb ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
-    okm &= make_map(&a.mR, F32, d.R, d.n, d.m, d.ld_r * 4, tcstream::BK, tcstream::BM, CU_TENSOR_MAP_SWIZZLE_128B);
-    okm &= make_map(&a.mBh, F32, VTh, d.n, rp, p->ldt_n[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
-    okm &= make_map(&a.mBl, F32, VTl, d.n, rp, p->ldt_n[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
+                    gb ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
+    okm &= make_map(&a.mR, F32, d.R, d.n, d.m, d.ld_r * 4, tcstream::BK, tcstream::BM, CU_TENSOR_MAP_SWIZZLE_64B);
+    okm &= make_map(&a.mBh, F32, VTh, d.n, rp, p->ldt_n[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_64B);
+    okm &= make_map(&a.mBl, F32, VTl, d.n, rp, p->ldt_n[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_64B);
     a.out = x.P; a.ld_out = rp; a.split_stride = 0; a.rows = (int)d.m; a.kdim = (int)d.n;
     a.ksplit = 1; a.kchunk = (int)(cdiv(d.n, 32) * 32); a.ncb = p->ncb[i]; a.bn = p->bn[i];
     a.rp = (int)rp; a.gmode = gb ? tcstream::G_BF16 : tcstream::G_F32; a.status = x.status;
@@ -532,8 +598,8 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     std::memset(&c, 0, sizeof c);
     okm &= make_map(&c.mG, gdt, d.G, d.n, d.m, gpitch, gb ? 64 : 32, tcstream::BK, CU_TENSOR_MAP_SWIZZLE_128B);
     okm &= make_map(&c.mR, F32, d.R, d.n, d.m, d.ld_r * 4, 32, tcstream::BK, CU_TENSOR_MAP_SWIZZLE_128B);
-    okm &= make_map(&c.mBh, F32, UTh, d.m, rp, p->ldt_m[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
-    okm &= make_map(&c.mBl, F32, UTl, d.m, rp, p->ldt_m[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
+    okm &= make_map(&c.mBh, F32, UTh, d.m, rp, p->ldt_m[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_64B);
+    okm &= make_map(&c.mBl, F32, UTl, d.m, rp, p->ldt_m[i] * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_64B);
     if (!okm) return fail(DION_ERR_CUDA, "matrix %d: cuTensorMapEncodeTiled failed (streaming maps)", i);
     c.out = p->ksplit[i] > 1 ? x.Wpart : x.W; c.ld_out = rp; c.split_stride = d.n * rp;
     c.rows = (int)d.n; c.kdim = (int)d.m; c.ksplit = p->ksplit[i]; c.kchunk = p->kchunk[i];
@@ -564,9 +630,9 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
           g.nchunk = (int)cdiv(o.rows, tcgram::CHUNK_ROWS); g.pass = ps; g.flag = o.flag; g.status = o.status;
           tcstream::SJob& t = tj[k];
           std::memset(&t, 0, sizeof t);
-          okm &= make_map(&t.mR, F32, src, rp, o.rows, lds * 4, tcstream::BK, tcstream::BM, CU_TENSOR_MAP_SWIZZLE_128B);
-          okm &= make_map(&t.mBh, F32, o.Tt_hi, rp, rp, rp * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
-          okm &= make_map(&t.mBl, F32, o.Tt_lo, rp, rp, rp * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_128B);
+          okm &= make_map(&t.mR, F32, src, rp, o.rows, lds * 4, tcstream::BK, tcstream::BM, CU_TENSOR_MAP_SWIZZLE_64B);
+          okm &= make_map(&t.mBh, F32, o.Tt_hi, rp, rp, rp * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_64B);
+          okm &= make_map(&t.mBl, F32, o.Tt_lo, rp, rp, rp * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_64B);
           if (!okm) return fail(DION_ERR_CUDA, "matrix %d: cuTensorMapEncodeTiled failed (orth maps)", i);
           t.out = o.out; t.ld_out = o.ldo; t.split_stride = 0; t.q1 = o.Q; t.q2 = o.Q2; t.flag = o.flag;
           t.pass = ps; t.out_cols = (int)o.out_cols; t.rows = (int)o.rows; t.kdim = (int)rp;
@@ -589,6 +655,13 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     put(p->image, p->t_vcopy, vc.data(), vc.size());
     put(p->image, p->t_ts_vcopy, p->ts_vcopy.data(), p->ts_vcopy.size());
   }
+  if (!p->it_sa.empty()) put(p->image, p->t_it_sa, p->it_sa.data(), p->it_sa.size());
+  if (!p->it_sc.empty()) put(p->image, p->t_it_sc, p->it_sc.data(), p->it_sc.size());
+  for (int L = 0; L < 3; ++L) {
+    if (!p->it_tr[L].empty()) put(p->image, p->t_it_tr[L], p->it_tr[L].data(), p->it_tr[L].size());
+    if (!p->it_g[L].empty()) put(p->image, p->t_it_g[L], p->it_g[L].data(), p->it_g[L].size());
+  }
+  if (!p->it_epi.empty()) put(p->image, p->t_it_epi, p->it_epi.data(), p->it_epi.size());
   put(p->image, p->t_sj_a, sa.data(), sa.size());
   put(p->image, p->t_sj_c, sc.data(), sc.size());
   put(p->image, p->t_ts_sa, p->ts_sa.data(), p->ts_sa.size());
@@ -636,11 +709,14 @@ dion_status_t launch_orth(const dion_plan* p, unsigned char* base, cudaStream_t 
   // the largest rank of the list decides whether the Cholesky works in shared memory
   long long rmax = 0;
   for (int i = 0; i < p->count; ++i) rmax = std::max<long long>(rmax, p->descs[i].r);
-  const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax) * 4);
+  const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax + 32 * rmax) * 4);
   const int use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
   for (int pass = 0; pass < 3; ++pass) {
     simt::k_gram<<<ts_gram[njob], simt::NT, 0, s>>>(jobs, tg, njob, pass);
-    simt::k_chol_inv<<<njob, simt::CHOL_NT, use_smem ? chol_smem : 0, s>>>(jobs, pass, use_smem, 0);
+    if (use_smem)
+      simt::k_chol_inv<true><<<njob, simt::CHOL_NT, chol_smem, s>>>(jobs, pass, 0);
+    else
+      simt::k_chol_inv<false><<<njob, simt::CHOL_NT, 0, s>>>(jobs, pass, 0);
     simt::k_trmm<<<ts_trmm[njob], simt::NT, 0, s>>>(jobs, tt, njob, pass);
   }
   return cuda_check("orth launch");
@@ -653,16 +729,19 @@ dion_status_t launch_orth_tc(const dion_plan* p, unsigned char* base, cudaStream
   const OrthJob* jobs = tab<OrthJob>(p, base, t_jobs);
   long long rmax = 0;
   for (int i = 0; i < p->count; ++i) rmax = std::max<long long>(rmax, p->descs[i].r);
-  const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax) * 4);
+  const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax + 32 * rmax) * 4);
   const int use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
-  const int ng = p->ts_g[L][njob], nt = p->ts_t[L][njob];
+  const int ng = (int)p->it_g[L].size(), nt = (int)p->it_tr[L].size();
   for (int ps = 0; ps < 3; ++ps) {
     tcgram::k_gram<<<std::min(ng, p->num_sms), tcgram::NTHREADS, tcgram::SMEM_BYTES, s>>>(
-        tab<tcgram::GJob>(p, base, p->t_gj[L][ps]), tab<int>(p, base, p->t_ts_g[L]), njob, ng);
+        tab<tcgram::GJob>(p, base, p->t_gj[L][ps]), tab<tcgram::GItem>(p, base, p->t_it_g[L]), ng);
     simt::k_gram_reduce<<<p->ts_gred[L][njob], 256, 0, s>>>(jobs, tab<int>(p, base, p->t_ts_gred[L]), njob, ps);
-    simt::k_chol_inv<<<njob, simt::CHOL_NT, use_smem ? chol_smem : 0, s>>>(jobs, ps, use_smem, 1);
+    if (use_smem)
+      simt::k_chol_inv<true><<<njob, simt::CHOL_NT, chol_smem, s>>>(jobs, ps, 1);
+    else
+      simt::k_chol_inv<false><<<njob, simt::CHOL_NT, 0, s>>>(jobs, ps, 1);
     tcstream::k_stream<false><<<std::min(nt, p->num_sms), tcstream::NTHREADS, tcstream::SMEM_BYTES, s>>>(
-        tab<tcstream::SJob>(p, base, p->t_tj[L][ps]), tab<int>(p, base, p->t_ts_t[L]), njob, nt);
+        tab<tcstream::SJob>(p, base, p->t_tj[L][ps]), tab<tcstream::Item>(p, base, p->t_it_tr[L]), nt);
   }
   return cuda_check("orth launch");
 }
@@ -700,9 +779,10 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
         if (st) return st;
         tcsplit::k_tsplit<<<p->ts_tv[cnt], tcsplit::NT, 0, s>>>(
             tab<tcsplit::TJob>(p, base, p->t_tj_v), tab<int>(p, base, p->t_ts_tv), cnt);
-        tcstream::k_stream<false><<<std::min(p->ts_sa[cnt], p->num_sms), tcstream::NTHREADS,
+        tcstream::k_stream<false><<<std::min((int)p->it_sa.size(), p->num_sms), tcstream::NTHREADS,
                                     tcstream::SMEM_BYTES, s>>>(tab<tcstream::SJob>(p, base, p->t_sj_a),
-                                                               tab<int>(p, base, p->t_ts_sa), cnt, p->ts_sa[cnt]);
+                                                               tab<tcstream::Item>(p, base, p->t_it_sa),
+                                                               (int)p->it_sa.size());
         break;
       case 1:
         st = p->tc_orth ? launch_orth_tc(p, base, s, 0, p->t_jobs_p, cnt)
@@ -713,9 +793,10 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
       case 2:
         tcsplit::k_tsplit<<<p->ts_tu[cnt], tcsplit::NT, 0, s>>>(
             tab<tcsplit::TJob>(p, base, p->t_tj_u), tab<int>(p, base, p->t_ts_tu), cnt);
-        tcstream::k_stream<true><<<std::min(p->ts_sc[cnt], p->num_sms), tcstream::NTHREADS,
+        tcstream::k_stream<true><<<std::min((int)p->it_sc.size(), p->num_sms), tcstream::NTHREADS,
                                    tcstream::SMEM_BYTES, s>>>(tab<tcstream::SJob>(p, base, p->t_sj_c),
-                                                              tab<int>(p, base, p->t_ts_sc), cnt, p->ts_sc[cnt]);
+                                                              tab<tcstream::Item>(p, base, p->t_it_sc),
+                                                              (int)p->it_sc.size());
         if (p->any_split)
           simt::k_wreduce<<<p->ts_wred[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_wred), cnt);
         break;
@@ -732,10 +813,10 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
       case 4: {
         tcsplit::k_split<<<p->ts_split[p->n_split], tcsplit::NT, 0, s>>>(
             tab<tcsplit::SplitJob>(p, base, p->t_split), tab<int>(p, base, p->t_ts_split), p->n_split);
-        const int tiles = p->ts_epi_tc[cnt];
+        const int tiles = (int)p->it_epi.size();
         const int grid = std::min(tiles, p->num_sms);
         tcepi::k_epi<<<grid, tcepi::NTHREADS, tcepi::SMEM_BYTES, s>>>(
-            tab<tcepi::EpiMat>(p, base, p->t_epi), tab<int>(p, base, p->t_ts_epi_tc), cnt, tiles);
+            tab<tcepi::EpiMat>(p, base, p->t_epi), tab<tcepi::Tile>(p, base, p->t_it_epi), tiles);
         break;
       }
     }
@@ -816,7 +897,7 @@ dion_status_t dion_plan_upload(dion_plan* plan, void* workspace, size_t ws_bytes
                              (int)tcstream::SMEM_BYTES) != cudaSuccess ||
         cudaFuncSetAttribute(tcstream::k_stream<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)tcstream::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(simt::k_chol_inv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(simt::k_chol_inv<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              simt::CHOL_SMEM_MAX) != cudaSuccess ||
         cudaFuncSetAttribute(tcgram::k_gram, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)tcgram::SMEM_BYTES) != cudaSuccess)

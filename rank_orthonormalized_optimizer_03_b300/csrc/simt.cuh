@@ -204,12 +204,12 @@ __global__ void __launch_bounds__(256) k_gram_reduce(const OrthJob* __restrict__
   }
 }
 
-__device__ void chol_load(const OrthJob& o, int nchunk, float* S, long long lds, float shift, float* s_trace) {
+__device__ void chol_load(const OrthJob& o, int nchunk, float* S, int lds, float shift, float* s_trace) {
   const int tid = threadIdx.x, nth = blockDim.x;
-  const long long r = o.r, rp = o.rp;
+  const int r = o.r, rp = o.rp;
   float tr = 0.f;
-  for (long long e = tid; e < r * r; e += nth) {
-    const long long a = e / r, b = e % r;
+  for (int e = tid; e < r * r; e += nth) {
+    const int a = e / r, b = e % r;
     float v = 0.f;
     for (int c = 0; c < nchunk; ++c) v += o.gpart[(long long)c * rp * rp + a * rp + b];
     if (a == b) { tr += v; v += shift; }
@@ -221,97 +221,195 @@ __device__ void chol_load(const OrthJob& o, int nchunk, float* S, long long lds,
   __syncthreads();
 }
 
-// In-place upper Cholesky; returns 0, or the status bits of a failure.
-// *min_piv2 / *max_diag receive the smallest squared pivot and largest diagonal.
-__device__ int chol_factor(float* S, long long lds, long long r, float* s_piv, int* s_bad, float* s_min, float* s_max) {
-  const int tid = threadIdx.x, nth = blockDim.x;
-  const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
-  if (tid == 0) { *s_bad = 0; *s_min = INFINITY; *s_max = 0.f; }
-  if (tid == 0)
-    for (long long j = 0; j < r; ++j) *s_max = fmaxf(*s_max, S[j * lds + j]);
+// Storage of the factorisation in the r x lds array S: Rc (upper triangular,
+// S = Rc^T Rc) in the upper triangle, T = Rc^{-1} (upper triangular) transposed
+// into the strict lower triangle (T[a][c] at S[c][a], a < c), diag(T) in tdiag.
+__device__ __forceinline__ float Rv(const float* S, int lds, int r, int a, int b) {
+  return (a <= b && b < r) ? S[a * lds + b] : 0.f;
+}
+__device__ __forceinline__ float Tv(const float* S, int lds, const float* tdiag, int r, int a,
+                                    int c) {
+  if (c >= r) return 0.f;
+  return a < c ? S[c * lds + a] : (a == c ? tdiag[a] : 0.f);
+}
+
+// In-place upper Cholesky, blocked right-looking with 32-wide panels.  Per panel:
+// one warp factors the diagonal block in registers (lane l holds column l) and
+// inverts it (T_pp = Rc_pp^{-1}); the row panel is Rc_pc = T_pp^T S_pc (a
+// product, no substitution chain); the trailing matrix takes a rank-32 update.
+// Returns 0 or the status bits of a failure; *s_min / *s_max receive the
+// smallest squared pivot and the largest diagonal.  `scratch` holds 32 * r floats.
+__device__ int chol_factor(float* S, int lds, int r, float* tdiag, float* scratch, int* s_bad,
+                           float* s_min, float* s_max) {
+  const int tid = threadIdx.x, nth = blockDim.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 0) {
+    float mx = 0.f;
+    for (int j = lane; j < r; j += 32) mx = fmaxf(mx, S[j * lds + j]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) { *s_max = mx; *s_bad = 0; *s_min = INFINITY; }
+  }
   __syncthreads();
-  for (long long jj = 0; jj < r; ++jj) {
-    if (tid == 0) {
-      const float dd = S[jj * lds + jj];
-      if (!isfinite(dd)) *s_bad = (int)(ST_BREAKDOWN | ST_NONFINITE);
-      else if (!(dd > 0.f)) *s_bad = (int)ST_BREAKDOWN;
-      else { *s_min = fminf(*s_min, dd); *s_piv = sqrtf(dd); S[jj * lds + jj] = *s_piv; }
+  for (int k0 = 0; k0 < r; k0 += 32) {
+    const int nb = (int)min(32, r - k0);
+    // (1) diagonal block, one warp: col[i] = S[k0 + i][k0 + lane] for i <= lane
+    if (warp == 0) {
+      float col[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) col[i] = (i <= lane && lane < nb) ? S[(k0 + i) * lds + k0 + lane] : 0.f;
+      int bad = 0;
+      float mn = INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j < nb && !bad) {
+          const float d = __shfl_sync(0xffffffffu, col[j], j);
+          if (!isfinite(d)) bad = (int)(ST_BREAKDOWN | ST_NONFINITE);
+          else if (!(d > 0.f)) bad = (int)ST_BREAKDOWN;
+          if (!bad) {
+            mn = fminf(mn, d);
+            const float piv = sqrtf(d);
+            if (lane == j) col[j] = piv;
+            else if (lane > j) col[j] = col[j] / piv;          // Rc[j][lane]
+#pragma unroll
+            for (int i = j + 1; i < 32; ++i) {
+              const float rji = __shfl_sync(0xffffffffu, col[j], i);   // Rc[j][i]
+              if (lane >= i) col[i] = fmaf(-rji, col[j], col[i]);
+            }
+          }
+        }
+      }
+      if (lane == 0) { *s_bad = bad; *s_min = fminf(*s_min, mn); }
+      if (!bad) {
+        // T_pp = Rc_pp^{-1}, column `lane`: t[i] = T_pp[i][lane]
+        float t[32];
+#pragma unroll
+        for (int i = 31; i >= 0; --i) {
+          const float rii = __shfl_sync(0xffffffffu, col[i], i);
+          float sum = 0.f;
+#pragma unroll
+          for (int k = i + 1; k < 32; ++k) {
+            const float rik = __shfl_sync(0xffffffffu, col[i], k);   // Rc[i][k]
+            if (k <= lane) sum = fmaf(rik, t[k], sum);
+          }
+          t[i] = i == lane ? 1.f / rii : (i < lane ? -sum / rii : 0.f);
+        }
+        if (lane < nb) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i <= lane) S[(k0 + i) * lds + k0 + lane] = col[i];     // Rc (upper, with the diagonal)
+            if (i < lane) S[(k0 + lane) * lds + k0 + i] = t[i];        // T (lower, transposed)
+            if (i == lane) tdiag[k0 + lane] = t[i];
+          }
+        }
+      }
     }
     __syncthreads();
     if (*s_bad) return *s_bad;
-    const float inv = 1.f / *s_piv;
-    for (long long c = jj + 1 + tid; c < r; c += nth) S[jj * lds + c] *= inv;
+    const int c0 = k0 + nb;
+    if (c0 >= r) break;
+    const int n2 = r - c0;
+    // (2) row panel Rc[k0 + i][c] = sum_{t <= i} T_pp[t][i] S[k0 + t][c], via scratch
+    for (int e = tid; e < nb * n2; e += nth) {
+      const int i = e / n2, c = c0 + e % n2;
+      float y = 0.f;
+      for (int t = 0; t <= i; ++t) y = fmaf(Tv(S, lds, tdiag, r, k0 + t, k0 + i), S[(k0 + t) * lds + c], y);
+      scratch[e] = y;
+    }
     __syncthreads();
-    for (long long a = jj + 1 + warp; a < r; a += nwarp) {
-      const float sa = S[jj * lds + a];
-      for (long long c = a + lane; c < r; c += 32) S[a * lds + c] -= sa * S[jj * lds + c];
+    for (int e = tid; e < nb * n2; e += nth) {
+      const int i = e / n2, c = c0 + e % n2;
+      S[(k0 + i) * lds + c] = scratch[e];
+    }
+    __syncthreads();
+    // (3) trailing update of the upper triangle: S[a][c] -= sum_i Rc[k0 + i][a] Rc[k0 + i][c]
+    for (int e = tid; e < n2 * n2; e += nth) {
+      const int a = c0 + e / n2, c = c0 + e % n2;
+      if (a > c) continue;
+      float v = S[a * lds + c];
+#pragma unroll 8
+      for (int i = 0; i < nb; ++i) v = fmaf(-S[(k0 + i) * lds + a], S[(k0 + i) * lds + c], v);
+      S[a * lds + c] = v;
     }
     __syncthreads();
   }
   return 0;
 }
 
-// reduced != 0: the partials were already summed into partial 0 by k_gram_reduce.
-__global__ void __launch_bounds__(CHOL_NT) k_chol_inv(const OrthJob* __restrict__ jobs, int pass, int use_smem,
-                                                     int reduced) {
+// Off-diagonal blocks of T = Rc^{-1}, by block diagonals d = q - p:
+//   T_pq = -T_pp (sum_{k = p+1..q} Rc_pk T_kq),
+// with the diagonal blocks T_pp already in place.  `scratch` holds 32 * r floats.
+__device__ void inverse_blocks(float* S, int lds, int r, float* tdiag, float* scratch) {
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const int np = (int)((r + 31) / 32);
+  for (int d = 1; d < np; ++d) {
+    const int nout = (int)(np - d) * 1024;
+    for (int e = tid; e < nout; e += nth) {
+      const int p = (int)(e >> 10), i = (int)((e >> 5) & 31), j = (int)(e & 31), q = p + d;
+      const int a = 32 * p + i, c = 32 * q + j;
+      float sum = 0.f;
+      for (int kk = 32 * (p + 1); kk < min(r, 32 * (q + 1)); ++kk)
+        sum = fmaf(Rv(S, lds, r, a, kk), Tv(S, lds, tdiag, r, kk, c), sum);
+      scratch[e] = sum;   // C_pq[i][j]
+    }
+    __syncthreads();
+    for (int e = tid; e < nout; e += nth) {
+      const int p = (int)(e >> 10), i = (int)((e >> 5) & 31), j = (int)(e & 31), q = p + d;
+      const int a = 32 * p + i, c = 32 * q + j;
+      if (a >= r || c >= r) continue;
+      float sum = 0.f;
+      for (int t = i; t < 32; ++t) sum = fmaf(Tv(S, lds, tdiag, r, a, 32 * p + t), scratch[(p << 10) + t * 32 + j], sum);
+      S[c * lds + a] = -sum;
+    }
+    __syncthreads();
+  }
+}
+
+template <bool SMEM>
+__global__ void __launch_bounds__(CHOL_NT, 1) k_chol_inv(const OrthJob* __restrict__ jobs, int pass, int reduced) {
   extern __shared__ float sm_dyn[];
   const OrthJob& o = jobs[blockIdx.x];
   __shared__ int s_bad;
-  __shared__ float s_piv, s_min, s_max;
+  __shared__ float s_min, s_max;
   __shared__ float s_trace[CHOL_NT / 32];
   if (*o.status & ST_FATAL) return;
   if (pass == 2 && !*o.flag) return;
   const int tid = threadIdx.x, nth = blockDim.x;
-  const long long r = o.r, rp = o.rp;
-  float* S = use_smem ? sm_dyn : o.S;
-  const long long lds = use_smem ? r + 1 : rp;
+  const int r = o.r, rp = o.rp;
+  // shared (or the job's global scratch): S r x lds, tdiag r, scratch 32 r
+  float* S = SMEM ? sm_dyn : o.S;
+  const int lds = SMEM ? r + 1 : rp;
+  float* tdiag = S + r * lds;
+  float* scratch = tdiag + r;
   const int nchunk = reduced ? 1 : o.nchunk;
   chol_load(o, nchunk, S, lds, 0.f, s_trace);
-  int bad = chol_factor(S, lds, r, &s_piv, &s_bad, &s_min, &s_max);
+  int bad = chol_factor(S, lds, r, tdiag, scratch, &s_bad, &s_min, &s_max);
   if (pass == 0 && (bad || s_min < 1e-6f * s_max)) {
     float trace = 0.f;
     for (int w = 0; w < nth / 32; ++w) trace += s_trace[w];
     const float shift = 11.f * ((float)o.rows * (float)r + (float)r * (float)(r + 1)) * 5.9604645e-8f * trace;
     __syncthreads();
     chol_load(o, nchunk, S, lds, shift, s_trace);
-    bad = chol_factor(S, lds, r, &s_piv, &s_bad, &s_min, &s_max);
+    bad = chol_factor(S, lds, r, tdiag, scratch, &s_bad, &s_min, &s_max);
     if (!bad && tid == 0) { *o.flag = 1u; atomicOr(o.status, ST_SHIFTED); }
   }
   if (bad) {
     if (tid == 0) atomicOr(o.status, (unsigned)bad);
     return;
   }
-  // T = Rc^{-1}, one column per warp with no block-wide barrier:
-  //   T[c][c] = 1 / Rc[c][c];  T[a][c] = -(sum_{k=a+1..c} Rc[a][k] T[k][c]) / Rc[a][a],  a = c-1 .. 0.
-  // Column c of T (a < c) is kept in row c of S's lower triangle, its diagonal in tdiag[c].
-  float* tdiag = use_smem ? sm_dyn + r * lds : o.S + rp * rp;   // r floats of scratch
-  const int warp = tid >> 5, lane = tid & 31, nwarp = nth >> 5;
-  for (long long c = warp; c < r; c += nwarp) {
-    const float tcc = 1.f / S[c * lds + c];
-    for (long long a = c - 1; a >= 0; --a) {
-      float sum = 0.f;
-      for (long long k = a + 1 + lane; k <= c; k += 32)
-        sum = fmaf(S[a * lds + k], k == c ? tcc : S[c * lds + k], sum);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      if (lane == 0) S[c * lds + a] = -sum / S[a * lds + a];
-      __syncwarp();
-    }
-    if (lane == 0) tdiag[c] = tcc;
-  }
-  __syncthreads();
-  // T (row-major rp x rp, zero outside the upper triangle) and T^T split for the tensor core
-  float* T = o.T;
-  for (long long e = tid; e < rp * rp; e += nth) {
-    const long long a = e / rp, c = e % rp;
-    float v = 0.f;
-    if (a < r && c < r) v = a < c ? S[c * lds + a] : (a == c ? tdiag[a] : 0.f);
-    if (!o.Tt_hi) T[e] = v;
-    else {
+  inverse_blocks(S, lds, r, tdiag, scratch);
+  // outputs: T^T split for the tensor core (row c of T^T = column c of T), or T
+  if (o.Tt_hi) {
+    for (int e = tid; e < rp * rp; e += nth) {
+      const int c = e / rp, a = e % rp;
       float h, l;
-      tc::split_tf32(v, h, l);
-      o.Tt_hi[c * rp + a] = h;   // Tt[c][a] = T[a][c]
-      o.Tt_lo[c * rp + a] = l;
+      tc::split_tf32(a < r ? Tv(S, lds, tdiag, r, a, c) : 0.f, h, l);
+      o.Tt_hi[e] = h;
+      o.Tt_lo[e] = l;
+    }
+  } else {
+    for (int e = tid; e < rp * rp; e += nth) {
+      const int a = e / rp, c = e % rp;
+      o.T[e] = a < r ? Tv(S, lds, tdiag, r, a, c) : 0.f;
     }
   }
 }

@@ -5,15 +5,16 @@
 //     T1 = U Vbar^T,  T2 = U W^T            (K = r, 3xTF32, fp32 accumulation in TMEM)
 //     X <- X - eta s T1,   R <- beta (G + R - T2)
 //
-// One CTA per SM, persistent over 128 x 64 tiles of every m x n matrix.
+// One CTA per SM, persistent over 128 x 128 tiles of every m x n matrix.
 // Warp roles:
 //   0  TMA producer of the MMA operands (U hi/lo rows; [Vbar; W] hi/lo rows)
 //   1  TMEM allocator and MMA issuer (one thread)
 //   2  TMA producer of the streamed state (G, R, X in 16-column sub-chunks)
 //   3  idle
 //   4-7 epilogue: TMEM -> registers, update in the staging buffers, TMA store
-// The accumulator is double-buffered in TMEM (2 x 128 columns: T1 | T2) so the
-// MMAs of the next tile overlap the epilogue of this one.
+// The accumulator is double-buffered in TMEM (2 x 256 columns: T1 | T2) so the
+// MMAs of the next tile overlap the epilogue of this one.  Operand stages hold
+// 16 of K (64-byte swizzle), three in flight.
 #pragma once
 
 #include "common.cuh"
@@ -25,21 +26,20 @@ namespace tcepi {
 using namespace dion::tc;
 
 constexpr int BM = 128;          // rows of X per tile (TMEM lanes)
-constexpr int BNJ = 64;          // columns of X per tile
+constexpr int BNJ = 128;         // columns of X per tile
 constexpr int NMMA = 2 * BNJ;    // MMA N: [Vbar rows | W rows]
-constexpr int BK = 32;           // K per operand stage (one 128-byte swizzle row of fp32)
-constexpr int OSTAGES = 2;       // operand ring
+constexpr int BK = 16;           // K per operand stage (one 64-byte swizzle row of fp32)
+constexpr int OSTAGES = 3;       // operand ring
 constexpr int SUB = 16;          // columns per streamed sub-chunk
-constexpr int QSTAGES = 4;       // streamed-state ring
+constexpr int QSTAGES = 3;       // streamed-state ring
 constexpr int NTHREADS = 256;
-constexpr uint32_t TMEM_COLS = 256;   // 2 accumulators x NMMA
+constexpr uint32_t TMEM_COLS = 512;   // 2 accumulators x NMMA
 
-constexpr uint32_t A_BYTES = BM * BK * 4;            // 16 KB
-constexpr uint32_t BH_BYTES = NMMA * BK * 4;         // 16 KB ([Vbar; W] 128 rows)
-constexpr uint32_t OST_BYTES = 2 * A_BYTES + 2 * BH_BYTES;   // 64 KB
-constexpr uint32_t G_BYTES_MAX = BM * SUB * 4;       // 8 KB (fp32 G), 4 KB for bf16
+constexpr uint32_t A_BYTES = BM * BK * 4;            // 8 KB
+constexpr uint32_t BH_BYTES = NMMA * BK * 4;         // 16 KB ([Vbar; W] 256 rows)
+constexpr uint32_t OST_BYTES = 2 * A_BYTES + 2 * BH_BYTES;   // 48 KB
 constexpr uint32_t RX_BYTES = BM * SUB * 4;          // 8 KB
-constexpr uint32_t QST_BYTES = 8192 + 2 * RX_BYTES;  // 24 KB (1024-aligned pieces)
+constexpr uint32_t QST_BYTES = 8192 + 2 * RX_BYTES;  // 24 KB (G | R | X, 1024-aligned pieces)
 constexpr uint32_t SMEM_BYTES = 1024 + OSTAGES * OST_BYTES + QSTAGES * QST_BYTES + 512;
 
 enum { MAP_UH, MAP_UL, MAP_VH, MAP_VL, MAP_WH, MAP_WL, MAP_G, MAP_R, MAP_X, NMAPS };
@@ -53,20 +53,10 @@ struct EpiMat {
 };
 static_assert(sizeof(EpiMat) % 64 == 0, "EpiMat must keep 64-byte alignment of its maps");
 
+// One 128 x 128 tile of matrix `mat` at rows i0.., columns j0.. (host-built table).
 struct Tile {
-  int mat, i0, j0;
+  int mat, i0, j0, pad;
 };
-
-__device__ __forceinline__ Tile tile_of(const EpiMat* __restrict__ mats, const int* __restrict__ tstart, int nmat,
-                                        int t) {
-  Tile r;
-  r.mat = find_job(tstart, nmat, t);
-  const int local = t - tstart[r.mat];
-  const int ntj = (mats[r.mat].n + BNJ - 1) / BNJ;
-  r.i0 = (local / ntj) * BM;
-  r.j0 = (local % ntj) * BNJ;
-  return r;
-}
 
 __device__ __forceinline__ bool skip(const EpiMat& e) { return (*e.status & ST_FATAL) != 0; }
 
@@ -76,7 +66,7 @@ __device__ __forceinline__ int nsub(const EpiMat& e, int j0) {
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-k_epi(const EpiMat* __restrict__ mats, const int* __restrict__ tstart, int nmat, int ntiles) {
+k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntiles) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* ost = smem;                                   // operand ring
@@ -111,9 +101,9 @@ k_epi(const EpiMat* __restrict__ mats, const int* __restrict__ tstart, int nmat,
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------- operand producer
     int s = 0; uint32_t ph = 0;
-    uint32_t last_ph[OSTAGES] = {0, 0}; bool used[OSTAGES] = {false, false};
+    uint32_t last_ph[OSTAGES] = {0, 0, 0}; bool used[OSTAGES] = {false, false, false};
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const Tile tl = tile_of(mats, tstart, nmat, t);
+      const Tile tl = tiles[t];
       const EpiMat& e = mats[tl.mat];
       if (skip(e)) continue;
       const int nk = (e.rp + BK - 1) / BK;
@@ -141,7 +131,7 @@ k_epi(const EpiMat* __restrict__ mats, const int* __restrict__ tstart, int nmat,
     int s = 0; uint32_t ph = 0; int b = 0; uint32_t aph[2] = {0, 0};
     bool issued = false;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const Tile tl = tile_of(mats, tstart, nmat, t);
+      const Tile tl = tiles[t];
       const EpiMat& e = mats[tl.mat];
       if (skip(e)) continue;
       const int nk = (e.rp + BK - 1) / BK;
@@ -156,9 +146,9 @@ k_epi(const EpiMat* __restrict__ mats, const int* __restrict__ tstart, int nmat,
 #pragma unroll
         for (int kk = 0; kk < BK / 8; ++kk) {
           const uint32_t o = kk * 32;
-          mma_tf32(d, sdesc_k_sw128(al + o), sdesc_k_sw128(bh + o), idesc, (kc | kk) != 0);
-          mma_tf32(d, sdesc_k_sw128(ah + o), sdesc_k_sw128(bl + o), idesc, 1);
-          mma_tf32(d, sdesc_k_sw128(ah + o), sdesc_k_sw128(bh + o), idesc, 1);
+          mma_tf32(d, sdesc_k_sw64(al + o), sdesc_k_sw64(bh + o), idesc, (kc | kk) != 0);
+          mma_tf32(d, sdesc_k_sw64(ah + o), sdesc_k_sw64(bl + o), idesc, 1);
+          mma_tf32(d, sdesc_k_sw64(ah + o), sdesc_k_sw64(bh + o), idesc, 1);
         }
         issued = true;
         mma_commit(&op_empty[s]);
@@ -172,9 +162,9 @@ k_epi(const EpiMat* __restrict__ mats, const int* __restrict__ tstart, int nmat,
   } else if (warp == 2 && lane == 0) {
     // ---------------------------------------------------------- streamed-state producer
     int q = 0; uint32_t ph = 0;
-    uint32_t last_ph[QSTAGES] = {0, 0, 0, 0}; bool used[QSTAGES] = {false, false, false, false};
+    uint32_t last_ph[QSTAGES] = {0, 0, 0}; bool used[QSTAGES] = {false, false, false};
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const Tile tl = tile_of(mats, tstart, nmat, t);
+      const Tile tl = tiles[t];
       const EpiMat& e = mats[tl.mat];
       if (skip(e)) continue;
       const uint32_t gbytes = e.g_bf16 ? BM * SUB * 2 : BM * SUB * 4;
@@ -203,7 +193,7 @@ k_epi(const EpiMat* __restrict__ mats, const int* __restrict__ tstart, int nmat,
     int q = 0; uint32_t ph = 0;
     int prev_q = -1;   // staging slot whose TMA stores are still reading it (leader only)
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const Tile tl = tile_of(mats, tstart, nmat, t);
+      const Tile tl = tiles[t];
       const EpiMat& e = mats[tl.mat];
       if (skip(e)) continue;
       // every wait is followed by a vote of the 128 epilogue threads, so that

@@ -38,6 +38,11 @@ constexpr uint32_t OST_BYTES = 2 * OP_BYTES;             // 64 KB
 constexpr uint32_t SST_BYTES = RP_MAX * BK * 4;          // 24 KB: rp / 32 boxes of 32 x 32
 constexpr uint32_t SMEM_BYTES = 1024 + OSTAGES * OST_BYTES + SSTAGES * SST_BYTES + 512;
 
+// One 256-row chunk `chunk` of job `job` (host-built table).
+struct GItem {
+  int job, chunk, pad0, pad1;
+};
+
 struct GJob {
   CUtensorMap mA;            // A (rows x rp fp32), box 32 (columns) x 32 (rows), 128-byte swizzle
   float* gpart;              // nchunk x rp x rp
@@ -54,7 +59,7 @@ __device__ __forceinline__ bool skip(const GJob& j) {
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-k_gram(const GJob* __restrict__ jobs, const int* __restrict__ tstart, int njob, int nitems) {
+k_gram(const GJob* __restrict__ jobs, const GItem* __restrict__ items, int nitems) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* ost = smem;
@@ -92,10 +97,10 @@ k_gram(const GJob* __restrict__ jobs, const int* __restrict__ tstart, int njob, 
     int ss = 0; uint32_t sph = 0;
     uint32_t slast[SSTAGES] = {0, 0}; bool sused[SSTAGES] = {false, false};
     for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
-      const int jb = find_job(tstart, njob, t);
+      const int jb = items[t].job;
       const GJob& j = jobs[jb];
       if (skip(j)) continue;
-      const int r0 = (t - tstart[jb]) * CHUNK_ROWS;
+      const int r0 = items[t].chunk * CHUNK_ROWS;
       const int nk = (min(j.rows - r0, CHUNK_ROWS) + BK - 1) / BK;
       const int nbox = j.rp / 32;
       for (int kc = 0; kc < nk; ++kc) {
@@ -115,10 +120,10 @@ k_gram(const GJob* __restrict__ jobs, const int* __restrict__ tstart, int njob, 
     int os = 0; uint32_t oph = 0; uint32_t aph = 0;
     bool issued = false;
     for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
-      const int jb = find_job(tstart, njob, t);
+      const int jb = items[t].job;
       const GJob& j = jobs[jb];
       if (skip(j)) continue;
-      const int r0 = (t - tstart[jb]) * CHUNK_ROWS;
+      const int r0 = items[t].chunk * CHUNK_ROWS;
       const int nk = (min(j.rows - r0, CHUNK_ROWS) + BK - 1) / BK;
       const int nblk = j.rp > 128 ? 2 : 1;
       const uint32_t idesc = idesc_tf32(128, j.rp);
@@ -156,10 +161,10 @@ k_gram(const GJob* __restrict__ jobs, const int* __restrict__ tstart, int njob, 
     const int blk = cw >> 2;                 // Gram block drained by this warp
     int os = 0, ss = 0; uint32_t oph = 0, sph = 0; uint32_t aph = 0;
     for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
-      const int jb = find_job(tstart, njob, t);
+      const int jb = items[t].job;
       const GJob& j = jobs[jb];
       if (skip(j)) continue;
-      const int ch = t - tstart[jb];
+      const int ch = items[t].chunk;
       const int r0 = ch * CHUNK_ROWS;
       const int nk = (min(j.rows - r0, CHUNK_ROWS) + BK - 1) / BK;
       bool ok = true;

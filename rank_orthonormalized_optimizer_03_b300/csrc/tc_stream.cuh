@@ -7,9 +7,11 @@
 //
 // M is never stored: every CTA streams G and R tiles by TMA into a staging
 // ring, and 8 converter warps form M = G + R in fp32, split it into the two
-// tf32 halves of a 3xTF32 product and write them into the 128-byte-swizzled
-// K-major operand layout the MMA reads (transposing on the way for M^T).  The
-// second operand (V^T or U^T, already split) comes in by TMA.
+// tf32 halves of a 3xTF32 product and write them into the 64-byte-swizzled
+// K-major operand layout the MMA reads (transposing 4 x 2 register blocks on
+// the way for M^T).  The second operand (V^T or U^T, already split) comes in by
+// TMA.  Chunks of 16 along K keep four operand and four staging stages in
+// flight in shared memory.
 //
 // The tensor core's fp32 accumulation truncates: its bias grows with the
 // number of accumulation steps (measured -1e-5 relative per 1024 of K).  So a
@@ -17,8 +19,8 @@
 // converter warps, between conversions, add finished slices into registers in
 // round-to-nearest fp32; the bias then stays near 2e-6.
 //
-// Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..9 converter and
-// slice drain.  One CTA per SM, persistent over (row tile, K range, column
+// Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..9 converters
+// (two groups of four, alternate chunks) and slice drain.  One CTA per SM, persistent over (row tile, K range, column
 // block) items of every matrix.
 #pragma once
 
@@ -31,20 +33,21 @@ namespace tcstream {
 using namespace dion::tc;
 
 constexpr int BM = 128;              // output rows per tile (TMEM lanes)
-constexpr int BK = 32;               // K per chunk
-constexpr int SLICE = 8;             // chunks per TMEM slice (256 of K)
-constexpr int OSTAGES = 2;
-constexpr int SSTAGES = 2;
+constexpr int BK = 16;               // K per chunk: one 64-byte swizzle row of fp32
+constexpr int SLICE = 16;            // chunks per TMEM slice (256 of K)
+constexpr int OSTAGES = 4;
+constexpr int SSTAGES = 4;
 constexpr int NCONV = 8;             // converter / drain warps
 constexpr int NTHREADS = (2 + NCONV) * 32;
 constexpr int BN_MAX = 192;          // widest column block (TMEM: 2 x 192 <= 512)
 constexpr int HALF_MAX = BN_MAX / 2; // accumulator columns per converter thread
 constexpr uint32_t TMEM_COLS = 512;
 
-constexpr uint32_t A_BYTES = BM * BK * 4;                // 16 KB
-constexpr uint32_t B_BYTES_MAX = BN_MAX * BK * 4;        // 24 KB
-constexpr uint32_t OST_BYTES = 2 * A_BYTES + 2 * B_BYTES_MAX;   // 80 KB
-constexpr uint32_t SST_BYTES = 32768;                    // G (<= 16 KB) | R (16 KB)
+constexpr uint32_t A_BYTES = BM * BK * 4;                // 8 KB
+constexpr uint32_t B_BYTES_MAX = BN_MAX * BK * 4;        // 12 KB
+constexpr uint32_t OST_BYTES = 2 * A_BYTES + 2 * B_BYTES_MAX;   // 40 KB
+constexpr uint32_t SST_BYTES = 16384;                    // G (<= 8 KB) | R (8 KB)
+constexpr uint32_t SST_R = 8192;                         // offset of the R tile in a staging stage
 constexpr uint32_t SMEM_BYTES = 1024 + OSTAGES * OST_BYTES + SSTAGES * SST_BYTES + 512;
 
 // gmode: what the staged tiles hold.  G_BF16 / G_F32: M = G + R (phases a, c);
@@ -71,26 +74,11 @@ struct SJob {
 };
 static_assert(sizeof(SJob) % 64 == 0, "SJob must keep 64-byte alignment of its maps");
 
+// One work item (host-built table, heaviest first): output rows row0..row0+127 of
+// job `job`, K range [k0, k0 + 16 nk) (partial `ks`), output columns from c0.
 struct Item {
-  int job, row0, ks, c0, k0, nk;
+  int job, row0, ks, c0, k0, nk, pad0, pad1;
 };
-
-__device__ __forceinline__ Item item_of(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob,
-                                        int t) {
-  Item it;
-  it.job = find_job(tstart, njob, t);
-  const SJob& j = jobs[it.job];
-  int local = t - tstart[it.job];
-  const int cb = local % j.ncb;
-  local /= j.ncb;
-  it.ks = local % j.ksplit;
-  it.row0 = (local / j.ksplit) * BM;
-  it.c0 = cb * j.bn;
-  it.k0 = it.ks * j.kchunk;
-  const int k1 = min(j.kdim, it.k0 + j.kchunk);
-  it.nk = (k1 - it.k0 + BK - 1) / BK;
-  return it;
-}
 
 __device__ __forceinline__ bool skip(const SJob& j) {
   return (*j.status & ST_FATAL) != 0 || (j.pass == 2 && !*j.flag);
@@ -113,16 +101,16 @@ __device__ __forceinline__ void drain_add(uint32_t taddr, int half, float (&acc)
 
 template <bool TRANS>
 __global__ void __launch_bounds__(NTHREADS, 1)
-k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob, int nitems) {
+k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nitems) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* ost = smem;
   unsigned char* sst = smem + OSTAGES * OST_BYTES;
   uint64_t* bars = (uint64_t*)(sst + SSTAGES * SST_BYTES);
-  uint64_t* o_full = bars;                 // B bytes (TMA) + NCONV converter arrivals
+  uint64_t* o_full = bars;                 // B bytes (TMA) + NCONV / 2 converter arrivals
   uint64_t* o_empty = o_full + OSTAGES;    // MMA commit
   uint64_t* s_full = o_empty + OSTAGES;    // staging bytes (TMA)
-  uint64_t* s_empty = s_full + SSTAGES;    // NCONV converter arrivals
+  uint64_t* s_empty = s_full + SSTAGES;    // NCONV / 2 converter arrivals
   uint64_t* acc_full = s_empty + SSTAGES;  // MMA commit per slice
   uint64_t* acc_empty = acc_full + 2;      // NCONV drain arrivals
   uint64_t* drain = acc_empty + 2;
@@ -131,8 +119,9 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < OSTAGES; ++i) { mbar_init(&o_full[i], 1 + NCONV); mbar_init(&o_empty[i], 1); }
-    for (int i = 0; i < SSTAGES; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], NCONV); }
+    // a chunk is converted by one group of NCONV / 2 warps
+    for (int i = 0; i < OSTAGES; ++i) { mbar_init(&o_full[i], 1 + NCONV / 2); mbar_init(&o_empty[i], 1); }
+    for (int i = 0; i < SSTAGES; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], NCONV / 2); }
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], NCONV); }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -151,7 +140,7 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
     uint32_t olast[OSTAGES] = {0, 0}, slast[SSTAGES] = {0, 0};
     bool oused[OSTAGES] = {false, false}, sused[SSTAGES] = {false, false};
     for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
-      const Item it = item_of(jobs, tstart, njob, t);
+      const Item it = items[t];
       const SJob& j = jobs[it.job];
       if (skip(j)) continue;
       const uint32_t gbytes = j.gmode == G_NONE ? 0u : BM * BK * (j.gmode == G_BF16 ? 2 : 4);
@@ -163,17 +152,17 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
         mbar_arrive_expect_tx(&s_full[ss], gbytes + BM * BK * 4);
         {
           unsigned char* gdst = sst + ss * SST_BYTES;
-          unsigned char* rdst = gdst + 16384;
+          unsigned char* rdst = gdst + SST_R;
           if (!TRANS) {
             if (j.gmode != G_NONE) tma_load_2d(gdst, &j.mG, &s_full[ss], k, it.row0);
             tma_load_2d(rdst, &j.mR, &s_full[ss], k, it.row0);
           } else {
-            // rows k..k+31 of M, columns row0..row0+127 (boxes of 128 bytes per row)
+            // rows k..k+15 of M, columns row0..row0+127, in boxes of 128 bytes per row
             const int gbox = j.gmode == G_BF16 ? 64 : 32;
             for (int b = 0; b < BM / gbox; ++b)
-              tma_load_2d(gdst + b * 4096, &j.mG, &s_full[ss], it.row0 + b * gbox, k);
+              tma_load_2d(gdst + b * 2048, &j.mG, &s_full[ss], it.row0 + b * gbox, k);
             for (int b = 0; b < BM / 32; ++b)
-              tma_load_2d(rdst + b * 4096, &j.mR, &s_full[ss], it.row0 + b * 32, k);
+              tma_load_2d(rdst + b * 2048, &j.mR, &s_full[ss], it.row0 + b * 32, k);
           }
         }
         sused[ss] = true; slast[ss] = sph;
@@ -200,7 +189,7 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
     int os = 0; uint32_t oph = 0; int b = 0; uint32_t aph[2] = {0, 0};
     bool issued = false;
     for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
-      const Item it = item_of(jobs, tstart, njob, t);
+      const Item it = items[t];
       const SJob& j = jobs[it.job];
       if (skip(j)) continue;
       const uint32_t idesc = idesc_tf32(BM, j.bn);
@@ -217,9 +206,9 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
 #pragma unroll
         for (int kk = 0; kk < BK / 8; ++kk) {
           const uint32_t o = kk * 32;
-          mma_tf32(d, sdesc_k_sw128(al + o), sdesc_k_sw128(bh + o), idesc, ((kc % SLICE) | kk) != 0);
-          mma_tf32(d, sdesc_k_sw128(ah + o), sdesc_k_sw128(bl + o), idesc, 1);
-          mma_tf32(d, sdesc_k_sw128(ah + o), sdesc_k_sw128(bh + o), idesc, 1);
+          mma_tf32(d, sdesc_k_sw64(al + o), sdesc_k_sw64(bh + o), idesc, ((kc % SLICE) | kk) != 0);
+          mma_tf32(d, sdesc_k_sw64(ah + o), sdesc_k_sw64(bl + o), idesc, 1);
+          mma_tf32(d, sdesc_k_sw64(ah + o), sdesc_k_sw64(bh + o), idesc, 1);
         }
         issued = true;
         mma_commit(&o_empty[os]);
@@ -234,15 +223,21 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
     if (*abort_flag && issued) { mma_commit(drain); mbar_wait_drain(drain, 0); }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ converters + slice drain
+    // Two groups of four warps convert alternate chunks (group g takes the chunks
+    // whose sequence number is g mod 2, i.e. stages g and g + 2), so two chunks
+    // are in conversion at once.  For the drain every warp owns TMEM lane quarter
+    // (warp % 4) and column half g of the tile.
     const int cw = warp - 2;                 // 0..7
     const int quarter = warp & 3;            // TMEM lane quarter of this warp
-    const int h = cw >> 2;                   // K half (conversion) and column half (drain)
+    const int g = cw >> 2;                   // converter group; column half for the drain
+    const int gt = (cw & 3) * 32 + lane;     // thread index within the group, 0..127
     const int row = quarter * 32 + lane;     // output row within the tile (TMEM lane)
-    int os = 0, ss = 0; uint32_t oph = 0, sph = 0;
+    uint32_t seq = (uint32_t)g;              // sequence number of this group's next chunk
     int b = 0; uint32_t aph[2] = {0, 0};
+    uint32_t base_seq = 0;                   // sequence number of the current item's first chunk
     float acc[HALF_MAX];
     for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
-      const Item it = item_of(jobs, tstart, njob, t);
+      const Item it = items[t];
       const SJob& j = jobs[it.job];
       if (skip(j)) continue;
       const int half = j.bn >> 1;
@@ -251,50 +246,52 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
 #pragma unroll
       for (int k = 0; k < HALF_MAX; ++k) acc[k] = 0.f;
       bool ok = true;
-      for (int kc = 0; kc < it.nk && ok; ++kc) {
-        // before the first chunk of slice s + 2, fold slice s into the registers
-        if (kc % SLICE == 0 && kc / SLICE >= 2) {
+      for (; ok && seq < base_seq + (uint32_t)it.nk; seq += 2) {
+        const int kc = (int)(seq - base_seq);
+        // before converting a chunk of slice s, fold every slice up to s - 2 into the registers
+        while (drained < kc / SLICE - 1) {
           if (!mbar_wait_warp(&acc_full[b], aph[b], abort_flag)) { failed = it.job; ok = false; break; }
           tc_fence_after();
-          drain_add(tmem + ((uint32_t)(quarter * 32) << 16) + b * BN_MAX + h * half, half, acc);
+          drain_add(tmem + ((uint32_t)(quarter * 32) << 16) + b * BN_MAX + g * half, half, acc);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[b]);
           aph[b] ^= 1; b ^= 1; ++drained;
         }
+        if (!ok) break;
+        const int ss = (int)(seq % SSTAGES), os = (int)(seq % OSTAGES);
+        const uint32_t sph = (seq / SSTAGES) & 1u, oph = (seq / OSTAGES) & 1u;
         if (!mbar_wait_warp(&s_full[ss], sph, abort_flag)) { failed = it.job; ok = false; break; }
         if (!mbar_wait_warp(&o_empty[os], oph ^ 1, abort_flag)) { failed = it.job; ok = false; break; }
         const unsigned char* gsrc = sst + ss * SST_BYTES;
-        const unsigned char* rsrc = gsrc + 16384;
+        const unsigned char* rsrc = gsrc + SST_R;
         unsigned char* ahp = ost + os * OST_BYTES;
         unsigned char* alp = ahp + A_BYTES;
         if (!TRANS) {
-          // row `row` of M, K elements [16h, 16h + 16) of this chunk
+          // row `row` of M, the chunk's 16 K elements (64-byte rows, 64-byte swizzle)
           float mv[16];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int ch = 4 * h + c;
-            const float4 r = *reinterpret_cast<const float4*>(rsrc + row * 128 + (((ch ^ row) & 7) << 4));
+            const float4 r = *reinterpret_cast<const float4*>(rsrc + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
             mv[4 * c] = r.x; mv[4 * c + 1] = r.y; mv[4 * c + 2] = r.z; mv[4 * c + 3] = r.w;
           }
           if (j.gmode == G_BF16) {
+            // 32-byte rows, 32-byte swizzle: 8 bf16 per 16-byte chunk
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-              const int ch = 2 * h + c;   // 64-byte rows, 64-byte swizzle
-              const uint4 v = *reinterpret_cast<const uint4*>(gsrc + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4));
+              const uint4 v = *reinterpret_cast<const uint4*>(gsrc + row * 32 + ((c ^ ((row >> 2) & 1)) << 4));
               const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                mv[c * 8 + 2 * k] += __uint_as_float(w[k] << 16);
-                mv[c * 8 + 2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+                mv[8 * c + 2 * k] += __uint_as_float(w[k] << 16);
+                mv[8 * c + 2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
               }
             }
           } else if (j.gmode == G_F32) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              const int ch = 4 * h + c;
-              const float4 g = *reinterpret_cast<const float4*>(gsrc + row * 128 + (((ch ^ row) & 7) << 4));
-              mv[4 * c] += g.x; mv[4 * c + 1] += g.y; mv[4 * c + 2] += g.z; mv[4 * c + 3] += g.w;
+              const float4 gv = *reinterpret_cast<const float4*>(gsrc + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+              mv[4 * c] += gv.x; mv[4 * c + 1] += gv.y; mv[4 * c + 2] += gv.z; mv[4 * c + 3] += gv.w;
             }
           }
 #pragma unroll
@@ -304,38 +301,45 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
             split_tf32(mv[4 * c + 1], hi.y, lo.y);
             split_tf32(mv[4 * c + 2], hi.z, lo.z);
             split_tf32(mv[4 * c + 3], hi.w, lo.w);
-            const uint32_t off = sw128_off(row, 16 * h + 4 * c);
+            const uint32_t off = sw64_off(row, 4 * c);
             *reinterpret_cast<float4*>(ahp + off) = hi;
             *reinterpret_cast<float4*>(alp + off) = lo;
           }
         } else {
-          // column `row` of M (row of M^T), K = rows [16h, 16h + 16) of this chunk
-          const int jb = row >> 5, jj = row & 31;
+          // a 4 (K = rows i of M) x 4 (columns j of M) block per thread, transposed in registers
+          const int ig = gt >> 5, jq = gt & 31;   // rows 4 ig .. 4 ig + 3, columns 4 jq .. 4 jq + 3
+          const int jb = jq >> 3, jj = (4 * jq) & 31;
+          float m[4][4];   // m[e][c] = M[4 ig + e][4 jq + c]
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float mv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int i = 16 * h + 4 * c + e;
-              float v = *reinterpret_cast<const float*>(rsrc + jb * 4096 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4) +
-                                                        ((jj & 3) << 2));
-              if (j.gmode == G_BF16) {
-                const int gb = row >> 6, gj = row & 63;
-                const uint16_t gv = *reinterpret_cast<const uint16_t*>(
-                    gsrc + gb * 4096 + i * 128 + ((((gj >> 3) ^ i) & 7) << 4) + ((gj & 7) << 1));
-                v += __uint_as_float((uint32_t)gv << 16);
-              } else {
-                v += *reinterpret_cast<const float*>(gsrc + jb * 4096 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4) +
-                                                     ((jj & 3) << 2));
-              }
-              mv[e] = v;
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * ig + e;
+            const float4 rv = *reinterpret_cast<const float4*>(rsrc + jb * 2048 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4));
+            m[e][0] = rv.x; m[e][1] = rv.y; m[e][2] = rv.z; m[e][3] = rv.w;
+            if (j.gmode == G_BF16) {
+              const int gb = jq >> 4, gj = (4 * jq) & 63;
+              const uint2 gv = *reinterpret_cast<const uint2*>(
+                  gsrc + gb * 2048 + i * 128 + ((((gj >> 3) ^ i) & 7) << 4) + ((gj & 7) << 1));
+              m[e][0] += __uint_as_float(gv.x << 16);
+              m[e][1] += __uint_as_float(gv.x & 0xFFFF0000u);
+              m[e][2] += __uint_as_float(gv.y << 16);
+              m[e][3] += __uint_as_float(gv.y & 0xFFFF0000u);
+            } else if (j.gmode == G_F32) {
+              const float4 gv = *reinterpret_cast<const float4*>(gsrc + jb * 2048 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4));
+              m[e][0] += gv.x; m[e][1] += gv.y; m[e][2] += gv.z; m[e][3] += gv.w;
             }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = (e + jq) & 3;            // rotated so that a quarter warp spreads over banks
+            float cv[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) cv[q4] = c == 0 ? m[q4][0] : c == 1 ? m[q4][1] : c == 2 ? m[q4][2] : m[q4][3];
             float4 hi, lo;
-            split_tf32(mv[0], hi.x, lo.x);
-            split_tf32(mv[1], hi.y, lo.y);
-            split_tf32(mv[2], hi.z, lo.z);
-            split_tf32(mv[3], hi.w, lo.w);
-            const uint32_t off = sw128_off(row, 16 * h + 4 * c);
+            split_tf32(cv[0], hi.x, lo.x);
+            split_tf32(cv[1], hi.y, lo.y);
+            split_tf32(cv[2], hi.z, lo.z);
+            split_tf32(cv[3], hi.w, lo.w);
+            const uint32_t off = sw64_off(4 * jq + c, 4 * ig);
             *reinterpret_cast<float4*>(ahp + off) = hi;
             *reinterpret_cast<float4*>(alp + off) = lo;
           }
@@ -346,19 +350,18 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
           mbar_arrive(&s_empty[ss]);
           mbar_arrive(&o_full[os]);
         }
-        if (++ss == SSTAGES) { ss = 0; sph ^= 1; }
-        if (++os == OSTAGES) { os = 0; oph ^= 1; }
       }
-      // the last (up to two) slices
+      // the remaining slices
       while (ok && drained < nslices) {
         if (!mbar_wait_warp(&acc_full[b], aph[b], abort_flag)) { failed = it.job; ok = false; break; }
         tc_fence_after();
-        drain_add(tmem + ((uint32_t)(quarter * 32) << 16) + b * BN_MAX + h * half, half, acc);
+        drain_add(tmem + ((uint32_t)(quarter * 32) << 16) + b * BN_MAX + g * half, half, acc);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[b]);
         aph[b] ^= 1; b ^= 1; ++drained;
       }
+      base_seq += (uint32_t)it.nk;
       if (!ok) break;
       const int grow = it.row0 + row;
       // destination: phases (a) / (c) write out (+ the K-range partial); orth() passes
@@ -373,7 +376,7 @@ k_stream(const SJob* __restrict__ jobs, const int* __restrict__ tstart, int njob
       }
       if (grow < j.rows) {
         dst += (long long)grow * ld;
-        const int cbase = it.c0 + h * half;
+        const int cbase = it.c0 + g * half;
 #pragma unroll
         for (int cb = 0; cb < HALF_MAX / 16; ++cb)
           if (cb * 16 < half) {
