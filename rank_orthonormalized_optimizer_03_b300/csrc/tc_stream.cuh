@@ -19,8 +19,8 @@
 // converter warps, between conversions, add finished slices into registers in
 // round-to-nearest fp32; the bias then stays near 2e-6.
 //
-// Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..9 converters
-// (two groups of four, alternate chunks) and slice drain.  One CTA per SM, persistent over (row tile, K range, column
+// Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..17 converters
+// (four groups of four, one stage each) and slice drain.  One CTA per SM, persistent over (row tile, K range, column
 // block) items of every matrix.
 #pragma once
 
@@ -37,10 +37,11 @@ constexpr int BK = 16;               // K per chunk: one 64-byte swizzle row of 
 constexpr int SLICE = 16;            // chunks per TMEM slice (256 of K)
 constexpr int OSTAGES = 4;
 constexpr int SSTAGES = 4;
-constexpr int NCONV = 8;             // converter / drain warps
+constexpr int NCONV = 16;            // converter / drain warps: four groups of four
+constexpr int NGROUP = 4;            // converter groups; group g converts the chunks of stage g (mod 4)
 constexpr int NTHREADS = (2 + NCONV) * 32;
 constexpr int BN_MAX = 192;          // widest column block (TMEM: 2 x 192 <= 512)
-constexpr int HALF_MAX = BN_MAX / 2; // accumulator columns per converter thread
+constexpr int QMAX = BN_MAX / 4;     // accumulator columns per converter thread (one column quarter)
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint32_t A_BYTES = BM * BK * 4;                // 8 KB
@@ -84,17 +85,17 @@ __device__ __forceinline__ bool skip(const SJob& j) {
   return (*j.status & ST_FATAL) != 0 || (j.pass == 2 && !*j.flag);
 }
 
-// Drain one finished TMEM slice (columns [col0, col0 + half) of this thread's
-// lane) into the register accumulator.
-__device__ __forceinline__ void drain_add(uint32_t taddr, int half, float (&acc)[HALF_MAX]) {
+// Drain one finished TMEM slice (columns [col0, col0 + quarter) of this
+// thread's lane, a multiple of 8) into the register accumulator.
+__device__ __forceinline__ void drain_add(uint32_t taddr, int quarter, float (&acc)[QMAX]) {
 #pragma unroll
-  for (int cb = 0; cb < HALF_MAX / 16; ++cb) {
-    if (cb * 16 < half) {
-      float v[16];
-      tmem_ld16(taddr + cb * 16, v);
+  for (int cb = 0; cb < QMAX / 8; ++cb) {
+    if (cb * 8 < quarter) {
+      float v[8];
+      tmem_ld8(taddr + cb * 8, v);
       tmem_wait_ld();
 #pragma unroll
-      for (int k = 0; k < 16; ++k) acc[cb * 16 + k] += v[k];
+      for (int k = 0; k < 8; ++k) acc[cb * 8 + k] += v[k];
     }
   }
 }
@@ -107,10 +108,10 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
   unsigned char* ost = smem;
   unsigned char* sst = smem + OSTAGES * OST_BYTES;
   uint64_t* bars = (uint64_t*)(sst + SSTAGES * SST_BYTES);
-  uint64_t* o_full = bars;                 // B bytes (TMA) + NCONV / 2 converter arrivals
+  uint64_t* o_full = bars;                 // B bytes (TMA) + NCONV / NGROUP converter arrivals
   uint64_t* o_empty = o_full + OSTAGES;    // MMA commit
   uint64_t* s_full = o_empty + OSTAGES;    // staging bytes (TMA)
-  uint64_t* s_empty = s_full + SSTAGES;    // NCONV / 2 converter arrivals
+  uint64_t* s_empty = s_full + SSTAGES;    // NCONV / NGROUP converter arrivals
   uint64_t* acc_full = s_empty + SSTAGES;  // MMA commit per slice
   uint64_t* acc_empty = acc_full + 2;      // NCONV drain arrivals
   uint64_t* drain = acc_empty + 2;
@@ -119,9 +120,9 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    // a chunk is converted by one group of NCONV / 2 warps
-    for (int i = 0; i < OSTAGES; ++i) { mbar_init(&o_full[i], 1 + NCONV / 2); mbar_init(&o_empty[i], 1); }
-    for (int i = 0; i < SSTAGES; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], NCONV / 2); }
+    // a chunk is converted by one group of NCONV / NGROUP warps
+    for (int i = 0; i < OSTAGES; ++i) { mbar_init(&o_full[i], 1 + NCONV / NGROUP); mbar_init(&o_empty[i], 1); }
+    for (int i = 0; i < SSTAGES; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], NCONV / NGROUP); }
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], NCONV); }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -223,36 +224,34 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
     if (*abort_flag && issued) { mma_commit(drain); mbar_wait_drain(drain, 0); }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ converters + slice drain
-    // Two groups of four warps convert alternate chunks (group g takes the chunks
-    // whose sequence number is g mod 2, i.e. stages g and g + 2), so two chunks
-    // are in conversion at once.  For the drain every warp owns TMEM lane quarter
-    // (warp % 4) and column half g of the tile.
-    const int cw = warp - 2;                 // 0..7
+    // Four groups of four warps; group g converts the chunks whose sequence number
+    // is g mod 4 (stage g), so four chunks are in conversion at once.  For the
+    // drain every warp owns TMEM lane quarter (warp % 4) and column quarter g.
+    const int cw = warp - 2;                 // 0..15
     const int quarter = warp & 3;            // TMEM lane quarter of this warp
-    const int g = cw >> 2;                   // converter group; column half for the drain
-    const int gt = (cw & 3) * 32 + lane;     // thread index within the group, 0..127
+    const int g = cw >> 2;                   // converter group; column quarter for the drain
     const int row = quarter * 32 + lane;     // output row within the tile (TMEM lane)
     uint32_t seq = (uint32_t)g;              // sequence number of this group's next chunk
     int b = 0; uint32_t aph[2] = {0, 0};
     uint32_t base_seq = 0;                   // sequence number of the current item's first chunk
-    float acc[HALF_MAX];
+    float acc[QMAX];
     for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
       const Item it = items[t];
       const SJob& j = jobs[it.job];
       if (skip(j)) continue;
-      const int half = j.bn >> 1;
+      const int qw = j.bn >> 2;              // columns per quarter
       const int nslices = (it.nk + SLICE - 1) / SLICE;
       int drained = 0;
 #pragma unroll
-      for (int k = 0; k < HALF_MAX; ++k) acc[k] = 0.f;
+      for (int k = 0; k < QMAX; ++k) acc[k] = 0.f;
       bool ok = true;
-      for (; ok && seq < base_seq + (uint32_t)it.nk; seq += 2) {
+      for (; ok && seq < base_seq + (uint32_t)it.nk; seq += NGROUP) {
         const int kc = (int)(seq - base_seq);
         // before converting a chunk of slice s, fold every slice up to s - 2 into the registers
         while (drained < kc / SLICE - 1) {
           if (!mbar_wait_warp(&acc_full[b], aph[b], abort_flag)) { failed = it.job; ok = false; break; }
           tc_fence_after();
-          drain_add(tmem + ((uint32_t)(quarter * 32) << 16) + b * BN_MAX + g * half, half, acc);
+          drain_add(tmem + ((uint32_t)(quarter * 32) << 16) + b * BN_MAX + g * qw, qw, acc);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[b]);
@@ -306,40 +305,37 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
             *reinterpret_cast<float4*>(alp + off) = lo;
           }
         } else {
-          // a 4 (K = rows i of M) x 4 (columns j of M) block per thread, transposed in registers
-          const int ig = gt >> 5, jq = gt & 31;   // rows 4 ig .. 4 ig + 3, columns 4 jq .. 4 jq + 3
-          const int jb = jq >> 3, jj = (4 * jq) & 31;
-          float m[4][4];   // m[e][c] = M[4 ig + e][4 jq + c]
+          // column `row` of M (row of the M^T operand), the chunk's 16 rows of M as K:
+          // scalar loads walk one staged row across the warp (conflict-free), the
+          // 16-byte stores go to 32 consecutive operand rows (conflict-free)
+          const int jb = row >> 5, jj = row & 31;
+          float mv[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = 4 * ig + e;
-            const float4 rv = *reinterpret_cast<const float4*>(rsrc + jb * 2048 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4));
-            m[e][0] = rv.x; m[e][1] = rv.y; m[e][2] = rv.z; m[e][3] = rv.w;
-            if (j.gmode == G_BF16) {
-              const int gb = jq >> 4, gj = (4 * jq) & 63;
-              const uint2 gv = *reinterpret_cast<const uint2*>(
+          for (int i = 0; i < 16; ++i)
+            mv[i] = *reinterpret_cast<const float*>(rsrc + jb * 2048 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4) +
+                                                    ((jj & 3) << 2));
+          if (j.gmode == G_BF16) {
+            const int gb = row >> 6, gj = row & 63;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint16_t gv = *reinterpret_cast<const uint16_t*>(
                   gsrc + gb * 2048 + i * 128 + ((((gj >> 3) ^ i) & 7) << 4) + ((gj & 7) << 1));
-              m[e][0] += __uint_as_float(gv.x << 16);
-              m[e][1] += __uint_as_float(gv.x & 0xFFFF0000u);
-              m[e][2] += __uint_as_float(gv.y << 16);
-              m[e][3] += __uint_as_float(gv.y & 0xFFFF0000u);
-            } else if (j.gmode == G_F32) {
-              const float4 gv = *reinterpret_cast<const float4*>(gsrc + jb * 2048 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4));
-              m[e][0] += gv.x; m[e][1] += gv.y; m[e][2] += gv.z; m[e][3] += gv.w;
+              mv[i] += __uint_as_float((uint32_t)gv << 16);
             }
+          } else if (j.gmode == G_F32) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              mv[i] += *reinterpret_cast<const float*>(gsrc + jb * 2048 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4) +
+                                                       ((jj & 3) << 2));
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = (e + jq) & 3;            // rotated so that a quarter warp spreads over banks
-            float cv[4];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) cv[q4] = c == 0 ? m[q4][0] : c == 1 ? m[q4][1] : c == 2 ? m[q4][2] : m[q4][3];
+          for (int c = 0; c < 4; ++c) {
             float4 hi, lo;
-            split_tf32(cv[0], hi.x, lo.x);
-            split_tf32(cv[1], hi.y, lo.y);
-            split_tf32(cv[2], hi.z, lo.z);
-            split_tf32(cv[3], hi.w, lo.w);
-            const uint32_t off = sw64_off(4 * jq + c, 4 * ig);
+            split_tf32(mv[4 * c], hi.x, lo.x);
+            split_tf32(mv[4 * c + 1], hi.y, lo.y);
+            split_tf32(mv[4 * c + 2], hi.z, lo.z);
+            split_tf32(mv[4 * c + 3], hi.w, lo.w);
+            const uint32_t off = sw64_off(row, 4 * c);
             *reinterpret_cast<float4*>(ahp + off) = hi;
             *reinterpret_cast<float4*>(alp + off) = lo;
           }
@@ -355,7 +351,7 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
       while (ok && drained < nslices) {
         if (!mbar_wait_warp(&acc_full[b], aph[b], abort_flag)) { failed = it.job; ok = false; break; }
         tc_fence_after();
-        drain_add(tmem + ((uint32_t)(quarter * 32) << 16) + b * BN_MAX + g * half, half, acc);
+        drain_add(tmem + ((uint32_t)(quarter * 32) << 16) + b * BN_MAX + g * qw, qw, acc);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[b]);
@@ -376,13 +372,13 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
       }
       if (grow < j.rows) {
         dst += (long long)grow * ld;
-        const int cbase = it.c0 + g * half;
+        const int cbase = it.c0 + g * qw;
 #pragma unroll
-        for (int cb = 0; cb < HALF_MAX / 16; ++cb)
-          if (cb * 16 < half) {
+        for (int cb = 0; cb < QMAX / 8; ++cb)
+          if (cb * 8 < qw) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-              if (cbase + cb * 16 + k < cols) dst[cbase + cb * 16 + k] = acc[cb * 16 + k];
+            for (int k = 0; k < 8; ++k)
+              if (cbase + cb * 8 + k < cols) dst[cbase + cb * 8 + k] = acc[cb * 8 + k];
           }
       }
     }
