@@ -83,6 +83,7 @@ struct dion_plan {
   std::vector<int> ts_sa, ts_sc, ts_tv, ts_tu;
   // tensor-core orth(): per list (0 = P, 1 = W, 2 = V) and pass, Gram and A T jobs
   bool tc_orth = false;
+  bool any_g_f32 = false;   // a gradient in fp32: larger staging slots
   std::vector<size_t> off_Tth, off_Ttl;
   size_t t_gj[3][3] = {}, t_tj[3][3] = {}, t_ts_g[3] = {}, t_ts_t[3] = {};
   std::vector<int> ts_g[3], ts_t[3], ts_gred[3];
@@ -194,6 +195,8 @@ void layout(dion_plan* p) {
     *ch = (int)c;
     *nch = (int)cdiv(rows, c);
   };
+  p->any_g_f32 = false;
+  for (int i = 0; i < cnt; ++i) p->any_g_f32 = p->any_g_f32 || p->descs[i].g_dtype == DION_DTYPE_F32;
   p->tc_orth = true;
   for (int i = 0; i < cnt; ++i) p->tc_orth = p->tc_orth && p->rp[i] <= tcgram::RP_MAX;
   for (int i = 0; i < cnt; ++i) {
@@ -816,7 +819,8 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
         const int tiles = (int)p->it_epi.size();
         const int grid = std::min(tiles, p->num_sms);
         tcepi::k_epi<<<grid, tcepi::NTHREADS, tcepi::SMEM_BYTES, s>>>(
-            tab<tcepi::EpiMat>(p, base, p->t_epi), tab<tcepi::Tile>(p, base, p->t_it_epi), tiles);
+            tab<tcepi::EpiMat>(p, base, p->t_epi), tab<tcepi::Tile>(p, base, p->t_it_epi), tiles,
+            p->any_g_f32 ? 24576 : 20480, p->any_g_f32 ? 3 : 4);
         break;
       }
     }

@@ -31,7 +31,7 @@ constexpr int NMMA = 2 * BNJ;    // MMA N: [Vbar rows | W rows]
 constexpr int BK = 16;           // K per operand stage (one 64-byte swizzle row of fp32)
 constexpr int OSTAGES = 3;       // operand ring
 constexpr int SUB = 16;          // columns per streamed sub-chunk
-constexpr int QSTAGES = 3;       // streamed-state ring
+constexpr int QSTAGES_MAX = 4;   // streamed-state ring; the slot count is chosen per launch
 constexpr int NTHREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;   // 2 accumulators x NMMA
 
@@ -39,8 +39,10 @@ constexpr uint32_t A_BYTES = BM * BK * 4;            // 8 KB
 constexpr uint32_t BH_BYTES = NMMA * BK * 4;         // 16 KB ([Vbar; W] 256 rows)
 constexpr uint32_t OST_BYTES = 2 * A_BYTES + 2 * BH_BYTES;   // 48 KB
 constexpr uint32_t RX_BYTES = BM * SUB * 4;          // 8 KB
-constexpr uint32_t QST_BYTES = 8192 + 2 * RX_BYTES;  // 24 KB (G | R | X, 1024-aligned pieces)
-constexpr uint32_t SMEM_BYTES = 1024 + OSTAGES * OST_BYTES + QSTAGES * QST_BYTES + 512;
+// Streamed-state region, cut per launch into slots of [G | R (8 KB) | X (8 KB)]:
+// 4 x 20 KB when every gradient of the launch is bf16, 3 x 24 KB with fp32 gradients.
+constexpr uint32_t QREG_BYTES = 81920;
+constexpr uint32_t SMEM_BYTES = 1024 + OSTAGES * OST_BYTES + QREG_BYTES + 512;
 
 enum { MAP_UH, MAP_UL, MAP_VH, MAP_VL, MAP_WH, MAP_WL, MAP_G, MAP_R, MAP_X, NMAPS };
 
@@ -66,19 +68,22 @@ __device__ __forceinline__ int nsub(const EpiMat& e, int j0) {
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntiles) {
+k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntiles, int qslot, int nq) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* ost = smem;                                   // operand ring
   unsigned char* qst = smem + OSTAGES * OST_BYTES;             // streamed-state ring
-  uint64_t* bars = (uint64_t*)(qst + QSTAGES * QST_BYTES);
+  const int QSTAGES = nq;                  // streamed-state slots of this launch (<= QSTAGES_MAX)
+  const int QST_BYTES = qslot;
+  const int Q_R = qslot - 2 * RX_BYTES;    // offsets of R and X in a slot (G first)
+  uint64_t* bars = (uint64_t*)(qst + QREG_BYTES);
   uint64_t* op_full = bars;
   uint64_t* op_empty = op_full + OSTAGES;
   uint64_t* acc_full = op_empty + OSTAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* q_full = acc_empty + 2;
-  uint64_t* q_empty = q_full + QSTAGES;
-  uint64_t* drain = q_empty + QSTAGES;
+  uint64_t* q_empty = q_full + QSTAGES_MAX;
+  uint64_t* drain = q_empty + QSTAGES_MAX;
   uint32_t* tslot = (uint32_t*)(drain + 1);
   volatile int* abort_flag = (volatile int*)(tslot + 1);
 
@@ -162,7 +167,7 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
   } else if (warp == 2 && lane == 0) {
     // ---------------------------------------------------------- streamed-state producer
     int q = 0; uint32_t ph = 0;
-    uint32_t last_ph[QSTAGES] = {0, 0, 0}; bool used[QSTAGES] = {false, false, false};
+    uint32_t last_ph[QSTAGES_MAX] = {0, 0, 0, 0}; bool used[QSTAGES_MAX] = {false, false, false, false};
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile tl = tiles[t];
       const EpiMat& e = mats[tl.mat];
@@ -175,15 +180,15 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
         unsigned char* b = qst + q * QST_BYTES;
         const int x = tl.j0 + sc * SUB;
         tma_load_2d(b, &e.map[MAP_G], &q_full[q], x, tl.i0);
-        tma_load_2d(b + 8192, &e.map[MAP_R], &q_full[q], x, tl.i0);
-        tma_load_2d(b + 8192 + RX_BYTES, &e.map[MAP_X], &q_full[q], x, tl.i0);
+        tma_load_2d(b + Q_R, &e.map[MAP_R], &q_full[q], x, tl.i0);
+        tma_load_2d(b + Q_R + RX_BYTES, &e.map[MAP_X], &q_full[q], x, tl.i0);
         used[q] = true; last_ph[q] = ph;
         if (++q == QSTAGES) { q = 0; ph ^= 1; }
       }
     }
   stream_done:
     if (*abort_flag)
-      for (int i = 0; i < QSTAGES; ++i) if (used[i]) mbar_wait_drain(&q_full[i], last_ph[i]);
+      for (int i = 0; i < QSTAGES_MAX; ++i) if (used[i]) mbar_wait_drain(&q_full[i], last_ph[i]);
   } else if (warp >= 4) {
     // ---------------------------------------------------------- epilogue
     const int quarter = warp & 3;
@@ -214,7 +219,7 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
         tmem_ld16(lane_addr + BNJ, t2);
         tmem_wait_ld();
         unsigned char* gb = qst + q * QST_BYTES;
-        unsigned char* rb = gb + 8192;
+        unsigned char* rb = gb + Q_R;
         unsigned char* xb = rb + RX_BYTES;
         float g[16];
         if (e.g_bf16) {

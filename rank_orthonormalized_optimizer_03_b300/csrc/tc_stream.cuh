@@ -10,8 +10,8 @@
 // tf32 halves of a 3xTF32 product and write them into the 64-byte-swizzled
 // K-major operand layout the MMA reads (transposing 4 x 2 register blocks on
 // the way for M^T).  The second operand (V^T or U^T, already split) comes in by
-// TMA.  Chunks of 16 along K keep four operand and four staging stages in
-// flight in shared memory.
+// TMA.  Chunks of 16 along K keep four operand stages and four staging slots
+// in flight in shared memory.
 //
 // The tensor core's fp32 accumulation truncates: its bias grows with the
 // number of accumulation steps (measured -1e-5 relative per 1024 of K).  So a
@@ -20,7 +20,7 @@
 // round-to-nearest fp32; the bias then stays near 2e-6.
 //
 // Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..17 converters
-// (four groups of four, one stage each) and slice drain.  One CTA per SM, persistent over (row tile, K range, column
+// (four groups of four, alternating chunks) and slice drain.  One CTA per SM, persistent over (row tile, K range, column
 // block) items of every matrix.
 #pragma once
 
@@ -35,10 +35,10 @@ using namespace dion::tc;
 constexpr int BM = 128;              // output rows per tile (TMEM lanes)
 constexpr int BK = 16;               // K per chunk: one 64-byte swizzle row of fp32
 constexpr int SLICE = 16;            // chunks per TMEM slice (256 of K)
-constexpr int OSTAGES = 4;
-constexpr int SSTAGES = 4;
+constexpr int OSTAGES = 4;           // operand stages (A hi/lo written by the converters, B by TMA)
+constexpr int SSTAGES = 4;           // staging slots of G and R (HBM latency)
 constexpr int NCONV = 16;            // converter / drain warps: four groups of four
-constexpr int NGROUP = 4;            // converter groups; group g converts the chunks of stage g (mod 4)
+constexpr int NGROUP = 4;            // converter groups; group g converts the chunks numbered g (mod 4)
 constexpr int NTHREADS = (2 + NCONV) * 32;
 constexpr int BN_MAX = 192;          // widest column block (TMEM: 2 x 192 <= 512)
 constexpr int QMAX = BN_MAX / 4;     // accumulator columns per converter thread (one column quarter)
@@ -47,9 +47,14 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_BYTES = BM * BK * 4;                // 8 KB
 constexpr uint32_t B_BYTES_MAX = BN_MAX * BK * 4;        // 12 KB
 constexpr uint32_t OST_BYTES = 2 * A_BYTES + 2 * B_BYTES_MAX;   // 40 KB
-constexpr uint32_t SST_BYTES = 16384;                    // G (<= 8 KB) | R (8 KB)
-constexpr uint32_t SST_R = 8192;                         // offset of the R tile in a staging stage
+constexpr uint32_t SST_BYTES = 16384;                    // staging slot: G (<= 8 KB) | R (8 KB)
+constexpr uint32_t SST_R = 8192;                         // offset of the R tile in a slot
 constexpr uint32_t SMEM_BYTES = 1024 + OSTAGES * OST_BYTES + SSTAGES * SST_BYTES + 512;
+// Converter group g waits on the chunks numbered g mod NGROUP only.  mbarrier
+// parity waits are exact only when a waiter sees every phase of the barrier it
+// waits on, so every stage and slot must belong to a single group: chunk numbers
+// map to stages and slots modulo a multiple of NGROUP.
+static_assert(OSTAGES % NGROUP == 0 && SSTAGES % NGROUP == 0, "stages must be owned by one converter group");
 
 // gmode: what the staged tiles hold.  G_BF16 / G_F32: M = G + R (phases a, c);
 // G_NONE: a single fp32 matrix in the R slot (the A T product of orth()).
@@ -138,8 +143,10 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     int os = 0, ss = 0; uint32_t oph = 0, sph = 0;
-    uint32_t olast[OSTAGES] = {0, 0}, slast[SSTAGES] = {0, 0};
-    bool oused[OSTAGES] = {false, false}, sused[SSTAGES] = {false, false};
+    uint32_t olast[OSTAGES], slast[SSTAGES];
+    bool oused[OSTAGES], sused[SSTAGES];
+    for (int i = 0; i < OSTAGES; ++i) { olast[i] = 0; oused[i] = false; }
+    for (int i = 0; i < SSTAGES; ++i) { slast[i] = 0; sused[i] = false; }
     for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
       const Item it = items[t];
       const SJob& j = jobs[it.job];
@@ -225,8 +232,8 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
   } else if (warp >= 2) {
     // ------------------------------------------------------------ converters + slice drain
     // Four groups of four warps; group g converts the chunks whose sequence number
-    // is g mod 4 (stage g), so four chunks are in conversion at once.  For the
-    // drain every warp owns TMEM lane quarter (warp % 4) and column quarter g.
+    // is g mod 4, so four chunks are in conversion at once.  For the drain every
+    // warp owns TMEM lane quarter (warp % 4) and column quarter g.
     const int cw = warp - 2;                 // 0..15
     const int quarter = warp & 3;            // TMEM lane quarter of this warp
     const int g = cw >> 2;                   // converter group; column quarter for the drain
