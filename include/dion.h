@@ -180,6 +180,44 @@ DION_API dion_status_t dion_plan_get_status(dion_plan* plan, const void* workspa
 /* Kernel launches enqueued by one dion_step_batched() call of this plan. */
 DION_API int32_t dion_plan_launches_per_step(const dion_plan* plan);
 
+/*
+ * orth() of one matrix for callers that cannot allocate device memory.
+ *
+ * Some callers may not call cudaMalloc at all: code running inside a CUDA
+ * graph capture, inside another library's allocator callback, or under a
+ * memory manager that owns every device byte.  This entry point needs nothing
+ * beyond the caller's input and output: its scratch is a fixed array of
+ * 4,760,320 bytes inside libdion.so itself (one copy on every GPU that loads
+ * the library, kept until the process exits).  It has no counterpart on the pages; it
+ * computes the same orth() as the plan-based step (the Q factor of a thin QR
+ * whose triangular factor has a positive diagonal), with the CUDA-core kernels
+ * of that step (CholeskyQR2, shifted CholeskyQR3 for kappa(A) > ~1e3).
+ *
+ *   A  rows x r fp32 row-major device array (leading dimension lda >= r), read only
+ *   Q  rows x r fp32 row-major device array (ldq >= r), written; may not overlap A
+ *   1 <= r <= min(rows, DION_NOALLOC_MAX_RANK), rows <= DION_NOALLOC_MAX_ROWS
+ *
+ * Returns DION_ERR_UNSUPPORTED for sizes beyond those limits (nothing is
+ * launched), DION_ERR_INVALID_ARG for NULL pointers or bad leading
+ * dimensions, DION_ERR_CUDA if a launch fails.  The work is enqueued on
+ * `stream`; with status != NULL the call then copies the matrix's status word
+ * (DION_MAT_* bits; Q is valid when no bit other than DION_MAT_SHIFTED is set)
+ * to *status and synchronises the stream, with status == NULL it returns
+ * without waiting.
+ *
+ * Every call shares the one scratch array and overwrites it (the status word
+ * is cleared by each call).  Calls whose work overlaps on the GPU (different
+ * streams, different host threads) race on it: order them on one stream.  The
+ * first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before starting any
+ * stream capture.  The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ */
+#define DION_NOALLOC_MAX_ROWS 8192
+#define DION_NOALLOC_MAX_RANK 64
+DION_API dion_status_t dion_orth_noalloc(const float* A, int64_t rows, int64_t r, int64_t lda, float* Q,
+                                         int64_t ldq, uint32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

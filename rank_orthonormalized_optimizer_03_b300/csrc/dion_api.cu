@@ -48,6 +48,21 @@ constexpr long long kRankGranule = 32;
 
 }  // namespace
 
+// ---- scratch of dion_orth_noalloc (see include/dion.h): a fixed device array
+// inside the library, for callers that cannot allocate device memory.
+namespace noalloc {
+constexpr long long kRowsMax = DION_NOALLOC_MAX_ROWS;
+constexpr long long kRankMax = DION_NOALLOC_MAX_RANK;        // rp == kRankMax at most
+constexpr long long kChunksMax = 32;                           // Gram partials (CUDA-core chunking)
+constexpr size_t kJobBytes = 512;                              // OrthJob + two launch tables + status words
+constexpr size_t kGpartFloats = (size_t)kChunksMax * kRankMax * kRankMax;
+constexpr size_t kSFloats = (size_t)kRankMax * kRankMax + kRankMax + 32 * kRankMax;
+constexpr size_t kTFloats = (size_t)kRankMax * kRankMax;
+constexpr size_t kQFloats = (size_t)kRowsMax * kRankMax;
+constexpr size_t kBytes = kJobBytes + 4 * (kGpartFloats + kSFloats + kTFloats + 2 * kQFloats);
+}  // namespace noalloc
+static __device__ __align__(256) unsigned char g_noalloc_scratch[noalloc::kBytes];
+
 struct dion_plan {
   std::vector<dion_matrix_desc> descs;
   int count = 0;
@@ -830,6 +845,83 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
   return ok();
 }
 
+// ---- dion_orth_noalloc: one orth() on the CUDA-core kernels, scratch in g_noalloc_scratch
+
+// Writes the job and its launch tables into the scratch and clears the status
+// and three-pass flag (kernel arguments carry them, so no host buffer is read
+// after the call returns).
+__global__ void k_noalloc_setup(OrthJob job, int ngram, int ntrmm, unsigned char* base) {
+  if (threadIdx.x == 0) {
+    *reinterpret_cast<OrthJob*>(base) = job;
+    int* ts = reinterpret_cast<int*>(base + 256);
+    ts[0] = 0; ts[1] = ngram; ts[2] = 0; ts[3] = ntrmm;
+    *job.status = 0u;
+    *job.flag = 0u;
+  }
+}
+
+dion_status_t orth_noalloc_impl(const float* A, long long rows, long long r, long long lda, float* Q, long long ldq,
+                                uint32_t* status_out, void* stream) {
+  if (!A || !Q) return fail(DION_ERR_INVALID_ARG, "NULL matrix pointer");
+  if (rows < 1 || r < 1 || r > rows) return fail(DION_ERR_INVALID_ARG, "need 1 <= r <= rows");
+  if (lda < r || ldq < r) return fail(DION_ERR_INVALID_ARG, "leading dimension below r");
+  if (rows > noalloc::kRowsMax || r > noalloc::kRankMax)
+    return fail(DION_ERR_UNSUPPORTED, "%lld x %lld exceeds the fixed scratch (rows <= %d, r <= %d)", rows, r,
+                DION_NOALLOC_MAX_ROWS, DION_NOALLOC_MAX_RANK);
+  // device address of the scratch, looked up once per device with that device current
+  static void* dev_ptr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cuda_check("device query");
+  if (!dev_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+      return cuda_check("scratch address lookup");
+    dev_ptr[dev] = ptr;
+  }
+  unsigned char* base = static_cast<unsigned char*>(dev_ptr[dev]);
+  const long long rp = cdiv(r, kRankGranule) * kRankGranule;
+  long long nch = std::min<long long>(noalloc::kChunksMax, std::max<long long>(1, cdiv(rows, 512)));
+  const long long chunk = cdiv(cdiv(rows, nch), 64) * 64;
+  nch = cdiv(rows, chunk);
+  float* fbase = reinterpret_cast<float*>(base + noalloc::kJobBytes);
+  OrthJob job;
+  std::memset(&job, 0, sizeof job);
+  job.A = A; job.lda = lda;
+  job.gpart = fbase;
+  job.S = job.gpart + noalloc::kGpartFloats;
+  job.T = job.S + noalloc::kSFloats;
+  job.Q = job.T + noalloc::kTFloats;
+  job.Q2 = job.Q + noalloc::kQFloats;
+  job.out = Q; job.ldo = ldq; job.out_cols = r;
+  job.rows = rows; job.r = r; job.rp = rp;
+  job.nchunk = (int)nch; job.chunk = (int)chunk;
+  job.status = reinterpret_cast<unsigned*>(base + 256 + 32);
+  job.flag = job.status + 1;
+  job.Tt_hi = job.Tt_lo = nullptr;
+  const long long nt = cdiv(rp, simt::TN);
+  const int ngram = (int)(nch * nt * nt);
+  const int ntrmm = (int)(cdiv(rows, simt::TM) * nt);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  k_noalloc_setup<<<1, 32, 0, s>>>(job, ngram, ntrmm, base);
+  const OrthJob* jobs = reinterpret_cast<const OrthJob*>(base);
+  const int* tg = reinterpret_cast<const int*>(base + 256);
+  const int* tt = tg + 2;
+  const size_t chol_smem = (size_t)((r * (r + 1) + r + 32 * r) * 4);   // <= 25 KB at r = 64
+  for (int pass = 0; pass < 3; ++pass) {
+    simt::k_gram<<<ngram, simt::NT, 0, s>>>(jobs, tg, 1, pass);
+    simt::k_chol_inv<true><<<1, simt::CHOL_NT, chol_smem, s>>>(jobs, pass, 0);
+    simt::k_trmm<<<ntrmm, simt::NT, 0, s>>>(jobs, tt, 1, pass);
+  }
+  dion_status_t st = cuda_check("orth launch");
+  if (st) return st;
+  if (status_out) {
+    if (cudaMemcpyAsync(status_out, job.status, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return cuda_check("status copy");
+    if (cudaStreamSynchronize(s) != cudaSuccess) return cuda_check("status sync");
+  }
+  return ok();
+}
+
 }  // namespace
 
 extern "C" {
@@ -967,6 +1059,11 @@ int32_t dion_plan_launches_per_step(const dion_plan* plan) {
   n += plan->dion_idx.empty() ? 0 : 1;         // phase (d), Dion matrices
   n += 2;                                      // phase (e): operand split + tensor-core update
   return n;
+}
+
+dion_status_t dion_orth_noalloc(const float* A, int64_t rows, int64_t r, int64_t lda, float* Q, int64_t ldq,
+                                uint32_t* status, void* stream) {
+  return orth_noalloc_impl(A, rows, r, lda, Q, ldq, status, stream);
 }
 
 }  // extern "C"

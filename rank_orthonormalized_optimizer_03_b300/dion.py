@@ -65,6 +65,7 @@ def _declare(L):
                                    ctypes.POINTER(I64), ctypes.POINTER(I64)]),
         "dion_plan_get_status": (I32, [P, P, SZ, ctypes.POINTER(ctypes.c_uint32), P]),
         "dion_plan_launches_per_step": (I32, [P]),
+        "dion_orth_noalloc": (I32, [P, I64, I64, I64, P, I64, ctypes.POINTER(ctypes.c_uint32), P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -121,6 +122,29 @@ def make_desc(X, G, R, V, eta, beta, variant="orth", scale=0.0) -> MatrixDesc:
         X.stride(0), G.stride(0), R.stride(0),
         DTYPE_BF16 if G.dtype == torch.bfloat16 else DTYPE_F32, VARIANT[variant],
         float(eta), float(beta), float(scale), 0.0)
+
+
+NOALLOC_MAX_ROWS, NOALLOC_MAX_RANK = 8192, 64
+
+
+def orth_noalloc(A, Q, stream=None, status: bool = True) -> Optional[int]:
+    """Q = orth(A) for one matrix through dion_orth_noalloc (no device allocation
+    in the library; its scratch is a fixed array inside libdion.so).
+
+    A and Q are float32 CUDA tensors (rows x r views with unit column stride).
+    With status=True the call waits for the result and returns the matrix's
+    status word; otherwise it returns None without waiting.
+    """
+    import torch
+    if A.dim() != 2 or Q.dim() != 2 or A.shape != Q.shape:
+        raise ValueError("A and Q must be rows x r matrices of the same shape")
+    if A.dtype != torch.float32 or Q.dtype != torch.float32 or A.stride(1) != 1 or Q.stride(1) != 1:
+        raise ValueError("A and Q must be float32 with unit column stride")
+    rows, r = A.shape
+    st = ctypes.c_uint32(0)
+    check(lib().dion_orth_noalloc(A.data_ptr(), rows, r, A.stride(0), Q.data_ptr(), Q.stride(0),
+                                  ctypes.byref(st) if status else None, _stream_ptr(stream)), "dion_orth_noalloc")
+    return st.value if status else None
 
 
 class Plan:
