@@ -152,7 +152,8 @@ DION_API dion_status_t dion_step_batched(dion_plan* plan, void* workspace, size_
  *          orth(P) unchanged and keeps P well conditioned)
  *   1 (b): U = orth(P)                                     (U in the workspace)
  *   2 (c): W = (G + R)^T U                                 (W in the workspace)
- *   3 (d): Vbar = orth(W) or colnorm(W), written into V
+ *   3 (d): Vbar = orth(W) or colnorm(W), written into V (and the tf32
+ *          halves of U, Vbar and W that phase (e) reads, in the workspace)
  *   4 (e): X <- X - eta s U Vbar^T,  R <- beta (G + R - U W^T)
  * Running 0..4 equals dion_step_batched().
  */

@@ -74,17 +74,4 @@ __device__ __forceinline__ int find_job(const int* __restrict__ start, int n, in
   return lo;
 }
 
-__device__ __forceinline__ float load_g(const MatDev& d, long long i, long long k) {
-  if (d.g_bf16) {
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(d.G)[i * d.ldg + k]);
-  }
-  return reinterpret_cast<const float*>(d.G)[i * d.ldg + k];
-}
-
-// M = G + R, element (i, k); zero outside the matrix.
-__device__ __forceinline__ float load_m(const MatDev& d, long long i, long long k) {
-  if (i >= d.m || k >= d.n) return 0.f;
-  return load_g(d, i, k) + d.R[i * d.ldr + k];
-}
-
 }  // namespace dion

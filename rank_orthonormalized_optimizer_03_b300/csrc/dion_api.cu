@@ -78,30 +78,30 @@ struct dion_plan {
 
   // table image layout (byte offsets inside the tables region)
   size_t t_mats = 0, t_jobs_p = 0, t_jobs_w = 0, t_jobs_v = 0, t_ts_gram_v = 0, t_ts_trmm_v = 0;
-  size_t t_ts_mv = 0, t_ts_gram_p = 0, t_ts_trmm_p = 0, t_ts_mtu = 0, t_ts_wred = 0,
-         t_ts_epi = 0, t_ts_gram_w = 0, t_ts_trmm_w = 0, t_ts_coln = 0, t_coln_idx = 0;
-  std::vector<int> ts_mv, ts_gram_p, ts_trmm_p, ts_mtu, ts_wred, ts_epi, ts_gram_w, ts_trmm_w, ts_coln;
+  size_t t_ts_gram_p = 0, t_ts_trmm_p = 0, t_ts_wred = 0, t_ts_gram_w = 0, t_ts_trmm_w = 0, t_ts_coln = 0,
+         t_coln_idx = 0;
+  std::vector<int> ts_gram_p, ts_trmm_p, ts_wred, ts_gram_w, ts_trmm_w, ts_coln;
   std::vector<int> ts_gram_v, ts_trmm_v;   // orth(V) of the Dion matrices
   bool any_split = false;
 
   // tensor-core path: split (hi/lo tf32) operand copies and the phase (e) tables
   std::vector<size_t> off_Uh, off_Ul, off_Vh, off_Vl, off_Wh, off_Wl;
-  size_t t_epi = 0, t_ts_epi_tc = 0, t_split = 0, t_ts_split = 0;
-  std::vector<int> ts_epi_tc, ts_split;
+  size_t t_epi = 0, t_split = 0, t_ts_split = 0;
+  std::vector<int> ts_split;
   int n_split = 0;
   int num_sms = 0;
   // phases (a) and (c): streaming jobs, transposed split copies V^T, U^T
   std::vector<int> ncb, bn;
   std::vector<long long> ldt_n, ldt_m;
   std::vector<size_t> off_VTh, off_VTl, off_UTh, off_UTl;
-  size_t t_sj_a = 0, t_sj_c = 0, t_ts_sa = 0, t_ts_sc = 0, t_tj_v = 0, t_tj_u = 0, t_ts_tv = 0, t_ts_tu = 0;
-  std::vector<int> ts_sa, ts_sc, ts_tv, ts_tu;
+  size_t t_sj_a = 0, t_sj_c = 0, t_tj_v = 0, t_tj_u = 0, t_ts_tv = 0, t_ts_tu = 0;
+  std::vector<int> ts_tv, ts_tu;
   // tensor-core orth(): per list (0 = P, 1 = W, 2 = V) and pass, Gram and A T jobs
   bool tc_orth = false;
   bool any_g_f32 = false;   // a gradient in fp32: larger staging slots
   std::vector<size_t> off_Tth, off_Ttl;
-  size_t t_gj[3][3] = {}, t_tj[3][3] = {}, t_ts_g[3] = {}, t_ts_t[3] = {};
-  std::vector<int> ts_g[3], ts_t[3], ts_gred[3];
+  size_t t_gj[3][3] = {}, t_tj[3][3] = {};
+  std::vector<int> ts_gred[3];
   size_t t_ts_gred[3] = {};
   size_t t_vcopy = 0, t_ts_vcopy = 0;
   std::vector<int> ts_vcopy;
@@ -234,13 +234,9 @@ void layout(dion_plan* p) {
   std::vector<int> all(cnt);
   for (int i = 0; i < cnt; ++i) all[i] = i;
   auto D = [&](int i) -> const dion_matrix_desc& { return p->descs[i]; };
-  prefix(p->ts_mv, all, [&](int i) { return cdiv(D(i).m, simt::TM) * cdiv(p->rp[i], simt::TN); });
   prefix(p->ts_gram_p, all, [&](int i) { long long t = cdiv(p->rp[i], simt::TN); return p->nchunk_p[i] * t * t; });
   prefix(p->ts_trmm_p, all, [&](int i) { return cdiv(D(i).m, simt::TM) * cdiv(p->rp[i], simt::TN); });
-  prefix(p->ts_mtu, all, [&](int i) {
-    return (long long)p->ksplit[i] * cdiv(D(i).n, simt::TM) * cdiv(p->rp[i], simt::TN); });
   prefix(p->ts_wred, all, [&](int i) { return p->ksplit[i] > 1 ? cdiv(D(i).n * p->rp[i], 1024) : 1; });
-  prefix(p->ts_epi, all, [&](int i) { return cdiv(D(i).m, simt::TM) * cdiv(D(i).n, simt::TN); });
   prefix(p->ts_gram_w, p->orth_idx, [&](int i) { long long t = cdiv(p->rp[i], simt::TN); return p->nchunk_w[i] * t * t; });
   prefix(p->ts_trmm_w, p->orth_idx, [&](int i) { return cdiv(D(i).n, simt::TM) * cdiv(p->rp[i], simt::TN); });
   prefix(p->ts_coln, p->dion_idx, [&](int i) { return cdiv(D(i).r, 32); });
@@ -251,7 +247,6 @@ void layout(dion_plan* p) {
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 128); return o; };
   // tensor-core tables first: they hold CUtensorMaps (64-byte alignment)
-  prefix(p->ts_epi_tc, all, [&](int i) { return cdiv(D(i).m, tcepi::BM) * cdiv(D(i).n, tcepi::BNJ); });
   p->n_split = 3 * cnt;
   {
     std::vector<int> jobs(p->n_split);
@@ -262,17 +257,12 @@ void layout(dion_plan* p) {
       return cdiv(rows * p->rp[i], tcsplit::ELEMS_PER_CTA);
     });
   }
-  prefix(p->ts_sa, all, [&](int i) { return cdiv(D(i).m, tcstream::BM) * p->ncb[i]; });
-  prefix(p->ts_sc, all, [&](int i) { return cdiv(D(i).n, tcstream::BM) * (long long)p->ksplit[i] * p->ncb[i]; });
   prefix(p->ts_tv, all, [&](int i) { return cdiv(D(i).n, 32) * cdiv(p->rp[i], 32); });
   prefix(p->ts_tu, all, [&](int i) { return cdiv(D(i).m, 32) * cdiv(p->rp[i], 32); });
   {
     const std::vector<int>* lists[3] = {&all, &p->orth_idx, &p->dion_idx};
     for (int L = 0; L < 3; ++L) {
       const size_t nj = std::max<size_t>(1, lists[L]->size());
-      prefix(p->ts_g[L], *lists[L], [&](int i) { return cdiv(L == 0 ? D(i).m : D(i).n, tcgram::CHUNK_ROWS); });
-      prefix(p->ts_t[L], *lists[L], [&](int i) {
-        return cdiv(L == 0 ? D(i).m : D(i).n, tcstream::BM) * p->ncb[i]; });
       prefix(p->ts_gred[L], *lists[L], [&](int i) { return cdiv(p->rp[i] * p->rp[i], simt::GRED_ELEMS); });
       for (int ps = 0; ps < 3; ++ps) {
         p->t_gj[L][ps] = take(sizeof(tcgram::GJob) * nj);
@@ -283,8 +273,6 @@ void layout(dion_plan* p) {
     p->t_vcopy = take(sizeof(tcsplit::SplitJob) * std::max<size_t>(1, p->dion_idx.size()));
     for (int L = 0; L < 3; ++L) {
       p->t_ts_gred[L] = take(4 * p->ts_gred[L].size());
-      p->t_ts_g[L] = take(4 * p->ts_g[L].size());
-      p->t_ts_t[L] = take(4 * p->ts_t[L].size());
     }
     p->t_ts_vcopy = take(4 * p->ts_vcopy.size());
   }
@@ -350,10 +338,7 @@ void layout(dion_plan* p) {
   p->t_sj_c = take(sizeof(tcstream::SJob) * cnt);
   p->t_epi = take(sizeof(tcepi::EpiMat) * cnt);
   p->t_split = take(sizeof(tcsplit::SplitJob) * p->n_split);
-  p->t_ts_epi_tc = take(4 * p->ts_epi_tc.size());
   p->t_ts_split = take(4 * p->ts_split.size());
-  p->t_ts_sa = take(4 * p->ts_sa.size());
-  p->t_ts_sc = take(4 * p->ts_sc.size());
   p->t_tj_v = take(sizeof(tcsplit::TJob) * cnt);
   p->t_tj_u = take(sizeof(tcsplit::TJob) * cnt);
   p->t_ts_tv = take(4 * p->ts_tv.size());
@@ -364,12 +349,9 @@ void layout(dion_plan* p) {
   p->t_jobs_v = take(sizeof(OrthJob) * std::max<size_t>(1, p->dion_idx.size()));
   p->t_ts_gram_v = take(4 * p->ts_gram_v.size());
   p->t_ts_trmm_v = take(4 * p->ts_trmm_v.size());
-  p->t_ts_mv = take(4 * p->ts_mv.size());
   p->t_ts_gram_p = take(4 * p->ts_gram_p.size());
   p->t_ts_trmm_p = take(4 * p->ts_trmm_p.size());
-  p->t_ts_mtu = take(4 * p->ts_mtu.size());
   p->t_ts_wred = take(4 * p->ts_wred.size());
-  p->t_ts_epi = take(4 * p->ts_epi.size());
   p->t_ts_gram_w = take(4 * p->ts_gram_w.size());
   p->t_ts_trmm_w = take(4 * p->ts_trmm_w.size());
   p->t_ts_coln = take(4 * p->ts_coln.size());
@@ -533,12 +515,9 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
   put(p->image, p->t_ts_trmm_v, p->ts_trmm_v.data(), p->ts_trmm_v.size());
   put(p->image, p->t_jobs_p, jp.data(), jp.size());
   put(p->image, p->t_jobs_w, jw.data(), jw.size());
-  put(p->image, p->t_ts_mv, p->ts_mv.data(), p->ts_mv.size());
   put(p->image, p->t_ts_gram_p, p->ts_gram_p.data(), p->ts_gram_p.size());
   put(p->image, p->t_ts_trmm_p, p->ts_trmm_p.data(), p->ts_trmm_p.size());
-  put(p->image, p->t_ts_mtu, p->ts_mtu.data(), p->ts_mtu.size());
   put(p->image, p->t_ts_wred, p->ts_wred.data(), p->ts_wred.size());
-  put(p->image, p->t_ts_epi, p->ts_epi.data(), p->ts_epi.size());
   put(p->image, p->t_ts_gram_w, p->ts_gram_w.data(), p->ts_gram_w.size());
   put(p->image, p->t_ts_trmm_w, p->ts_trmm_w.data(), p->ts_trmm_w.size());
   put(p->image, p->t_ts_coln, p->ts_coln.data(), p->ts_coln.size());
@@ -660,9 +639,7 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
         put(p->image, p->t_gj[L][ps], gj.data(), gj.size());
         put(p->image, p->t_tj[L][ps], tj.data(), tj.size());
       }
-      put(p->image, p->t_ts_g[L], p->ts_g[L].data(), p->ts_g[L].size());
       put(p->image, p->t_ts_gred[L], p->ts_gred[L].data(), p->ts_gred[L].size());
-      put(p->image, p->t_ts_t[L], p->ts_t[L].data(), p->ts_t[L].size());
     }
     std::vector<tcsplit::SplitJob> vc(std::max<size_t>(1, p->dion_idx.size()));
     for (size_t k = 0; k < p->dion_idx.size(); ++k) {
@@ -682,15 +659,12 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
   if (!p->it_epi.empty()) put(p->image, p->t_it_epi, p->it_epi.data(), p->it_epi.size());
   put(p->image, p->t_sj_a, sa.data(), sa.size());
   put(p->image, p->t_sj_c, sc.data(), sc.size());
-  put(p->image, p->t_ts_sa, p->ts_sa.data(), p->ts_sa.size());
-  put(p->image, p->t_ts_sc, p->ts_sc.data(), p->ts_sc.size());
   put(p->image, p->t_tj_v, tv.data(), tv.size());
   put(p->image, p->t_tj_u, tu.data(), tu.size());
   put(p->image, p->t_ts_tv, p->ts_tv.data(), p->ts_tv.size());
   put(p->image, p->t_ts_tu, p->ts_tu.data(), p->ts_tu.size());
   put(p->image, p->t_epi, epi.data(), epi.size());
   put(p->image, p->t_split, sj.data(), sj.size());
-  put(p->image, p->t_ts_epi_tc, p->ts_epi_tc.data(), p->ts_epi_tc.size());
   put(p->image, p->t_ts_split, p->ts_split.data(), p->ts_split.size());
   return DION_OK;
 }
@@ -827,10 +801,11 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
           simt::k_colnorm<<<p->ts_coln[p->dion_idx.size()], simt::NT, 0, s>>>(
               mats, tab<int>(p, base, p->t_ts_coln), tab<int>(p, base, p->t_coln_idx),
               (int)p->dion_idx.size());
-        break;
-      case 4: {
+        // tf32 halves of U, Vbar and W: the operands of the tensor-core update (e)
         tcsplit::k_split<<<p->ts_split[p->n_split], tcsplit::NT, 0, s>>>(
             tab<tcsplit::SplitJob>(p, base, p->t_split), tab<int>(p, base, p->t_ts_split), p->n_split);
+        break;
+      case 4: {
         const int tiles = (int)p->it_epi.size();
         const int grid = std::min(tiles, p->num_sms);
         tcepi::k_epi<<<grid, tcepi::NTHREADS, tcepi::SMEM_BYTES, s>>>(
@@ -953,7 +928,7 @@ dion_status_t dion_plan_create(const dion_matrix_desc* descs, int32_t count, siz
   p->count = count;
   layout(p);
   // every grouped launch must fit in one grid dimension
-  const long long grids[] = {p->ts_mv[count], p->ts_gram_p[count], p->ts_mtu[count], p->ts_epi[count]};
+  const long long grids[] = {p->ts_gram_p[count], p->ts_trmm_p[count], p->ts_wred[count], p->ts_split[p->n_split]};
   for (long long g : grids)
     if (g >= (1LL << 31)) {
       delete p;
@@ -1057,7 +1032,8 @@ int32_t dion_plan_launches_per_step(const dion_plan* plan) {
   n += 2 + (plan->any_split ? 1 : 0);          // phase (c): U^T split, tensor-core W = M^T U, reduce
   n += plan->orth_idx.empty() ? 0 : per_orth;  // phase (d), Orth-Dion matrices
   n += plan->dion_idx.empty() ? 0 : 1;         // phase (d), Dion matrices
-  n += 2;                                      // phase (e): operand split + tensor-core update
+  n += 1;                                      // phase (d): tf32 halves of U, Vbar, W
+  n += 1;                                      // phase (e): tensor-core update
   return n;
 }
 

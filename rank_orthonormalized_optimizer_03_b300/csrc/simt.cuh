@@ -1,16 +1,15 @@
-// CUDA-core (FFMA) kernels of the step: every phase as a grouped launch over
-// all matrices (or orth jobs) of a plan.  fp32 storage, fp32 accumulation in a
-// fixed order, so results are bitwise reproducible run to run.
+// CUDA-core kernels of the step: the small, latency-bound pieces that do not
+// map to tensor-core tiles, each a grouped launch over all matrices (or orth
+// jobs) of a plan.  fp32 storage, fp32 accumulation in a fixed order, so
+// results are bitwise reproducible run to run.
 //
-// Phase map (junaidaliop.github.io "Orth-Dion", update equations):
-//   k_mv        P = (G + R) V                          equations 1-2 (argument of orth)
-//   k_gram      partial Grams A^T A of a row chunk     orth(), CholeskyQR2 Gram
-//   k_chol_inv  Gram reduce, Cholesky, inverse         orth(), positive diagonal
-//   k_trmm      Q = A T  (T upper triangular)          orth(), triangular solve
-//   k_mtu       W = (G + R)^T U  (split over rows)     equation 3
-//   k_wreduce   W = sum of the split partials          equation 3
-//   k_colnorm   Vbar = W diag(1/||w_j||)               Dion right factor
-//   k_epilogue  X -= eta s U Vbar^T; R = beta (M - U W^T)   equations 5-6
+// Kernel map (junaidaliop.github.io "Orth-Dion", update equations and glossary):
+//   k_gram          partial Grams A^T A of a row chunk   orth() (the plan path for r > 192, and
+//   k_trmm          Q = A T  (T upper triangular)        dion_orth_noalloc)
+//   k_gram_reduce   sum of the Gram partials             orth(), tensor-core path
+//   k_chol_inv      Cholesky + inverse, one CTA per job  orth(), positive diagonal, shifted pass
+//   k_wreduce       W = sum of the K-range partials      equation 3
+//   k_colnorm       Vbar = W diag(1/||w_j||)             Dion right factor
 #pragma once
 
 #include "common.cuh"
@@ -78,48 +77,11 @@ struct LoadRMT {
     return (k < rows && i < cols) ? p[k * ld + i] : 0.f;
   }
 };
-struct LoadM {
-  const MatDev* d;
-  __device__ float operator()(long long i, long long k) const { return load_m(*d, i, k); }
-};
-// M^T: element (j, i) = M[i][j]
-struct LoadMT {
-  const MatDev* d;
-  __device__ float operator()(long long j, long long i) const { return load_m(*d, i, j); }
-};
-
 __device__ __forceinline__ void zero(float (&acc)[4][4]) {
 #pragma unroll
   for (int u = 0; u < 4; ++u)
 #pragma unroll
     for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
-}
-
-// ---------------------------------------------------------------- phase (a)
-__global__ void __launch_bounds__(NT) k_mv(const MatDev* __restrict__ mats,
-                                           const int* __restrict__ tstart, int nmat) {
-  __shared__ float As[TK * LDS], Bs[TK * LDS];
-  const int j = find_job(tstart, nmat, blockIdx.x);
-  const MatDev& d = mats[j];
-  const int local = blockIdx.x - tstart[j];
-  const int ntc = (int)((d.rp + TN - 1) / TN);
-  const long long i0 = (long long)(local / ntc) * TM, c0 = (long long)(local % ntc) * TN;
-  float acc[4][4];
-  zero(acc);
-  LoadM la{&d};
-  LoadRM lb{d.Vin, d.ldvin, d.n, d.r};
-  tile_acc<true, true>(la, lb, i0, c0, 0, d.n, acc, As, Bs);
-  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const long long i = i0 + ty * 4 + u;
-    if (i >= d.m) continue;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const long long c = c0 + tx * 4 + v;
-      if (c < d.rp) d.P[i * d.rp + c] = acc[u][v];
-    }
-  }
 }
 
 // ---------------------------------------------------------------- orth()
@@ -453,38 +415,6 @@ __global__ void __launch_bounds__(NT) k_trmm(const OrthJob* __restrict__ jobs,
 }
 
 // ---------------------------------------------------------------- phase (c)
-__global__ void __launch_bounds__(NT) k_mtu(const MatDev* __restrict__ mats,
-                                            const int* __restrict__ tstart, int nmat) {
-  __shared__ float As[TK * LDS], Bs[TK * LDS];
-  const int j = find_job(tstart, nmat, blockIdx.x);
-  const MatDev& d = mats[j];
-  if (*d.status & ST_FATAL) return;
-  const int local = blockIdx.x - tstart[j];
-  const int ntc = (int)((d.rp + TN - 1) / TN);
-  const int ntn = (int)((d.n + TM - 1) / TM);
-  const int split = local / (ntn * ntc), rem = local % (ntn * ntc);
-  const long long j0 = (long long)(rem / ntc) * TM, c0 = (long long)(rem % ntc) * TN;
-  const long long ib = (long long)split * d.kchunk;
-  const long long ie = ib + d.kchunk < d.m ? ib + d.kchunk : d.m;
-  float acc[4][4];
-  zero(acc);
-  LoadMT la{&d};
-  LoadRM lb{d.U, d.rp, d.m, d.rp};
-  tile_acc<false, true>(la, lb, j0, c0, ib, ie, acc, As, Bs);
-  float* out = d.ksplit > 1 ? d.Wpart + (long long)split * d.n * d.rp : d.W;
-  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const long long jr = j0 + ty * 4 + u;
-    if (jr >= d.n) continue;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const long long c = c0 + tx * 4 + v;
-      if (c < d.rp) out[jr * d.rp + c] = acc[u][v];
-    }
-  }
-}
-
 // W = sum over splits (fixed order); one CTA covers 1024 elements.
 __global__ void __launch_bounds__(NT) k_wreduce(const MatDev* __restrict__ mats,
                                                 const int* __restrict__ tstart, int nmat) {
@@ -531,67 +461,6 @@ __global__ void __launch_bounds__(NT) k_colnorm(const MatDev* __restrict__ mats,
   if (c < d.r) {
     const float sc = scale[threadIdx.x & 31];
     for (long long row = w; row < d.n; row += NT / 32) d.V[row * d.r + c] = d.W[row * d.rp + c] * sc;
-  }
-}
-
-// ---------------------------------------------------------------- phase (e)
-// Per 64 x 64 tile of the m x n state: T1 = U Vbar^T, T2 = U W^T (K = r),
-// X -= eta s T1, R = beta (G + R - T2).
-__global__ void __launch_bounds__(NT) k_epilogue(const MatDev* __restrict__ mats,
-                                                 const int* __restrict__ tstart, int nmat) {
-  __shared__ float As[TK * LDS], B1[TK * LDS], B2[TK * LDS];
-  const int j = find_job(tstart, nmat, blockIdx.x);
-  const MatDev& d = mats[j];
-  if (*d.status & ST_FATAL) return;
-  const int local = blockIdx.x - tstart[j];
-  const int ntn = (int)((d.n + TN - 1) / TN);
-  const long long i0 = (long long)(local / ntn) * TM, j0 = (long long)(local % ntn) * TN;
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  float t1[4][4], t2[4][4];
-  zero(t1);
-  zero(t2);
-  for (long long k0 = 0; k0 < d.r; k0 += TK) {
-#pragma unroll
-    for (int e = 0; e < (TM * TK) / NT; ++e) {
-      const int idx = tid + e * NT;
-      const int ii = idx / TK, kk = idx % TK;
-      const long long i = i0 + ii, k = k0 + kk;
-      As[kk * LDS + ii] = (i < d.m && k < d.r) ? d.U[i * d.rp + k] : 0.f;
-      const long long jr = j0 + ii;  // B tiles share the (row, k) walk
-      const bool ok = jr < d.n && k < d.r;
-      B1[kk * LDS + ii] = ok ? d.V[jr * d.r + k] : 0.f;
-      B2[kk * LDS + ii] = ok ? d.W[jr * d.rp + k] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < TK; ++kk) {
-      float a[4], b1[4], b2[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] = As[kk * LDS + ty * 4 + u];
-#pragma unroll
-      for (int v = 0; v < 4; ++v) { b1[v] = B1[kk * LDS + tx * 4 + v]; b2[v] = B2[kk * LDS + tx * 4 + v]; }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          t1[u][v] = fmaf(a[u], b1[v], t1[u][v]);
-          t2[u][v] = fmaf(a[u], b2[v], t2[u][v]);
-        }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const long long i = i0 + ty * 4 + u;
-    if (i >= d.m) continue;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const long long jc = j0 + tx * 4 + v;
-      if (jc >= d.n) continue;
-      const float mm = load_g(d, i, jc) + d.R[i * d.ldr + jc];
-      d.X[i * d.ldx + jc] = fmaf(-d.eta_s, t1[u][v], d.X[i * d.ldx + jc]);
-      d.R[i * d.ldr + jc] = d.beta * (mm - t2[u][v]);
-    }
   }
 }
 
