@@ -126,6 +126,24 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
+# ----------------------------------------------------------------------------- multi-rank
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank steps its own full copy of the workload
+    (weak scaling), and the job is done when the last rank is."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput_gbs(step_bytes: float, ms_per_step: float, world: int) -> float:
+    """Whole-job algorithmic GB/s: all ranks' bytes over the slowest rank's time."""
+    return world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------------------- CUDA arm
 def build_state(wl, dev, args):
     import torch
@@ -189,10 +207,7 @@ def run_cuda(args):
     total_ms = t_start.elapsed_time(t_end)
     phase_ms = {PHASES[p]: statistics.mean(ev[s][p].elapsed_time(ev[s][p + 1]) for s in range(args.steps))
                 for p in range(5)}
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     from rank_orthonormalized_optimizer_03_b300.dion import DION_MAT_SHIFTED, FATAL
     status = plan.status()
@@ -200,7 +215,7 @@ def run_cuda(args):
     shifted = sum(1 for v in status if v & DION_MAT_SHIFTED)
 
     step_bytes = cost["step"].bytes
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = job_throughput_gbs(step_bytes, ms_per_step, world)
 
     peaks = load_peaks()
     # dominant phase: the one with the largest share of the step

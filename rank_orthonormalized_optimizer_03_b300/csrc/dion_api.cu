@@ -102,6 +102,8 @@ struct dion_plan {
   std::vector<size_t> off_Tth, off_Ttl;
   size_t t_gj[3][3] = {}, t_tj[3][3] = {};
   std::vector<int> ts_gred[3];
+  std::vector<int> chol_order[3];          // jobs of each orth list, largest rank first
+  size_t t_chol_order[3] = {};
   size_t t_ts_gred[3] = {};
   size_t t_vcopy = 0, t_ts_vcopy = 0;
   std::vector<int> ts_vcopy;
@@ -333,6 +335,14 @@ void layout(dion_plan* p) {
       p->t_it_g[L] = take(sizeof(tcgram::GItem) * std::max<size_t>(1, p->it_g[L].size()));
     }
     p->t_it_epi = take(sizeof(tcepi::Tile) * std::max<size_t>(1, p->it_epi.size()));
+    for (int L = 0; L < 3; ++L) {
+      const size_t nj = lists[L]->size();
+      p->chol_order[L].resize(nj);
+      for (size_t k = 0; k < nj; ++k) p->chol_order[L][k] = (int)k;
+      std::stable_sort(p->chol_order[L].begin(), p->chol_order[L].end(), [&](int a, int b) {
+        return D((*lists[L])[a]).r > D((*lists[L])[b]).r; });
+      p->t_chol_order[L] = take(4 * std::max<size_t>(1, nj));
+    }
   }
   p->t_sj_a = take(sizeof(tcstream::SJob) * cnt);
   p->t_sj_c = take(sizeof(tcstream::SJob) * cnt);
@@ -657,6 +667,8 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     if (!p->it_g[L].empty()) put(p->image, p->t_it_g[L], p->it_g[L].data(), p->it_g[L].size());
   }
   if (!p->it_epi.empty()) put(p->image, p->t_it_epi, p->it_epi.data(), p->it_epi.size());
+  for (int L = 0; L < 3; ++L)
+    if (!p->chol_order[L].empty()) put(p->image, p->t_chol_order[L], p->chol_order[L].data(), p->chol_order[L].size());
   put(p->image, p->t_sj_a, sa.data(), sa.size());
   put(p->image, p->t_sj_c, sc.data(), sc.size());
   put(p->image, p->t_tj_v, tv.data(), tv.size());
@@ -706,9 +718,9 @@ dion_status_t launch_orth(const dion_plan* p, unsigned char* base, cudaStream_t 
   for (int pass = 0; pass < 3; ++pass) {
     simt::k_gram<<<ts_gram[njob], simt::NT, 0, s>>>(jobs, tg, njob, pass);
     if (use_smem)
-      simt::k_chol_inv<true><<<njob, simt::CHOL_NT, chol_smem, s>>>(jobs, pass, 0);
+      simt::k_chol_inv<true><<<njob, simt::CHOL_NT, chol_smem, s>>>(jobs, pass, 0, nullptr);
     else
-      simt::k_chol_inv<false><<<njob, simt::CHOL_NT, 0, s>>>(jobs, pass, 0);
+      simt::k_chol_inv<false><<<njob, simt::CHOL_NT, 0, s>>>(jobs, pass, 0, nullptr);
     simt::k_trmm<<<ts_trmm[njob], simt::NT, 0, s>>>(jobs, tt, njob, pass);
   }
   return cuda_check("orth launch");
@@ -724,14 +736,15 @@ dion_status_t launch_orth_tc(const dion_plan* p, unsigned char* base, cudaStream
   const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax + 32 * rmax) * 4);
   const int use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
   const int ng = (int)p->it_g[L].size(), nt = (int)p->it_tr[L].size();
+  const int* order = tab<int>(p, base, p->t_chol_order[L]);
   for (int ps = 0; ps < 3; ++ps) {
     tcgram::k_gram<<<std::min(ng, p->num_sms), tcgram::NTHREADS, tcgram::SMEM_BYTES, s>>>(
         tab<tcgram::GJob>(p, base, p->t_gj[L][ps]), tab<tcgram::GItem>(p, base, p->t_it_g[L]), ng);
     simt::k_gram_reduce<<<p->ts_gred[L][njob], 256, 0, s>>>(jobs, tab<int>(p, base, p->t_ts_gred[L]), njob, ps);
     if (use_smem)
-      simt::k_chol_inv<true><<<njob, simt::CHOL_NT, chol_smem, s>>>(jobs, ps, 1);
+      simt::k_chol_inv<true><<<njob, simt::CHOL_NT, chol_smem, s>>>(jobs, ps, 1, order);
     else
-      simt::k_chol_inv<false><<<njob, simt::CHOL_NT, 0, s>>>(jobs, ps, 1);
+      simt::k_chol_inv<false><<<njob, simt::CHOL_NT, 0, s>>>(jobs, ps, 1, order);
     tcstream::k_stream<false><<<std::min(nt, p->num_sms), tcstream::NTHREADS, tcstream::SMEM_BYTES, s>>>(
         tab<tcstream::SJob>(p, base, p->t_tj[L][ps]), tab<tcstream::Item>(p, base, p->t_it_tr[L]), nt);
   }
@@ -884,7 +897,7 @@ dion_status_t orth_noalloc_impl(const float* A, long long rows, long long r, lon
   const size_t chol_smem = (size_t)((r * (r + 1) + r + 32 * r) * 4);   // <= 25 KB at r = 64
   for (int pass = 0; pass < 3; ++pass) {
     simt::k_gram<<<ngram, simt::NT, 0, s>>>(jobs, tg, 1, pass);
-    simt::k_chol_inv<true><<<1, simt::CHOL_NT, chol_smem, s>>>(jobs, pass, 0);
+    simt::k_chol_inv<true><<<1, simt::CHOL_NT, chol_smem, s>>>(jobs, pass, 0, nullptr);
     simt::k_trmm<<<ntrmm, simt::NT, 0, s>>>(jobs, tt, 1, pass);
   }
   dion_status_t st = cuda_check("orth launch");

@@ -326,10 +326,13 @@ __device__ void inverse_blocks(float* S, int lds, int r, float* tdiag, float* sc
   }
 }
 
+// order (optional): job of each CTA, largest rank first, so that the big jobs
+// share the first wave of CTAs.
 template <bool SMEM>
-__global__ void __launch_bounds__(CHOL_NT, 1) k_chol_inv(const OrthJob* __restrict__ jobs, int pass, int reduced) {
+__global__ void __launch_bounds__(CHOL_NT, 1) k_chol_inv(const OrthJob* __restrict__ jobs, int pass, int reduced,
+                                                        const int* __restrict__ order) {
   extern __shared__ float sm_dyn[];
-  const OrthJob& o = jobs[blockIdx.x];
+  const OrthJob& o = jobs[order ? order[blockIdx.x] : blockIdx.x];
   __shared__ int s_bad;
   __shared__ float s_min, s_max;
   __shared__ float s_trace[CHOL_NT / 32];

@@ -380,12 +380,23 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
       if (grow < j.rows) {
         dst += (long long)grow * ld;
         const int cbase = it.c0 + g * qw;
+        // 16-byte stores where the row is 16-byte aligned (leading dimension rp);
+        // element stores for Vbar written into V (leading dimension r)
+        const bool vec = ((ld & 3) == 0) && ((((uintptr_t)dst) & 15) == 0);
 #pragma unroll
         for (int cb = 0; cb < QMAX / 8; ++cb)
           if (cb * 8 < qw) {
+            const int c = cbase + cb * 8;
+            if (vec && c + 8 <= cols) {
+              *reinterpret_cast<float4*>(dst + c) =
+                  make_float4(acc[cb * 8], acc[cb * 8 + 1], acc[cb * 8 + 2], acc[cb * 8 + 3]);
+              *reinterpret_cast<float4*>(dst + c + 4) =
+                  make_float4(acc[cb * 8 + 4], acc[cb * 8 + 5], acc[cb * 8 + 6], acc[cb * 8 + 7]);
+            } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              if (cbase + cb * 8 + k < cols) dst[cbase + cb * 8 + k] = acc[cb * 8 + k];
+              for (int k = 0; k < 8; ++k)
+                if (c + k < cols) dst[c + k] = acc[cb * 8 + k];
+            }
           }
       }
     }
