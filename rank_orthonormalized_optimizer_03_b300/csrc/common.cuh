@@ -34,6 +34,8 @@ struct MatDev {
   float* U;            // m x rp   U = orth(P)
   float* W;            // n x rp   W = M^T U
   float* Wpart;        // ksplit x n x rp partial sums of W (when ksplit > 1)
+  float* Wh;           // n x rp   tf32 halves of W (operands of the update), zero beyond column r
+  float* Wl;
   int ksplit;          // split of the m-range in phase (c)
   int kchunk;          // rows of M per split
   unsigned* status;    // per-matrix status word

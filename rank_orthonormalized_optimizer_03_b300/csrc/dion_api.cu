@@ -89,6 +89,8 @@ struct dion_plan {
   size_t t_epi = 0, t_split = 0, t_ts_split = 0;
   std::vector<int> ts_split;
   int n_split = 0;
+  // k_split jobs (matrix, 0: U / 1: Vbar): the halves that no earlier kernel wrote
+  std::vector<std::pair<int, int>> split_list;
   int num_sms = 0;
   // phases (a) and (c): streaming jobs, transposed split copies V^T, U^T
   std::vector<int> ncb, bn;
@@ -249,13 +251,20 @@ void layout(dion_plan* p) {
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 128); return o; };
   // tensor-core tables first: they hold CUtensorMaps (64-byte alignment)
-  p->n_split = 3 * cnt;
+  // tf32 halves for the update: the tensor-core orth() writes those of U and of an
+  // Orth-Dion Vbar itself, phase (c) those of W; the rest come from k_split
+  p->split_list.clear();
+  for (int i = 0; i < cnt; ++i) {
+    if (!p->tc_orth) p->split_list.push_back({i, 0});
+    if (!p->tc_orth || D(i).variant == DION_VARIANT_DION) p->split_list.push_back({i, 1});
+  }
+  p->n_split = (int)p->split_list.size();
   {
     std::vector<int> jobs(p->n_split);
     for (int k = 0; k < p->n_split; ++k) jobs[k] = k;
     prefix(p->ts_split, jobs, [&](int k) {
-      const int i = k / 3;
-      const long long rows = (k % 3 == 0) ? D(i).m : D(i).n;
+      const int i = p->split_list[k].first;
+      const long long rows = p->split_list[k].second == 0 ? D(i).m : D(i).n;
       return cdiv(rows * p->rp[i], tcsplit::ELEMS_PER_CTA);
     });
   }
@@ -347,7 +356,7 @@ void layout(dion_plan* p) {
   p->t_sj_a = take(sizeof(tcstream::SJob) * cnt);
   p->t_sj_c = take(sizeof(tcstream::SJob) * cnt);
   p->t_epi = take(sizeof(tcepi::EpiMat) * cnt);
-  p->t_split = take(sizeof(tcsplit::SplitJob) * p->n_split);
+  p->t_split = take(sizeof(tcsplit::SplitJob) * std::max(1, p->n_split));
   p->t_ts_split = take(4 * p->ts_split.size());
   p->t_tj_v = take(sizeof(tcsplit::TJob) * cnt);
   p->t_tj_u = take(sizeof(tcsplit::TJob) * cnt);
@@ -478,6 +487,8 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     x.U = reinterpret_cast<float*>(base + p->off_U[i]);
     x.W = reinterpret_cast<float*>(base + p->off_W[i]);
     x.Wpart = reinterpret_cast<float*>(base + p->off_Wpart[i]);
+    x.Wh = reinterpret_cast<float*>(base + p->off_Wh[i]);
+    x.Wl = reinterpret_cast<float*>(base + p->off_Wl[i]);
     x.ksplit = p->ksplit[i];
     x.kchunk = p->kchunk[i];
     x.status = status + i;
@@ -535,7 +546,7 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
 
   // ---- tensor-core phase (e): operand maps (split copies in the workspace) and state maps
   std::vector<tcepi::EpiMat> epi(cnt);
-  std::vector<tcsplit::SplitJob> sj(p->n_split);
+  std::vector<tcsplit::SplitJob> sj(std::max(1, p->n_split));
   const CUtensorMapDataType F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   for (int i = 0; i < cnt; ++i) {
     const auto& d = p->descs[i];
@@ -568,10 +579,19 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     if (!okm) return fail(DION_ERR_CUDA, "matrix %d: cuTensorMapEncodeTiled failed", i);
     e.m = (int)d.m; e.n = (int)d.n; e.rp = (int)rp; e.g_bf16 = x.g_bf16;
     e.eta_s = x.eta_s; e.beta = x.beta; e.status = x.status;
-    // split jobs: U (workspace, ld rp), Vbar (= V after phase (d), ld r), W (workspace, ld rp)
-    sj[3 * i + 0] = tcsplit::SplitJob{x.U, rp, Uh, Ul, rp, d.m, d.r, x.status};
-    sj[3 * i + 1] = tcsplit::SplitJob{d.V, d.r, Vh, Vl, rp, d.n, d.r, x.status};
-    sj[3 * i + 2] = tcsplit::SplitJob{x.W, rp, Wh, Wl, rp, d.n, d.r, x.status};
+  }
+  // split jobs: U (workspace, ld rp), Vbar (= V after phase (d), ld r)
+  for (int k = 0; k < p->n_split; ++k) {
+    const int i = p->split_list[k].first;
+    const auto& d = p->descs[i];
+    const MatDev& x = mats[i];
+    const long long rp = p->rp[i];
+    if (p->split_list[k].second == 0)
+      sj[k] = tcsplit::SplitJob{x.U, rp, reinterpret_cast<float*>(base + p->off_Uh[i]),
+                                reinterpret_cast<float*>(base + p->off_Ul[i]), rp, d.m, d.r, x.status};
+    else
+      sj[k] = tcsplit::SplitJob{d.V, d.r, reinterpret_cast<float*>(base + p->off_Vh[i]),
+                                reinterpret_cast<float*>(base + p->off_Vl[i]), rp, d.n, d.r, x.status};
   }
   // ---- tensor-core phases (a) and (c)
   std::vector<tcstream::SJob> sa(cnt), sc(cnt);
@@ -612,6 +632,10 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     c.rows = (int)d.n; c.kdim = (int)d.m; c.ksplit = p->ksplit[i]; c.kchunk = p->kchunk[i];
     c.ncb = p->ncb[i]; c.bn = p->bn[i]; c.rp = (int)rp; c.gmode = gb ? tcstream::G_BF16 : tcstream::G_F32;
     c.status = x.status; c.pass = -1; c.out_cols = (int)rp;
+    if (p->ksplit[i] == 1) {
+      // W written whole by this launch: its halves too (else by the reduction)
+      c.sh = x.Wh; c.sl = x.Wl; c.hcols = (int)d.r;
+    }
     tv[i] = tcsplit::TJob{x.Vin, x.ldvin, VTh, VTl, p->ldt_n[i], d.n, d.r, rp, x.status};
     tu[i] = tcsplit::TJob{x.U, rp, UTh, UTl, p->ldt_m[i], d.m, d.r, rp, x.status};
   }
@@ -645,6 +669,20 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
           t.pass = ps; t.out_cols = (int)o.out_cols; t.rows = (int)o.rows; t.kdim = (int)rp;
           t.ksplit = 1; t.kchunk = (int)rp; t.ncb = p->ncb[i]; t.bn = p->bn[i]; t.rp = (int)rp;
           t.gmode = tcstream::G_NONE; t.status = o.status;
+          if (L == 0) {
+            // U: halves for the update, transposed halves for W = M^T U
+            t.sh = reinterpret_cast<float*>(base + p->off_Uh[i]);
+            t.sl = reinterpret_cast<float*>(base + p->off_Ul[i]);
+            t.th = reinterpret_cast<float*>(base + p->off_UTh[i]);
+            t.tl = reinterpret_cast<float*>(base + p->off_UTl[i]);
+            t.ld_t = p->ldt_m[i];
+            t.hcols = (int)p->descs[i].r;
+          } else if (L == 1) {
+            // Orth-Dion Vbar: halves for the update
+            t.sh = reinterpret_cast<float*>(base + p->off_Vh[i]);
+            t.sl = reinterpret_cast<float*>(base + p->off_Vl[i]);
+            t.hcols = (int)p->descs[i].r;
+          }
         }
         put(p->image, p->t_gj[L][ps], gj.data(), gj.size());
         put(p->image, p->t_tj[L][ps], tj.data(), tj.size());
@@ -796,8 +834,9 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
         if (st) return st;
         break;
       case 2:
-        tcsplit::k_tsplit<<<p->ts_tu[cnt], tcsplit::NT, 0, s>>>(
-            tab<tcsplit::TJob>(p, base, p->t_tj_u), tab<int>(p, base, p->t_ts_tu), cnt);
+        if (!p->tc_orth)   // else the last A T pass of orth(P) wrote U^T's halves
+          tcsplit::k_tsplit<<<p->ts_tu[cnt], tcsplit::NT, 0, s>>>(
+              tab<tcsplit::TJob>(p, base, p->t_tj_u), tab<int>(p, base, p->t_ts_tu), cnt);
         tcstream::k_stream<true><<<std::min((int)p->it_sc.size(), p->num_sms), tcstream::NTHREADS,
                                    tcstream::SMEM_BYTES, s>>>(tab<tcstream::SJob>(p, base, p->t_sj_c),
                                                               tab<tcstream::Item>(p, base, p->t_it_sc),
@@ -814,9 +853,10 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
           simt::k_colnorm<<<p->ts_coln[p->dion_idx.size()], simt::NT, 0, s>>>(
               mats, tab<int>(p, base, p->t_ts_coln), tab<int>(p, base, p->t_coln_idx),
               (int)p->dion_idx.size());
-        // tf32 halves of U, Vbar and W: the operands of the tensor-core update (e)
-        tcsplit::k_split<<<p->ts_split[p->n_split], tcsplit::NT, 0, s>>>(
-            tab<tcsplit::SplitJob>(p, base, p->t_split), tab<int>(p, base, p->t_ts_split), p->n_split);
+        // tf32 halves of the update's operands that no earlier kernel wrote
+        if (p->n_split > 0)
+          tcsplit::k_split<<<p->ts_split[p->n_split], tcsplit::NT, 0, s>>>(
+              tab<tcsplit::SplitJob>(p, base, p->t_split), tab<int>(p, base, p->t_ts_split), p->n_split);
         break;
       case 4: {
         const int tiles = (int)p->it_epi.size();
@@ -1042,10 +1082,10 @@ int32_t dion_plan_launches_per_step(const dion_plan* plan) {
   const int per_orth = plan->tc_orth ? 12 : 9;  // up to three CholeskyQR rounds (+ partial reduce)
   n += plan->dion_idx.empty() ? 0 : per_orth + (plan->tc_orth ? 1 : 0);   // phase (a): orth(V) of Dion matrices
   n += per_orth;                               // phase (b)
-  n += 2 + (plan->any_split ? 1 : 0);          // phase (c): U^T split, tensor-core W = M^T U, reduce
+  n += (plan->tc_orth ? 1 : 2) + (plan->any_split ? 1 : 0);   // phase (c): [U^T split], W = M^T U, reduce
   n += plan->orth_idx.empty() ? 0 : per_orth;  // phase (d), Orth-Dion matrices
   n += plan->dion_idx.empty() ? 0 : 1;         // phase (d), Dion matrices
-  n += 1;                                      // phase (d): tf32 halves of U, Vbar, W
+  n += plan->n_split > 0 ? 1 : 0;              // phase (d): tf32 halves left to split
   n += 1;                                      // phase (e): tensor-core update
   return n;
 }

@@ -418,7 +418,8 @@ __global__ void __launch_bounds__(NT) k_trmm(const OrthJob* __restrict__ jobs,
 }
 
 // ---------------------------------------------------------------- phase (c)
-// W = sum over splits (fixed order); one CTA covers 1024 elements.
+// W = sum over splits (fixed order), with its tf32 halves for the update;
+// one CTA covers 1024 elements.
 __global__ void __launch_bounds__(NT) k_wreduce(const MatDev* __restrict__ mats,
                                                 const int* __restrict__ tstart, int nmat) {
   const int j = find_job(tstart, nmat, blockIdx.x);
@@ -432,6 +433,10 @@ __global__ void __launch_bounds__(NT) k_wreduce(const MatDev* __restrict__ mats,
     float s = 0.f;
     for (int sp = 0; sp < d.ksplit; ++sp) s += d.Wpart[(long long)sp * tot + idx];
     d.W[idx] = s;
+    float h, l;
+    tc::split_tf32(idx % d.rp < d.r ? s : 0.f, h, l);
+    d.Wh[idx] = h;
+    d.Wl[idx] = l;
   }
 }
 

@@ -6,12 +6,14 @@
 //     (c)  W = M^T U     rows j of M^T, K = m    (TRANS = true, K split over CTAs)
 //
 // M is never stored: every CTA streams G and R tiles by TMA into a staging
-// ring, and 8 converter warps form M = G + R in fp32, split it into the two
+// ring, and 16 converter warps form M = G + R in fp32, split it into the two
 // tf32 halves of a 3xTF32 product and write them into the 64-byte-swizzled
-// K-major operand layout the MMA reads (transposing 4 x 2 register blocks on
-// the way for M^T).  The second operand (V^T or U^T, already split) comes in by
-// TMA.  Chunks of 16 along K keep four operand stages and four staging slots
-// in flight in shared memory.
+// K-major operand layout the MMA reads (one thread per operand row; for M^T a
+// thread gathers one column of the staged rows).  The second operand (V^T or
+// U^T, already split) comes in by TMA.  Chunks of 16 along K keep four operand
+// stages and four staging slots in flight in shared memory.  The same kernel
+// runs the A T products of orth(); its final pass also writes the tf32 halves
+// of the result for the next tensor-core kernels.
 //
 // The tensor core's fp32 accumulation truncates: its bias grows with the
 // number of accumulation steps (measured -1e-5 relative per 1024 of K).  So a
@@ -76,7 +78,15 @@ struct SJob {
   int ncb, bn;                    // column blocks of width bn (multiple of 32, <= BN_MAX)
   int rp, gmode;
   unsigned* status;
-  int pad[6];
+  // tf32 halves of the final result for the tensor-core kernels that read it next
+  // (null: none): row-major with leading dimension rp, and (th / tl) transposed with
+  // leading dimension ld_t; columns hcols..rp-1 are written as zero
+  float* sh;
+  float* sl;
+  float* th;
+  float* tl;
+  long long ld_t;
+  int hcols;
 };
 static_assert(sizeof(SJob) % 64 == 0, "SJob must keep 64-byte alignment of its maps");
 
@@ -372,10 +382,12 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
       float* dst = j.out + (long long)it.ks * j.split_stride;
       long long ld = j.ld_out;
       int cols = j.out_cols;
+      bool fin = true;                       // writing the job's final result
       if (j.pass == 0 || (j.pass == 1 && *j.flag)) {
         dst = j.pass == 0 ? j.q1 : j.q2;
         ld = j.rp;
         cols = j.rp;
+        fin = false;
       }
       if (grow < j.rows) {
         dst += (long long)grow * ld;
@@ -398,6 +410,32 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
                 if (c + k < cols) dst[c + k] = acc[cb * 8 + k];
             }
           }
+        if (fin && j.sh) {
+          // the halves: c is a multiple of 8 and rp of 32, so a block of 8 is in or out
+          float* hrow = j.sh + (long long)grow * j.rp;
+          float* lrow = j.sl + (long long)grow * j.rp;
+#pragma unroll
+          for (int cb = 0; cb < QMAX / 8; ++cb)
+            if (cb * 8 < qw && cbase + cb * 8 < j.rp) {
+              const int c = cbase + cb * 8;
+              float h[8], l[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) split_tf32(c + k < j.hcols ? acc[cb * 8 + k] : 0.f, h[k], l[k]);
+              *reinterpret_cast<float4*>(hrow + c) = make_float4(h[0], h[1], h[2], h[3]);
+              *reinterpret_cast<float4*>(hrow + c + 4) = make_float4(h[4], h[5], h[6], h[7]);
+              *reinterpret_cast<float4*>(lrow + c) = make_float4(l[0], l[1], l[2], l[3]);
+              *reinterpret_cast<float4*>(lrow + c + 4) = make_float4(l[4], l[5], l[6], l[7]);
+              if (j.th) {
+                // transposed: the 32 lanes of a warp hold 32 consecutive rows, so each
+                // column is one 128-byte segment
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  j.th[(long long)(c + k) * j.ld_t + grow] = h[k];
+                  j.tl[(long long)(c + k) * j.ld_t + grow] = l[k];
+                }
+              }
+            }
+        }
       }
     }
   }
