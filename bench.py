@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--variant", default="orth", choices=["orth", "dion", "mixed"])
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-groups", type=int, default=14,
+                    help="matrix groups of the host-fed end-to-end step (copy/compute overlap)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seed", type=int, default=0)
@@ -278,25 +280,28 @@ def run_cuda(args):
 
 
 def run_e2e(args, plan, mats, stream, step_bytes, world):
-    """The same step through the public API with host buffers: every step copies
-    the gradients host->device from pinned memory, steps, and reads the
-    per-matrix status words back."""
-    import torch
+    """The same step through the public API with host-resident gradients:
+    dion.HostFedStep copies every step's gradients from pinned host memory, in
+    groups whose copy overlaps the previous group's step, and the per-matrix
+    status words are read back (which synchronises)."""
+    from rank_orthonormalized_optimizer_03_b300 import dion
     host_g = [d["G"].to("cpu").pin_memory() for d in mats]
-    h2d = sum(g.numel() * g.element_size() for g in host_g)
+    stepper = dion.HostFedStep(mats, groups=args.e2e_groups)
+    h2d = stepper.h2d_bytes()
     d2h = 4 * len(mats)
     steps = max(1, min(args.steps, 5))
-    plan.step()
-    torch.cuda.synchronize()
+    stepper.step(host_g)
+    stepper.status()
     t0 = time.perf_counter()
     for _ in range(steps):
-        for d, g in zip(mats, host_g):
-            d["G"].copy_(g, non_blocking=True)
-        plan.step()
-        plan.status()           # device -> host read of the step's result, synchronises
+        stepper.step(host_g)
+        stepper.status()        # device -> host read of the step's result
     dt = (time.perf_counter() - t0) / steps
+    groups = len(stepper.plans)
+    stepper.close()
     return {"value": round(world * step_bytes / dt / 1e9, 2), "unit": "GB/s", "ms_per_step": round(dt * 1e3, 3),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "api": f"HostFedStep, {groups} groups (copy of group g+1 overlaps the step of group g)"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle

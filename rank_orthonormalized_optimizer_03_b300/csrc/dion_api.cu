@@ -111,9 +111,10 @@ struct dion_plan {
   std::vector<int> ts_vcopy;
   // work-item tables of the persistent tensor-core kernels (built on the host, heaviest first)
   std::vector<tcstream::Item> it_sa, it_sc, it_tr[3];
-  std::vector<tcepi::Tile> it_epi;
+  std::vector<std::vector<tcepi::Tile>> it_epi;   // per K pass of the update
   std::vector<tcgram::GItem> it_g[3];
-  size_t t_it_sa = 0, t_it_sc = 0, t_it_tr[3] = {}, t_it_epi = 0, t_it_g[3] = {};
+  size_t t_it_sa = 0, t_it_sc = 0, t_it_tr[3] = {}, t_it_g[3] = {};
+  std::vector<size_t> t_it_epi;
 
   std::vector<unsigned char> image;
   const void* uploaded_ws = nullptr;
@@ -330,20 +331,30 @@ void layout(dion_plan* p) {
       }
       by_cost(p->it_tr[L], p->bn, false, lists[L]);
     }
-    p->it_epi.clear();
-    for (int i = 0; i < cnt; ++i)
-      for (long long i0 = 0; i0 < D(i).m; i0 += tcepi::BM)
-        for (long long j0 = 0; j0 < D(i).n; j0 += tcepi::BNJ)
-          p->it_epi.push_back(tcepi::Tile{i, (int)i0, (int)j0, 0});
-    std::stable_sort(p->it_epi.begin(), p->it_epi.end(), [&](const tcepi::Tile& a, const tcepi::Tile& b) {
-      return p->rp[a.mat] > p->rp[b.mat]; });
+    // update tiles per K pass: pass k holds the matrices with rp > k * KPASS
+    long long rpmax = 0;
+    for (int i = 0; i < cnt; ++i) rpmax = std::max<long long>(rpmax, p->rp[i]);
+    const int npass = (int)cdiv(rpmax, tcepi::KPASS);
+    p->it_epi.assign(npass, {});
+    for (int k = 0; k < npass; ++k) {
+      for (int i = 0; i < cnt; ++i) {
+        if (p->rp[i] <= (long long)k * tcepi::KPASS) continue;
+        for (long long i0 = 0; i0 < D(i).m; i0 += tcepi::BM)
+          for (long long j0 = 0; j0 < D(i).n; j0 += tcepi::BNJ)
+            p->it_epi[k].push_back(tcepi::Tile{i, (int)i0, (int)j0, 0});
+      }
+      std::stable_sort(p->it_epi[k].begin(), p->it_epi[k].end(), [&](const tcepi::Tile& a, const tcepi::Tile& b) {
+        return p->rp[a.mat] > p->rp[b.mat]; });
+    }
     p->t_it_sa = take(sizeof(tcstream::Item) * std::max<size_t>(1, p->it_sa.size()));
     p->t_it_sc = take(sizeof(tcstream::Item) * std::max<size_t>(1, p->it_sc.size()));
     for (int L = 0; L < 3; ++L) {
       p->t_it_tr[L] = take(sizeof(tcstream::Item) * std::max<size_t>(1, p->it_tr[L].size()));
       p->t_it_g[L] = take(sizeof(tcgram::GItem) * std::max<size_t>(1, p->it_g[L].size()));
     }
-    p->t_it_epi = take(sizeof(tcepi::Tile) * std::max<size_t>(1, p->it_epi.size()));
+    p->t_it_epi.resize(p->it_epi.size());
+    for (size_t k = 0; k < p->it_epi.size(); ++k)
+      p->t_it_epi[k] = take(sizeof(tcepi::Tile) * std::max<size_t>(1, p->it_epi[k].size()));
     for (int L = 0; L < 3; ++L) {
       const size_t nj = lists[L]->size();
       p->chol_order[L].resize(nj);
@@ -704,7 +715,8 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     if (!p->it_tr[L].empty()) put(p->image, p->t_it_tr[L], p->it_tr[L].data(), p->it_tr[L].size());
     if (!p->it_g[L].empty()) put(p->image, p->t_it_g[L], p->it_g[L].data(), p->it_g[L].size());
   }
-  if (!p->it_epi.empty()) put(p->image, p->t_it_epi, p->it_epi.data(), p->it_epi.size());
+  for (size_t k = 0; k < p->it_epi.size(); ++k)
+    if (!p->it_epi[k].empty()) put(p->image, p->t_it_epi[k], p->it_epi[k].data(), p->it_epi[k].size());
   for (int L = 0; L < 3; ++L)
     if (!p->chol_order[L].empty()) put(p->image, p->t_chol_order[L], p->chol_order[L].data(), p->chol_order[L].size());
   put(p->image, p->t_sj_a, sa.data(), sa.size());
@@ -859,11 +871,14 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
               tab<tcsplit::SplitJob>(p, base, p->t_split), tab<int>(p, base, p->t_ts_split), p->n_split);
         break;
       case 4: {
-        const int tiles = (int)p->it_epi.size();
-        const int grid = std::min(tiles, p->num_sms);
-        tcepi::k_epi<<<grid, tcepi::NTHREADS, tcepi::SMEM_BYTES, s>>>(
-            tab<tcepi::EpiMat>(p, base, p->t_epi), tab<tcepi::Tile>(p, base, p->t_it_epi), tiles,
-            p->any_g_f32 ? 24576 : 20480, p->any_g_f32 ? 3 : 4);
+        // one launch per K pass (K <= KPASS accumulated in TMEM per launch)
+        for (size_t k = 0; k < p->it_epi.size(); ++k) {
+          const int tiles = (int)p->it_epi[k].size();
+          const int grid = std::min(tiles, p->num_sms);
+          tcepi::k_epi<<<grid, tcepi::NTHREADS, tcepi::SMEM_BYTES, s>>>(
+              tab<tcepi::EpiMat>(p, base, p->t_epi), tab<tcepi::Tile>(p, base, p->t_it_epi[k]), tiles,
+              p->any_g_f32 ? 24576 : 20480, p->any_g_f32 ? 3 : 4, (int)k);
+        }
         break;
       }
     }
@@ -1086,7 +1101,7 @@ int32_t dion_plan_launches_per_step(const dion_plan* plan) {
   n += plan->orth_idx.empty() ? 0 : per_orth;  // phase (d), Orth-Dion matrices
   n += plan->dion_idx.empty() ? 0 : 1;         // phase (d), Dion matrices
   n += plan->n_split > 0 ? 1 : 0;              // phase (d): tf32 halves left to split
-  n += 1;                                      // phase (e): tensor-core update
+  n += (int)plan->it_epi.size();               // phase (e): tensor-core update, one launch per K pass
   return n;
 }
 

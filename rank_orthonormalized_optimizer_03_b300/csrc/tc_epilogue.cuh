@@ -5,6 +5,14 @@
 //     T1 = U Vbar^T,  T2 = U W^T            (K = r, 3xTF32, fp32 accumulation in TMEM)
 //     X <- X - eta s T1,   R <- beta (G + R - T2)
 //
+// The tensor core's fp32 accumulation truncates (its bias grows with the number
+// of accumulation steps, about -1e-5 relative per 1024 of K), and R can be a
+// small difference of large terms.  So one launch accumulates at most KPASS of
+// K: a matrix with r > KPASS takes several launches ("K passes"), the first
+// one as above with the first KPASS of K, every later one
+//     X <- X - eta s T1',  R <- R - beta T2'
+// with the next KPASS of K, the partial results carried in HBM in fp32.
+//
 // One CTA per SM, persistent over 128 x 128 tiles of every m x n matrix.
 // Warp roles:
 //   0  TMA producer of the MMA operands (U hi/lo rows; [Vbar; W] hi/lo rows)
@@ -34,6 +42,7 @@ constexpr int SUB = 16;          // columns per streamed sub-chunk
 constexpr int QSTAGES_MAX = 4;   // streamed-state ring; the slot count is chosen per launch
 constexpr int NTHREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;   // 2 accumulators x NMMA
+constexpr int KPASS = 256;            // K accumulated per launch (per K pass)
 
 constexpr uint32_t A_BYTES = BM * BK * 4;            // 8 KB
 constexpr uint32_t BH_BYTES = NMMA * BK * 4;         // 16 KB ([Vbar; W] 256 rows)
@@ -55,7 +64,8 @@ struct EpiMat {
 };
 static_assert(sizeof(EpiMat) % 64 == 0, "EpiMat must keep 64-byte alignment of its maps");
 
-// One 128 x 128 tile of matrix `mat` at rows i0.., columns j0.. (host-built table).
+// One 128 x 128 tile of matrix `mat` at rows i0.., columns j0.. (host-built table,
+// one per K pass holding the matrices with rp > KPASS * pass).
 struct Tile {
   int mat, i0, j0, pad;
 };
@@ -68,7 +78,7 @@ __device__ __forceinline__ int nsub(const EpiMat& e, int j0) {
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntiles, int qslot, int nq) {
+k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntiles, int qslot, int nq, int kpass) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* ost = smem;                                   // operand ring
@@ -76,6 +86,7 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
   const int QSTAGES = nq;                  // streamed-state slots of this launch (<= QSTAGES_MAX)
   const int QST_BYTES = qslot;
   const int Q_R = qslot - 2 * RX_BYTES;    // offsets of R and X in a slot (G first)
+  const int kc0 = kpass * (KPASS / BK);    // first K chunk of this pass
   uint64_t* bars = (uint64_t*)(qst + QREG_BYTES);
   uint64_t* op_full = bars;
   uint64_t* op_empty = op_full + OSTAGES;
@@ -110,9 +121,9 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile tl = tiles[t];
       const EpiMat& e = mats[tl.mat];
-      if (skip(e)) continue;
-      const int nk = (e.rp + BK - 1) / BK;
-      for (int kc = 0; kc < nk; ++kc) {
+      if (skip(e) || kc0 * BK >= e.rp) continue;
+      const int kc1 = min((e.rp + BK - 1) / BK, kc0 + KPASS / BK);
+      for (int kc = kc0; kc < kc1; ++kc) {
         if (!mbar_wait(&op_empty[s], ph ^ 1, abort_flag)) { failed_mat = tl.mat; goto prod_done; }
         mbar_arrive_expect_tx(&op_full[s], OST_BYTES);
         unsigned char* b = ost + s * OST_BYTES;
@@ -138,12 +149,12 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile tl = tiles[t];
       const EpiMat& e = mats[tl.mat];
-      if (skip(e)) continue;
-      const int nk = (e.rp + BK - 1) / BK;
+      if (skip(e) || kc0 * BK >= e.rp) continue;
+      const int kc1 = min((e.rp + BK - 1) / BK, kc0 + KPASS / BK);
       if (!mbar_wait(&acc_empty[b], aph[b] ^ 1, abort_flag)) { failed_mat = tl.mat; goto mma_done; }
       tc_fence_after();
       const uint32_t d = tmem + b * NMMA;
-      for (int kc = 0; kc < nk; ++kc) {
+      for (int kc = kc0; kc < kc1; ++kc) {
         if (!mbar_wait(&op_full[s], ph, abort_flag)) { failed_mat = tl.mat; goto mma_done; }
         tc_fence_after();
         const uint32_t ah = smem_u32(ost + s * OST_BYTES), al = ah + A_BYTES;
@@ -151,7 +162,7 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
 #pragma unroll
         for (int kk = 0; kk < BK / 8; ++kk) {
           const uint32_t o = kk * 32;
-          mma_tf32(d, sdesc_k_sw64(al + o), sdesc_k_sw64(bh + o), idesc, (kc | kk) != 0);
+          mma_tf32(d, sdesc_k_sw64(al + o), sdesc_k_sw64(bh + o), idesc, ((kc - kc0) | kk) != 0);
           mma_tf32(d, sdesc_k_sw64(ah + o), sdesc_k_sw64(bl + o), idesc, 1);
           mma_tf32(d, sdesc_k_sw64(ah + o), sdesc_k_sw64(bh + o), idesc, 1);
         }
@@ -171,15 +182,16 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile tl = tiles[t];
       const EpiMat& e = mats[tl.mat];
-      if (skip(e)) continue;
-      const uint32_t gbytes = e.g_bf16 ? BM * SUB * 2 : BM * SUB * 4;
+      if (skip(e) || kc0 * BK >= e.rp) continue;
+      // later K passes read the carried R and X only
+      const uint32_t gbytes = kpass > 0 ? 0u : (e.g_bf16 ? BM * SUB * 2 : BM * SUB * 4);
       const int ns = nsub(e, tl.j0);
       for (int sc = 0; sc < ns; ++sc) {
         if (!mbar_wait(&q_empty[q], ph ^ 1, abort_flag)) { failed_mat = tl.mat; goto stream_done; }
         mbar_arrive_expect_tx(&q_full[q], gbytes + 2 * RX_BYTES);
         unsigned char* b = qst + q * QST_BYTES;
         const int x = tl.j0 + sc * SUB;
-        tma_load_2d(b, &e.map[MAP_G], &q_full[q], x, tl.i0);
+        if (kpass == 0) tma_load_2d(b, &e.map[MAP_G], &q_full[q], x, tl.i0);
         tma_load_2d(b + Q_R, &e.map[MAP_R], &q_full[q], x, tl.i0);
         tma_load_2d(b + Q_R + RX_BYTES, &e.map[MAP_X], &q_full[q], x, tl.i0);
         used[q] = true; last_ph[q] = ph;
@@ -200,7 +212,7 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile tl = tiles[t];
       const EpiMat& e = mats[tl.mat];
-      if (skip(e)) continue;
+      if (skip(e) || kc0 * BK >= e.rp) continue;
       // every wait is followed by a vote of the 128 epilogue threads, so that
       // they leave together and nobody is left behind at a named barrier
       bool ok = mbar_wait(&acc_full[b], aph[b], abort_flag);
@@ -222,7 +234,11 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
         unsigned char* rb = gb + Q_R;
         unsigned char* xb = rb + RX_BYTES;
         float g[16];
-        if (e.g_bf16) {
+        if (kpass > 0) {
+          // a later K pass: R already holds beta (G + R - T2 of the earlier passes)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) g[k] = 0.f;
+        } else if (e.g_bf16) {
           // 32-byte rows, 32-byte swizzle: 16-byte chunk c of row t at c ^ ((t >> 2) & 1)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -252,10 +268,17 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
           x.y = fmaf(-eta_s, t1[k + 1], x.y);
           x.z = fmaf(-eta_s, t1[k + 2], x.z);
           x.w = fmaf(-eta_s, t1[k + 3], x.w);
-          r.x = beta * ((g[k] + r.x) - t2[k]);
-          r.y = beta * ((g[k + 1] + r.y) - t2[k + 1]);
-          r.z = beta * ((g[k + 2] + r.z) - t2[k + 2]);
-          r.w = beta * ((g[k + 3] + r.w) - t2[k + 3]);
+          if (kpass == 0) {
+            r.x = beta * ((g[k] + r.x) - t2[k]);
+            r.y = beta * ((g[k + 1] + r.y) - t2[k + 1]);
+            r.z = beta * ((g[k + 2] + r.z) - t2[k + 2]);
+            r.w = beta * ((g[k + 3] + r.w) - t2[k + 3]);
+          } else {
+            r.x = fmaf(-beta, t2[k], r.x);
+            r.y = fmaf(-beta, t2[k + 1], r.y);
+            r.z = fmaf(-beta, t2[k + 2], r.z);
+            r.w = fmaf(-beta, t2[k + 3], r.w);
+          }
           *reinterpret_cast<float4*>(rb + off) = r;
           *reinterpret_cast<float4*>(xb + off) = x;
         }

@@ -226,3 +226,75 @@ class Plan:
         nbytes = rows.value * ld.value * 4
         raw = self.workspace[off.value: off.value + nbytes]
         return raw.view(torch.float32).view(rows.value, ld.value)[:, : cols.value]
+
+
+def group_bounds(nbytes: Sequence[int], groups: int) -> List[tuple]:
+    """Split items 0..len-1 into at most ``groups`` consecutive ranges of about
+    equal total bytes (every range non-empty)."""
+    groups = max(1, min(groups, len(nbytes)))
+    total = float(sum(nbytes))
+    cuts, acc = [0], 0.0
+    for i, b in enumerate(nbytes[:-1]):
+        acc += b
+        # close a range once it reaches its share, leaving one item per remaining range
+        if len(cuts) < groups and acc >= total * len(cuts) / groups and len(nbytes) - (i + 1) >= groups - len(cuts):
+            cuts.append(i + 1)
+    cuts.append(len(nbytes))
+    return list(zip(cuts[:-1], cuts[1:]))
+
+
+class HostFedStep:
+    """Steps of a batch whose gradients arrive from (pinned) host memory.
+
+    The matrices are split into ``groups`` consecutive groups of about equal
+    gradient bytes, each with its own :class:`Plan`.  Every step copies group
+    g's gradients host -> device on a side stream and steps group g on the
+    caller's stream once they are in, so the copy of group g + 1 overlaps the
+    step of group g.  A group's copy waits until the previous step of that group
+    has read its gradients.  Each matrix gets the arithmetic of a plan over the
+    whole batch whenever each group still fills the GPU (the K split of W = M^T U
+    is the only choice that depends on the batch).
+    """
+
+    def __init__(self, mats: Sequence[dict], groups: int = 8):
+        import torch
+        self.mats = list(mats)
+        sizes = [d["G"].numel() * d["G"].element_size() for d in self.mats]
+        self.ranges = group_bounds(sizes, groups)
+        self.plans = [Plan(self.mats[a:b]) for a, b in self.ranges]
+        self.copy_stream = torch.cuda.Stream(device=self.mats[0]["X"].device)
+        self._read = [None] * len(self.plans)   # per group: event after its last step
+
+    def h2d_bytes(self) -> int:
+        return sum(d["G"].numel() * d["G"].element_size() for d in self.mats)
+
+    def step(self, host_grads: Sequence, stream=None):
+        """Copy ``host_grads[i]`` into matrix i's G and step every group (async)."""
+        import torch
+        if len(host_grads) != len(self.mats):
+            raise ValueError("one host gradient per matrix")
+        cs = stream if stream is not None else torch.cuda.current_stream()
+        for g, ((a, b), plan) in enumerate(zip(self.ranges, self.plans)):
+            ready = torch.cuda.Event()
+            with torch.cuda.stream(self.copy_stream):
+                if self._read[g] is not None:
+                    self.copy_stream.wait_event(self._read[g])
+                for i in range(a, b):
+                    self.mats[i]["G"].copy_(host_grads[i], non_blocking=True)
+                ready.record(self.copy_stream)
+            cs.wait_event(ready)
+            plan.step(cs)
+            done = torch.cuda.Event()
+            done.record(cs)
+            self._read[g] = done
+
+    def status(self, stream=None) -> List[int]:
+        """Per-matrix status words of the last step, in batch order (synchronises)."""
+        out: List[int] = []
+        for p in self.plans:
+            out += p.status(stream)
+        return out
+
+    def close(self):
+        for p in self.plans:
+            p.close()

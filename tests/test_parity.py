@@ -195,6 +195,34 @@ def test_mixed_batch_dtypes_variants_shapes(dev):
                    U_gpu=plan.buffer(k, dion.BUF_U))
 
 
+def test_update_in_k_passes_mixed_ranks(dev):
+    """Ranks above 256 take the update in several K passes (at most 256 of K
+    accumulated on the tensor core per launch); a batch mixing one, two and
+    three passes against the oracle."""
+    import torch
+    g = np.random.Generator(np.random.PCG64(11))
+    # bf16 row pitches stay multiples of 16 bytes (n a multiple of 8)
+    shapes = [(200, 160, 16, "orth"), (700, 600, 400, "orth"), (520, 896, 300, "dion"), (1100, 640, 520, "orth")]
+    mats = []
+    for m, n, r, var in shapes:
+        X = to_dev(g.normal(0, 0.02, (m, n)), dev)
+        R = to_dev(0.05 * g.standard_normal((m, n)), dev)
+        Gn = g.standard_normal((m, n)) + 0.2 * (g.standard_normal((m, 2)) @ g.standard_normal((2, n)))
+        G = grad_to_device(synth.f32_to_bf16_bits(Gn.astype(np.float32)), dev)
+        V = to_dev(g.standard_normal((n, r)) / math.sqrt(n), dev)
+        mats.append(dict(X=X, G=G, R=R, V=V, eta=0.02, beta=0.95, variant=var))
+    plan = dion.Plan(mats)
+    assert plan.launches_per_step > 0
+    befores = [state_snapshot(d) for d in mats]
+    plan.step()
+    torch.cuda.synchronize()
+    assert plan.failures() == [0] * len(mats)
+    for k, d in enumerate(mats):
+        _, errs = check_step(befores[k], grad_f64(d["G"]), d, 0.02, 0.95, d["variant"],
+                             U_gpu=plan.buffer(k, dion.BUF_U))
+        print(shapes[k], errs)
+
+
 # ---------------------------------------------------------------- failure handling
 def test_rank_deficient_sets_status_and_leaves_state(dev):
     import torch
