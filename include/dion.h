@@ -152,9 +152,11 @@ DION_API dion_status_t dion_step_batched(dion_plan* plan, void* workspace, size_
  *          orth(P) unchanged and keeps P well conditioned)
  *   1 (b): U = orth(P)                                     (U in the workspace)
  *   2 (c): W = (G + R)^T U                                 (W in the workspace)
- *   3 (d): Vbar = orth(W) or colnorm(W), written into V (and the tf32
- *          halves of U, Vbar and W that phase (e) reads, in the workspace)
- *   4 (e): X <- X - eta s U Vbar^T,  R <- beta (G + R - U W^T)
+ *   3 (d): Vbar = orth(W) or colnorm(W), written into V
+ *   4 (e): X <- X - eta s U Vbar^T,  R <- beta (G + R - U W^T), one launch per
+ *          256 of r (later launches carry X and R forward in fp32)
+ * The tf32 halves of U, U^T, W and Vbar that the tensor-core kernels read
+ * (workspace) are written by the phase that produces each factor.
  * Running 0..4 equals dion_step_batched().
  */
 DION_API dion_status_t dion_step_phases(dion_plan* plan, void* workspace, size_t ws_bytes,
