@@ -11,6 +11,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "simt.cuh"
 #include "tc_epilogue.cuh"
@@ -470,6 +472,118 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, long long
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Host check of the work tables that layout() built, before any kernel can use
+// them: every output tile of every launch covered exactly once, K ranges that
+// tile K without gaps or overlap, and every TMA x coordinate on a 16-byte
+// boundary (x * element size % 16 == 0; an unaligned x is an illegal
+// instruction on the device).  Returns an empty string or what is wrong.
+std::string verify_tables(const dion_plan* p) {
+  char buf[256];
+  auto bad = [&](const char* what, int i) {
+    std::snprintf(buf, sizeof buf, "%s (matrix %d)", what, i);
+    return std::string(buf);
+  };
+  const int cnt = p->count;
+  // (a): rows x column blocks, the whole of K; staging x = k (multiple of 16)
+  {
+    std::vector<std::vector<int>> seen(cnt);
+    for (int i = 0; i < cnt; ++i) seen[i].assign(cdiv(p->descs[i].m, tcstream::BM) * p->ncb[i], 0);
+    for (const auto& it : p->it_sa) {
+      const int i = it.job;
+      if (i < 0 || i >= cnt) return bad("phase (a) item of an unknown matrix", i);
+      const auto& d = p->descs[i];
+      if (it.row0 % tcstream::BM || it.row0 >= d.m || it.c0 % p->bn[i] || it.c0 >= p->rp[i] || it.k0 != 0 ||
+          (long long)it.nk * tcstream::BK < d.n || (long long)(it.nk - 1) * tcstream::BK >= d.n)
+        return bad("phase (a) item out of range", i);
+      if (++seen[i][(it.row0 / tcstream::BM) * p->ncb[i] + it.c0 / p->bn[i]] != 1)
+        return bad("phase (a) tile covered twice", i);
+    }
+    for (int i = 0; i < cnt; ++i)
+      for (int v : seen[i]) if (v != 1) return bad("phase (a) tile not covered", i);
+  }
+  // (c): rows of M^T x K ranges x column blocks; G / R boxes start at x = row0 + 32 b
+  // (row0 a multiple of 128), K ranges on multiples of 32
+  {
+    std::vector<std::vector<int>> seen(cnt);
+    for (int i = 0; i < cnt; ++i)
+      seen[i].assign(cdiv(p->descs[i].n, tcstream::BM) * p->ksplit[i] * p->ncb[i], 0);
+    for (const auto& it : p->it_sc) {
+      const int i = it.job;
+      if (i < 0 || i >= cnt) return bad("phase (c) item of an unknown matrix", i);
+      const auto& d = p->descs[i];
+      if (it.row0 % tcstream::BM || it.row0 >= d.n || it.c0 % p->bn[i] || it.c0 >= p->rp[i] ||
+          it.ks < 0 || it.ks >= p->ksplit[i] || it.k0 != (long long)it.ks * p->kchunk[i] || it.k0 % 32)
+        return bad("phase (c) item out of range", i);
+      const long long k1 = std::min<long long>(d.m, (long long)it.k0 + p->kchunk[i]);
+      if ((long long)it.nk != cdiv(k1 - it.k0, tcstream::BK)) return bad("phase (c) K range", i);
+      if (++seen[i][((it.row0 / tcstream::BM) * p->ksplit[i] + it.ks) * p->ncb[i] + it.c0 / p->bn[i]] != 1)
+        return bad("phase (c) tile covered twice", i);
+    }
+    for (int i = 0; i < cnt; ++i) {
+      for (int v : seen[i]) if (v != 1) return bad("phase (c) tile not covered", i);
+      if (p->kchunk[i] % 32 || (long long)p->ksplit[i] * p->kchunk[i] < p->descs[i].m ||
+          (long long)(p->ksplit[i] - 1) * p->kchunk[i] >= p->descs[i].m)
+        return bad("phase (c) K split", i);
+    }
+  }
+  // orth(): A T items cover the rows, Gram items the 256-row chunks, of every job
+  {
+    const std::vector<int>* lists[3] = {nullptr, &p->orth_idx, &p->dion_idx};
+    for (int L = 0; L < 3; ++L) {
+      const size_t nj = L == 0 ? (size_t)cnt : lists[L]->size();
+      std::vector<std::vector<int>> seen(nj), gseen(nj);
+      auto mat = [&](size_t k) { return L == 0 ? (int)k : (*lists[L])[k]; };
+      auto rows = [&](size_t k) { return L == 0 ? p->descs[mat(k)].m : p->descs[mat(k)].n; };
+      for (size_t k = 0; k < nj; ++k) {
+        seen[k].assign(cdiv(rows(k), tcstream::BM) * p->ncb[mat(k)], 0);
+        gseen[k].assign(cdiv(rows(k), tcgram::CHUNK_ROWS), 0);
+      }
+      for (const auto& it : p->it_tr[L]) {
+        if (it.job < 0 || (size_t)it.job >= nj) return bad("orth() item of an unknown job", it.job);
+        const int i = mat(it.job);
+        if (it.row0 % tcstream::BM || it.row0 >= rows(it.job) || it.c0 % p->bn[i] || it.c0 >= p->rp[i] ||
+            it.k0 != 0 || (long long)it.nk * tcstream::BK != p->rp[i])
+          return bad("orth() item out of range", i);
+        if (++seen[it.job][(it.row0 / tcstream::BM) * p->ncb[i] + it.c0 / p->bn[i]] != 1)
+          return bad("orth() tile covered twice", i);
+      }
+      for (const auto& g : p->it_g[L]) {
+        if (g.job < 0 || (size_t)g.job >= nj || g.chunk < 0 || (size_t)g.chunk >= gseen[g.job].size())
+          return bad("Gram item out of range", g.job);
+        if (++gseen[g.job][g.chunk] != 1) return bad("Gram chunk covered twice", mat(g.job));
+      }
+      for (size_t k = 0; k < nj; ++k) {
+        for (int v : seen[k]) if (v != 1) return bad("orth() tile not covered", mat(k));
+        for (int v : gseen[k]) if (v != 1) return bad("Gram chunk not covered", mat(k));
+      }
+    }
+  }
+  // (e): every K pass covers the m x n tiles of exactly the matrices with rp > KPASS * pass
+  for (size_t k = 0; k < p->it_epi.size(); ++k) {
+    std::vector<std::vector<int>> seen(cnt);
+    for (int i = 0; i < cnt; ++i)
+      if (p->rp[i] > (long long)k * tcepi::KPASS)
+        seen[i].assign(cdiv(p->descs[i].m, tcepi::BM) * cdiv(p->descs[i].n, tcepi::BNJ), 0);
+    for (const auto& t : p->it_epi[k]) {
+      const int i = t.mat;
+      if (i < 0 || i >= cnt || seen[i].empty()) return bad("update tile of a matrix without this K pass", i);
+      const auto& d = p->descs[i];
+      if (t.i0 % tcepi::BM || t.i0 >= d.m || t.j0 % tcepi::BNJ || t.j0 >= d.n)
+        return bad("update tile out of range", i);
+      if (++seen[i][(t.i0 / tcepi::BM) * cdiv(d.n, tcepi::BNJ) + t.j0 / tcepi::BNJ] != 1)
+        return bad("update tile covered twice", i);
+    }
+    for (int i = 0; i < cnt; ++i)
+      for (int v : seen[i]) if (v != 1) return bad("update tile not covered", i);
+  }
+  // widths the kernels assume: rp and bn multiples of 32 (fp32 operand boxes of
+  // 16 along K, 128-byte Gram boxes), bn within the TMEM budget
+  for (int i = 0; i < cnt; ++i)
+    if (p->rp[i] % 32 || p->bn[i] % 32 || p->bn[i] > tcstream::BN_MAX || (long long)p->ncb[i] * p->bn[i] < p->rp[i])
+      return bad("rank padding or column blocks", i);
+  return std::string();
+}
+
 dion_status_t build_image(dion_plan* p, unsigned char* base) {
   const int cnt = p->count;
   p->image.assign(p->tables_bytes, 0);
@@ -815,7 +929,16 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
   }
   const MatDev* mats = tab<MatDev>(p, base, p->t_mats);
   const int cnt = p->count;
+  // one NVTX range per phase, so that timeline tools show the step's structure
+  static const char* const kPhaseNames[5] = {
+      "dion (a) P = (G + R) V", "dion (b) U = orth(P)", "dion (c) W = (G + R)^T U",
+      "dion (d) Vbar = orth(W) | colnorm(W)", "dion (e) X, R update"};
+  struct Range {
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+  };
   for (int ph = first; ph <= last; ++ph) {
+    const Range range(kPhaseNames[ph]);
     switch (ph) {
       case 0:
         if (cudaMemsetAsync(base + p->off_status, 0, 16 * (size_t)cnt, s) != cudaSuccess)
@@ -995,6 +1118,11 @@ dion_status_t dion_plan_create(const dion_matrix_desc* descs, int32_t count, siz
   p->descs.assign(descs, descs + count);
   p->count = count;
   layout(p);
+  const std::string wrong = verify_tables(p);
+  if (!wrong.empty()) {
+    delete p;
+    return fail(DION_ERR_UNSUPPORTED, "internal: work tables failed their check: %s", wrong.c_str());
+  }
   // every grouped launch must fit in one grid dimension
   const long long grids[] = {p->ts_gram_p[count], p->ts_trmm_p[count], p->ts_wred[count], p->ts_split[p->n_split]};
   for (long long g : grids)

@@ -5,6 +5,8 @@ logic; the descriptors carry fake (never dereferenced) device addresses.
 """
 import ctypes
 
+import numpy as np
+
 import pytest
 
 from rank_orthonormalized_optimizer_03_b300 import build, dion
@@ -130,3 +132,41 @@ def test_status_strings(L):
     for code, name in dion.STATUS_NAMES.items():
         assert L.dion_status_string(code).decode() == name
     assert L.dion_status_string(99).decode() == "DION_ERR_UNKNOWN"
+
+
+def plan_of(L, shapes):
+    """Create (and destroy) a plan over fake buffers: (m, n, r, variant, g_dtype)."""
+    descs = [fake_desc(k, m=m, n=n, r=r, ld_x=n, ld_g=n, ld_r=n, variant=v, g_dtype=gd)
+             for k, (m, n, r, v, gd) in enumerate(shapes)]
+    code, ws, plan = create(L, descs)
+    msg = L.dion_last_error()
+    if code == dion.DION_OK:
+        L.dion_plan_destroy(plan)
+    return code, ws, msg
+
+
+@pytest.mark.parametrize("name", ["single_256x128_r16", "square_1024_r256", "gpt160m_12L_rdiv4",
+                                  "llama3b_28L_rdiv16", "llama3b_28L_rdiv4", "sweep_8192x8192_r2048",
+                                  "sweep_4096x16384_r32", "sweep_4096x16384_r1024"])
+def test_work_tables_pass_their_check_for_every_workload(L, name):
+    # dion_plan_create checks its work tables (coverage of every launch, K
+    # ranges, 16-byte TMA x coordinates) before returning DION_OK
+    from rank_orthonormalized_optimizer_03_b300 import workloads
+    wl = workloads.by_name(name)
+    bf = dion.DTYPE_BF16 if wl.g_dtype == "bf16" else dion.DTYPE_F32
+    code, ws, msg = plan_of(L, [(s.m, s.n, s.r, k % 2, bf) for k, s in enumerate(wl.mats)])
+    assert code == dion.DION_OK, msg
+    assert ws > 0
+
+
+def test_work_tables_pass_their_check_for_odd_batches(L):
+    g = np.random.Generator(np.random.PCG64(5))
+    for trial in range(40):
+        shapes = []
+        for _ in range(int(g.integers(1, 6))):
+            m = int(g.integers(1, 700))
+            n = int(g.integers(1, 90)) * 8          # bf16 / fp32 row pitches on 16 bytes
+            r = int(g.integers(1, min(m, n) + 1))
+            shapes.append((m, n, r, int(g.integers(0, 2)), int(g.integers(0, 2))))
+        code, _, msg = plan_of(L, shapes)
+        assert code == dion.DION_OK, (shapes, msg)
