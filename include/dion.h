@@ -80,7 +80,7 @@ typedef enum { DION_VARIANT_DION = 0, DION_VARIANT_ORTH = 1 } dion_variant_t;
 typedef enum { DION_DTYPE_F32 = 0, DION_DTYPE_BF16 = 1 } dion_dtype_t;
 
 /* One weight matrix and its optimizer state (all device pointers, caller-owned).
- * Requirements: 1 <= r <= min(m, n); ld_* >= n; every pointer 16-byte aligned;
+ * Requirements: 1 <= m, n < 2^31; 1 <= r <= min(m, n); ld_* >= n; every pointer 16-byte aligned;
  * ld_x, ld_r multiples of 4 and ld_g a multiple of 16 bytes / element size. */
 typedef struct {
   float* X;          /* parameters, m x n fp32, updated in place                 */

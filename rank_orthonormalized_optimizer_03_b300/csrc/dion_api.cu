@@ -133,7 +133,7 @@ dion_status_t validate(const dion_matrix_desc* d, int count) {
     const dion_matrix_desc& x = d[i];
     if (!x.X || !x.G || !x.R || !x.V)
       return fail(DION_ERR_INVALID_ARG, "matrix %d: NULL pointer", i);
-    if (x.m < 1 || x.n < 1 || x.m > (1LL << 31) || x.n > (1LL << 31))
+    if (x.m < 1 || x.n < 1 || x.m >= (1LL << 31) || x.n >= (1LL << 31))   // rows index as int32 on the device
       return fail(DION_ERR_INVALID_ARG, "matrix %d: bad shape %lld x %lld", i, (long long)x.m, (long long)x.n);
     if (x.r < 1 || x.r > std::min(x.m, x.n))
       return fail(DION_ERR_INVALID_ARG, "matrix %d: rank %lld outside [1, min(m, n) = %lld]", i,

@@ -81,6 +81,7 @@ def test_valid_plan_and_layout(L):
     (dict(r=0), dion.DION_ERR_INVALID_ARG),
     (dict(r=33), dion.DION_ERR_INVALID_ARG),            # r > min(m, n)
     (dict(m=0), dion.DION_ERR_INVALID_ARG),
+    (dict(m=1 << 31), dion.DION_ERR_INVALID_ARG),      # rows index as int32 on the device
     (dict(ld_x=16), dion.DION_ERR_INVALID_ARG),         # ld < n
     (dict(g_dtype=7), dion.DION_ERR_INVALID_ARG),
     (dict(variant=2), dion.DION_ERR_INVALID_ARG),
