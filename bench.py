@@ -6,7 +6,7 @@
 One "step" is the whole hot path -- phases (a)-(e) of every matrix of the
 workload -- through the C ABI.  The default workload is every weight matrix
 of a 28-layer Llama-3B (196 matrices, rank = min(m, n)/16, fp32 state, bf16
-gradients), synthetic seeded inputs.  All state (36 GB) is far larger than
+gradients), synthetic seeded inputs.  The state X, G, R (28 GB) is far larger than
 L2, so no L2 flush is needed between steps.
 
 Prints ONE JSON line on rank 0.  With --gpus N > 1 (launched by torchrun)
@@ -166,6 +166,14 @@ def build_state(wl, dev, args):
     return mats
 
 
+def bench_config(wl, args, world):
+    """The workload the line is quoted on (the same for both arms)."""
+    state_gb = sum(s.m * s.n for s in wl.mats) * (8 + (2 if wl.g_dtype == "bf16" else 4)) / 1e9
+    return {"workload": wl.name, "matrices": len(wl.mats), "elements": wl.elems, "g_dtype": wl.g_dtype,
+            "variant": args.variant, "parallelism": f"replica{world}",
+            "l2": f"inputs {state_gb:.0f} GB >> 126 MB L2, no flush"}
+
+
 def run_cuda(args):
     import torch
     import torch.distributed as dist
@@ -264,9 +272,7 @@ def run_cuda(args):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "precision": "fp32 state; contractions as 3xTF32 tensor-core products with fp32 accumulation",
-        "config": {"workload": wl.name, "matrices": len(wl.mats), "elements": wl.elems,
-                   "g_dtype": wl.g_dtype, "variant": args.variant, "parallelism": f"replica{world}",
-                   "l2": "inputs 36 GB >> 126 MB L2, no flush"},
+        "config": bench_config(wl, args, world),
         "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
         "tflops": round(world * cost["step"].flops / (ms_per_step * 1e-3) / 1e12, 3),
         "step_roofline_ms": round(step_roof_ms, 3),
@@ -382,9 +388,8 @@ def run_reference(args):
     out = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 2), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": wl.name, "matrices": len(wl.mats), "g_dtype": wl.g_dtype,
-                      "variant": args.variant, "parallelism": "host"},
-           "impl": "reference",
+           "config": bench_config(wl, args, world),
+           "impl": "reference", "execution": "float64 oracle on the host cores (rank 0 only)",
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
                             "sample": sample},
            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
