@@ -11,7 +11,9 @@ recomputed from G + R in every pass instead of being stored):
 
 The alternative of storing M in pass (a) costs the same (gb + 4 + 4, then
 4, then 4 + 4 + 8 = gb + 28 ... = 30 B for bf16 G) so either schedule's
-minimum is 30 B/element for bf16 G; the factors add 4 r (3 m + 4 n) bytes.
+minimum is 30 B/element for bf16 G.  The factors add 4 r (5 m + 6 n) bytes:
+(a) reads V, writes P; orth(P) reads P, writes U; (c) reads U, writes W;
+orth(W) / colnorm reads W, writes Vbar; (e) reads U, Vbar and W.
 
 Flops per matrix: 8 m n r for the four contractions (M V, M^T U, U Vbar^T,
 U W^T), plus 2 m r^2 - 2/3 r^3 for orth(P) (Householder count), plus
