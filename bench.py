@@ -74,12 +74,11 @@ def tensor_peak_3xtf32(peaks):
 
 
 # DRAM traffic of one k_epi launch per element of X, from the ncu capture of the
-# GPT-160M case (profiles/k_epi_gpt160m_rdiv4.md: 1.867 GB for 8.49e7 elements);
-# the traffic of a launch is this times the launch's elements.  That capture
-# predates the kernel's K passes (a single pass for r <= 256, the same work), so
-# the bench reports it beside a null `traffic` until k_epi is captured again.
-EPI_TRAFFIC_BYTES_PER_ELEM = 1.867e9 / 84934656
-EPI_TRAFFIC_CURRENT = False
+# GPT-160M case (profiles/k_epi_gpt160m_rdiv4.md: 1.8646 GB for 8.49e7 elements);
+# the traffic of a launch is this times the launch's elements.  Set
+# EPI_TRAFFIC_CURRENT to False when k_epi changes, until it is captured again.
+EPI_TRAFFIC_BYTES_PER_ELEM = (1232205312 + 632418560) / 84934656
+EPI_TRAFFIC_CURRENT = True
 
 
 def variant_of(args):
@@ -261,7 +260,7 @@ def run_cuda(args):
         roof["traffic_note"] = "ncu dram bytes of the GPT-160M k_epi capture, scaled by elements"
         if not EPI_TRAFFIC_CURRENT:
             roof["traffic_earlier_revision"] = round(traffic)
-            roof["traffic_note"] += "; captured before the kernel gained K passes (same work for r <= 256)"
+            roof["traffic_note"] += "; captured on an earlier revision of the kernel"
     step_roof_ms = max(step_bytes / (peaks["hbm_gbs"] * 1e9), cost["step"].flops / (tpeak * 1e12)) * 1e3
     e2e = None
     if not args.no_e2e:
