@@ -103,9 +103,23 @@ def _stream_ptr(stream) -> Optional[int]:
     return int(getattr(stream, "cuda_stream", stream)) or None
 
 
+def _check_device(tensors, names, device=None):
+    """Every tensor a CUDA tensor on one device (the library takes device pointers)."""
+    for t, nm in zip(tensors, names):
+        if not t.is_cuda:
+            raise ValueError(f"{nm} must be a CUDA tensor (got {t.device})")
+        if device is None:
+            device = t.device
+        elif t.device != device:
+            raise ValueError(f"{nm} is on {t.device}, expected {device}")
+    return device
+
+
 def make_desc(X, G, R, V, eta, beta, variant="orth", scale=0.0) -> MatrixDesc:
     """Descriptor for one matrix from torch tensors (row-major, unit column stride)."""
     import torch
+    if X.dim() != 2:
+        raise ValueError("X must be an m x n matrix")
     m, n = X.shape
     r = V.shape[1]
     for t, nm in ((X, "X"), (G, "G"), (R, "R")):
@@ -115,8 +129,11 @@ def make_desc(X, G, R, V, eta, beta, variant="orth", scale=0.0) -> MatrixDesc:
         raise ValueError("X, R, V must be float32")
     if G.dtype not in (torch.float32, torch.bfloat16):
         raise ValueError("G must be float32 or bfloat16")
-    if V.shape != (n, r) or not V.is_contiguous():
+    if V.dim() != 2 or V.shape != (n, r) or not V.is_contiguous():
         raise ValueError("V must be a contiguous n x r tensor")
+    if variant not in VARIANT:
+        raise ValueError(f"variant must be one of {sorted(VARIANT)}")
+    _check_device((X, G, R, V), ("X", "G", "R", "V"))
     return MatrixDesc(
         X.data_ptr(), G.data_ptr(), R.data_ptr(), V.data_ptr(), m, n, r,
         X.stride(0), G.stride(0), R.stride(0),
@@ -140,6 +157,7 @@ def orth_noalloc(A, Q, stream=None, status: bool = True) -> Optional[int]:
         raise ValueError("A and Q must be rows x r matrices of the same shape")
     if A.dtype != torch.float32 or Q.dtype != torch.float32 or A.stride(1) != 1 or Q.stride(1) != 1:
         raise ValueError("A and Q must be float32 with unit column stride")
+    _check_device((A, Q), ("A", "Q"))
     rows, r = A.shape
     st = ctypes.c_uint32(0)
     check(lib().dion_orth_noalloc(A.data_ptr(), rows, r, A.stride(0), Q.data_ptr(), Q.stride(0),
@@ -159,6 +177,13 @@ class Plan:
     def __init__(self, mats: Sequence[dict], workspace=None, device=None):
         import torch
         L = lib()
+        if len(mats) == 0:
+            raise ValueError("a plan needs at least one matrix")
+        dev0 = mats[0]["X"].device
+        for k, d in enumerate(mats):
+            for key in ("X", "G", "R", "V"):
+                if d[key].device != dev0:
+                    raise ValueError(f"matrix {k}: {key} is on {d[key].device}, the plan's first X on {dev0}")
         self._keep = [(d["X"], d["G"], d["R"], d["V"]) for d in mats]
         descs = (MatrixDesc * len(mats))(*[
             make_desc(d["X"], d["G"], d["R"], d["V"], d["eta"], d["beta"], d.get("variant", "orth"),
@@ -173,8 +198,10 @@ class Plan:
         if workspace is None:
             dev = device if device is not None else mats[0]["X"].device
             workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
-        if workspace.numel() < self.ws_bytes:
+        if workspace.numel() * workspace.element_size() < self.ws_bytes:
             raise ValueError("workspace too small")
+        if workspace.device != mats[0]["X"].device:
+            raise ValueError("workspace must be on the matrices' device")
         self.workspace = workspace
 
     def close(self):
@@ -273,6 +300,10 @@ class HostFedStep:
         import torch
         if len(host_grads) != len(self.mats):
             raise ValueError("one host gradient per matrix")
+        for i, (h, d) in enumerate(zip(host_grads, self.mats)):
+            if h.shape != d["G"].shape or h.dtype != d["G"].dtype:
+                raise ValueError(f"host gradient {i}: {tuple(h.shape)} {h.dtype}, expected "
+                                 f"{tuple(d['G'].shape)} {d['G'].dtype}")
         cs = stream if stream is not None else torch.cuda.current_stream()
         for g, ((a, b), plan) in enumerate(zip(self.ranges, self.plans)):
             ready = torch.cuda.Event()
