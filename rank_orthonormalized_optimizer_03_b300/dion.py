@@ -198,7 +198,9 @@ class Plan:
         if workspace is None:
             dev = device if device is not None else mats[0]["X"].device
             workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
-        if workspace.numel() * workspace.element_size() < self.ws_bytes:
+        if workspace.dtype != torch.uint8 or workspace.dim() != 1:
+            raise ValueError("workspace must be a 1-D uint8 tensor")
+        if workspace.numel() < self.ws_bytes:
             raise ValueError("workspace too small")
         if workspace.device != mats[0]["X"].device:
             raise ValueError("workspace must be on the matrices' device")
@@ -291,6 +293,7 @@ class HostFedStep:
         self.plans = [Plan(self.mats[a:b]) for a, b in self.ranges]
         self.copy_stream = torch.cuda.Stream(device=self.mats[0]["X"].device)
         self._read = [None] * len(self.plans)   # per group: event after its last step
+        self._checked = None
 
     def h2d_bytes(self) -> int:
         return sum(d["G"].numel() * d["G"].element_size() for d in self.mats)
@@ -300,10 +303,12 @@ class HostFedStep:
         import torch
         if len(host_grads) != len(self.mats):
             raise ValueError("one host gradient per matrix")
-        for i, (h, d) in enumerate(zip(host_grads, self.mats)):
-            if h.shape != d["G"].shape or h.dtype != d["G"].dtype:
-                raise ValueError(f"host gradient {i}: {tuple(h.shape)} {h.dtype}, expected "
-                                 f"{tuple(d['G'].shape)} {d['G'].dtype}")
+        if self._checked is not host_grads:      # shapes checked once per list of gradients
+            for i, (h, d) in enumerate(zip(host_grads, self.mats)):
+                if h.shape != d["G"].shape or h.dtype != d["G"].dtype:
+                    raise ValueError(f"host gradient {i}: {tuple(h.shape)} {h.dtype}, expected "
+                                     f"{tuple(d['G'].shape)} {d['G'].dtype}")
+            self._checked = host_grads
         cs = stream if stream is not None else torch.cuda.current_stream()
         for g, ((a, b), plan) in enumerate(zip(self.ranges, self.plans)):
             ready = torch.cuda.Event()
