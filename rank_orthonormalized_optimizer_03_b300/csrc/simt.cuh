@@ -8,7 +8,7 @@
 //   k_trmm          Q = A T  (T upper triangular)        dion_orth_noalloc)
 //   k_gram_reduce   sum of the Gram partials             orth(), tensor-core path
 //   k_chol_inv      Cholesky + inverse, one CTA per job  orth(), positive diagonal, shifted pass
-//   k_wreduce       W = sum of the K-range partials      equation 3
+//   k_wreduce       W = sum of the K-range partials      equation 3 (and its tf32 halves)
 //   k_colnorm       Vbar = W diag(1/||w_j||)             Dion right factor
 #pragma once
 
