@@ -6,6 +6,6 @@ against closed forms, invariants and brute-force SVD cases in
 ``tests/test_oracle.py`` before it is trusted.
 """
 from .dion_oracle import (  # noqa: F401
-    DION, ORTH, RANK_TOL, colnorm, default_scale, householder_qr_pos, orth,
+    DION, ORTH, RANK_TOL, colnorm, default_scale, householder_qr_pos, lapack_qr_pos, orth,
     oracle_chain, oracle_step,
 )

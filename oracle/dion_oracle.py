@@ -87,10 +87,25 @@ def householder_qr_pos(A):
     return Q, Rf
 
 
-def orth(A):
+def lapack_qr_pos(A):
+    """The same thin QR with a positive diagonal, with LAPACK's QR
+    (numpy.linalg.qr, blocked Householder) as the factorisation step and the
+    same sign fix: a library routine for the same definition, for arguments
+    too large for the textbook loop above (an 8192 x 2048 argument takes
+    minutes there).  Pinned against householder_qr_pos in the tests.
+    """
+    A = np.asarray(A, dtype=np.float64)
+    if A.shape[1] > A.shape[0]:
+        raise ValueError("thin QR needs rows >= columns")
+    Q, Rf = np.linalg.qr(A, mode="reduced")
+    d = np.where(np.diag(Rf) < 0.0, -1.0, 1.0)
+    return Q * d[None, :], d[:, None] * Rf
+
+
+def orth(A, qr=householder_qr_pos):
     """orth(A) with the positive-diagonal reading; returns (Q, deficient)."""
     A = np.asarray(A, dtype=np.float64)
-    Q, Rf = householder_qr_pos(A)
+    Q, Rf = qr(A)
     scale = np.linalg.norm(A)
     deficient = bool(np.any(np.abs(np.diag(Rf)) <= RANK_TOL * scale)) if scale > 0 else True
     return Q, deficient
@@ -112,12 +127,14 @@ def default_scale(m, n):
     return float(np.sqrt(m / n))
 
 
-def oracle_step(X, G, R, V, eta, beta, variant=ORTH, scale=None):
+def oracle_step(X, G, R, V, eta, beta, variant=ORTH, scale=None, qr=householder_qr_pos):
     """One Dion / Orth-Dion step on one matrix, in float64.
 
     Inputs are widened exactly to float64 (fp32 and bf16 values are exactly
     representable).  Shapes: X, G, R are m x n; V (the warm start V_{t-1})
-    is n x r.  ``scale=None`` means s = sqrt(m/n).  Returns a dict with the
+    is n x r.  ``scale=None`` means s = sqrt(m/n); ``qr`` is the thin-QR
+    routine behind orth() (householder_qr_pos, or lapack_qr_pos for large
+    arguments).  Returns a dict with the
     new state (X, R, V) and the intermediates M, P, U, W, Vbar plus a
     ``deficient`` flag (orth() met a rank-deficient argument).
     """
@@ -135,10 +152,10 @@ def oracle_step(X, G, R, V, eta, beta, variant=ORTH, scale=None):
 
     M = G + R                                   # M_t = G_t + R_t
     P = M @ V                                   # M_t V_{t-1}
-    U, def_u = orth(P)                          # U_t = orth(M_t V_{t-1})
+    U, def_u = orth(P, qr)                      # U_t = orth(M_t V_{t-1})
     W = M.T @ U                                 # W_t = M_t^T U_t
     if variant == ORTH:
-        Vbar, def_w = orth(W)                   # Vbar_t = orth(W_t)
+        Vbar, def_w = orth(W, qr)               # Vbar_t = orth(W_t)
     elif variant == DION:
         Vbar, def_w = colnorm(W), False         # Vbar_t = colnorm(W_t)
     else:
@@ -152,11 +169,12 @@ def oracle_step(X, G, R, V, eta, beta, variant=ORTH, scale=None):
     }
 
 
-def oracle_chain(X, R, V, grads, eta, beta, variant=ORTH, scale=None):
-    """Run ``len(grads)`` chained steps in float64; returns the list of step dicts."""
+def oracle_chain(X, R, V, grads, eta, beta, variant=ORTH, scale=None, qr=householder_qr_pos):
+    """Run ``len(grads)`` chained steps in float64, each step's new X, R and V
+    (V_t = Vbar_t) feeding the next; returns the list of step dicts."""
     out = []
     for G in grads:
-        st = oracle_step(X, G, R, V, eta, beta, variant, scale)
+        st = oracle_step(X, G, R, V, eta, beta, variant, scale, qr)
         X, R, V = st["X"], st["R"], st["V"]
         out.append(st)
     return out

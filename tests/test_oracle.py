@@ -235,8 +235,10 @@ def test_exact_rank_spanning_partial_isometry():
     assert np.trace(M.T @ Pm) <= nuc + 1e-12
 
 
-def test_fixed_gradient_converges_to_top_subspace():
-    """G fixed, beta = 0: V_t follows subspace iteration on G^T G (D6)."""
+def fixed_gradient_pin(chain):
+    """G fixed, beta = 0, through a chain function: V_t follows subspace
+    iteration on G^T G (D6), converging to the top-r right singular subspace
+    at (sigma_{r+1}/sigma_r)^2 per step.  Returns the list of failures."""
     g = rng(14)
     m, n, r = 50, 30, 4
     Ua, _ = np.linalg.qr(g.standard_normal((m, n)))
@@ -247,34 +249,97 @@ def test_fixed_gradient_converges_to_top_subspace():
     X, R = np.zeros((m, n)), np.zeros((m, n))
     top = Vb[:, :r]
     rate = (svals[r] / svals[r - 1]) ** 2
-    errs = []
-    for _ in range(12):
-        out = O.oracle_step(X, G, R, V, 0.0, 0.0, O.ORTH, scale=1.0)
-        V = out["V"]
-        errs.append(np.linalg.norm(top @ top.T - V @ V.T, 2))
-    assert errs[-1] < 1e-4
+    steps = chain(X, R, V, [G] * 12, 0.0, 0.0, O.ORTH, 1.0)
+    errs = [np.linalg.norm(top @ top.T - st["V"] @ st["V"].T, 2) for st in steps]
+    bad = []
+    if not errs[-1] < 1e-4:
+        bad.append(f"no convergence: {errs[-1]:.3g}")
     # geometric decay at (sigma_{r+1}/sigma_r)^2 per step, up to a constant
     for a, b in zip(errs[3:-1], errs[4:]):
-        assert b <= a * rate * 1.05
+        if not b <= a * rate * 1.05:
+            bad.append(f"decay {b / a:.3g} > {rate:.3g}")
+            break
+    return bad
+
+
+def deflation_pin(chain):
+    """G = 0, beta = 1, through a chain function: successive U_t are mutually
+    orthogonal, the residual energy falls by ||W_t||^2 per step (D6, D3) and
+    X collects every step's -eta s U_t Vbar_t^T, which holds only if every step
+    reads the previous step's X, R and V."""
+    g = rng(15)
+    m, n, r = 40, 30, 3
+    R0 = g.standard_normal((m, n))
+    V = g.standard_normal((n, r))
+    X = np.zeros((m, n))
+    steps = chain(X, R0, V, [np.zeros((m, n))] * 4, 0.1, 1.0, O.ORTH, 1.0)
+    bad = []
+    # X carried: X_T = X_0 - eta s sum_t U_t Vbar_t^T
+    X_sum = X - 0.1 * sum(st["U"] @ st["Vbar"].T for st in steps)
+    if np.abs(steps[-1]["X"] - X_sum).max() >= 1e-12:
+        bad.append("X not accumulated across steps")
+    e_prev = np.sum(R0 ** 2)
+    for t, st in enumerate(steps):
+        e = np.sum(st["R"] ** 2)
+        if abs(e - (e_prev - np.sum(st["W"] ** 2))) >= 1e-10 * e_prev:
+            bad.append(f"energy identity fails at step {t}")
+        e_prev = e
+        for j in range(t):
+            if np.abs(st["U"].T @ steps[j]["U"]).max() >= 1e-12:
+                bad.append(f"U_{t} not orthogonal to U_{j}")
+    return bad
+
+
+def test_fixed_gradient_converges_to_top_subspace():
+    assert fixed_gradient_pin(O.oracle_chain) == []
 
 
 def test_zero_gradient_deflates():
-    """G = 0, beta = 1: successive U_t mutually orthogonal, energy falls by ||W_t||^2 (D6, D3)."""
-    g = rng(15)
-    m, n, r = 40, 30, 3
-    R = g.standard_normal((m, n))
-    V = g.standard_normal((n, r))
-    X = np.zeros((m, n))
-    Us = []
-    for _ in range(4):
-        e0 = np.sum(R ** 2)
-        out = O.oracle_step(X, np.zeros((m, n)), R, V, 0.0, 1.0, O.ORTH, scale=1.0)
-        assert abs(np.sum(out["R"] ** 2) - (e0 - np.sum(out["W"] ** 2))) < 1e-10 * e0
-        R, V = out["R"], out["V"]
-        Us.append(out["U"])
-    for i in range(4):
-        for j in range(i):
-            assert np.abs(Us[i].T @ Us[j]).max() < 1e-12
+    assert deflation_pin(O.oracle_chain) == []
+
+
+def _chain_mutant(kind):
+    """oracle_chain with one plausible slip in how the state is carried."""
+    def chain(X, R, V, grads, eta, beta, variant=O.ORTH, scale=None):
+        out = []
+        R0, V0 = R, V
+        for G in grads:
+            st = O.oracle_step(X, G, R, V, eta, beta, variant, scale)
+            X = X if kind == "X_not_carried" else st["X"]
+            R = R0 if kind == "R_not_carried" else st["R"]
+            V = {"V_not_carried": V0, "V_from_P": st["P"][: V0.shape[0]]}.get(kind, st["V"])
+            out.append(st)
+        return out
+    return chain
+
+
+# (Carrying W instead of Vbar = orth(W) is not among them: orth(M W) = orth(M orth(W))
+# because W's triangular factor has a positive diagonal, so that chain is the same
+# computation for Orth-Dion, not a slip.)
+CHAIN_MUTANTS = ["X_not_carried", "R_not_carried", "V_not_carried", "V_from_P"]
+
+
+@pytest.mark.parametrize("kind", CHAIN_MUTANTS)
+def test_planted_chain_mistakes_are_caught(kind):
+    """A chain that drops or mis-carries R or V fails one of the chain pins."""
+    mutant = _chain_mutant(kind)
+    assert fixed_gradient_pin(mutant) or deflation_pin(mutant), kind
+
+
+def test_lapack_qr_equals_householder():
+    """The library-routine QR (used for the largest parity cases) and the
+    textbook Householder QR compute the same positive-diagonal factors."""
+    g = rng(23)
+    for shape in [(300, 40), (97, 97), (512, 3)]:
+        A = g.standard_normal(shape)
+        Qh, Rh = O.householder_qr_pos(A)
+        Ql, Rl = O.lapack_qr_pos(A)
+        assert np.abs(Qh - Ql).max() < 1e-11 and np.abs(Rh - Rl).max() < 1e-10
+    X, G, R, V = random_state(60, 40, 6, seed=24)
+    a = O.oracle_step(X, G, R, V, 0.01, 0.9, O.ORTH)
+    b = O.oracle_step(X, G, R, V, 0.01, 0.9, O.ORTH, qr=O.lapack_qr_pos)
+    for k in ("X", "R", "V", "U", "W"):
+        assert np.abs(a[k] - b[k]).max() < 1e-11, k
 
 
 def test_variants_share_U_R_W_trajectory():
