@@ -1,6 +1,8 @@
 """Benchmark of the batched Dion / Orth-Dion optimizer step on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--variant orth|dion|mixed]
+    python bench.py --configs all|models|sweep  # one line per workload configuration, then the
+                                                # memory -> compute crossover of the rank sweep
     python bench.py --impl reference ...      # the float64 CPU oracle, timed on host cores
 
 One "step" is the whole hot path -- phases (a)-(e) of every matrix of the
@@ -35,8 +37,10 @@ PHASES = "abcde"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--configs", default=None, choices=["all", "models", "sweep"],
+                    help="measure every configuration (one JSON line each) instead of the headline")
     ap.add_argument("--workload", default="llama3b_28L_rdiv16")
     ap.add_argument("--variant", default="orth", choices=["orth", "dion", "mixed"])
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
@@ -61,22 +65,50 @@ def load_peaks():
                 "source": "fallback"}
 
 
-# The contractions run as 3xTF32 on the tensor core (three tf32 products per
-# fp32-accurate product).  Their peak, in algorithmic (fp32-equivalent) flops,
-# is the dense tf32 rate / 3, and the tf32 rate is the measured bf16 rate times
-# the nominal tf32 / bf16 ratio 1.1 / 2.25.  The sustained bf16 figure applies:
-# the kernels are timed inside a step that runs for a large fraction of a second.
-TF32_PER_BF16 = 1.1 / 2.25
+NOMINAL_HBM_GBS = 8000.0        # the spec-sheet figure, reported beside the measured copy rate
+TF32_PER_BF16 = 1.1 / 2.25      # nominal dense tf32 / bf16 ratio (context only)
 
 
-def tensor_peak_3xtf32(peaks):
-    return peaks["bf16_tflops_sustained"] * TF32_PER_BF16 / 3.0
+def measure_tf32_tflops(dev, size=8192, reps=10):
+    """Dense TF32 tensor-core throughput on this GPU: cuBLAS fp32 matmul with
+    TF32 enabled, size^3, best of ``reps`` (a burst, like the bf16 peak it sits
+    beside).  The contractions here are 3xTF32 (three tf32 products per
+    fp32-accurate product), so their peak in fp32-equivalent flops is this / 3."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn(size, size, device=dev)
+        b = torch.randn(size, size, device=dev)
+        c = torch.empty(size, size, device=dev)
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b, c
+        return 2.0 * size ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def tensor_peak(peaks):
+    """3xTF32 peak in fp32-equivalent TFLOP/s and where it comes from."""
+    if peaks.get("tf32_tflops"):
+        return peaks["tf32_tflops"] / 3.0, "measured here: cuBLAS TF32 8192^3 burst / 3 (3xTF32)"
+    return peaks["bf16_tflops"] * TF32_PER_BF16 / 3.0, \
+        peaks["source"] + " bf16 burst x 1.1/2.25 (tf32) / 3 (3xTF32)"
 
 
 # DRAM traffic of one k_epi launch per element of X, from the ncu capture of the
-# GPT-160M case (profiles/k_epi_gpt160m_rdiv4.md: 1.8646 GB for 8.49e7 elements);
-# the traffic of a launch is this times the launch's elements.  Set
-# EPI_TRAFFIC_CURRENT to False when k_epi changes, until it is captured again.
+# GPT-160M case (1.8646 GB for 8.49e7 elements); the traffic of a launch is this
+# times the launch's elements.  Set EPI_TRAFFIC_CURRENT to False when k_epi
+# changes, until it is captured again.
 EPI_TRAFFIC_BYTES_PER_ELEM = (1232205312 + 632418560) / 84934656
 EPI_TRAFFIC_CURRENT = True
 
@@ -99,6 +131,7 @@ class ClockSampler:
 
     def _run(self):
         while not self._stop.is_set():
+            t0 = time.perf_counter()
             try:
                 out = subprocess.run(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                                       "--format=csv,noheader,nounits"], capture_output=True, text=True,
@@ -107,7 +140,7 @@ class ClockSampler:
                     self.rows.append([x.strip() for x in out.split(",")])
             except Exception:
                 pass
-            self._stop.wait(0.2)
+            self._stop.wait(max(0.0, 0.1 - (time.perf_counter() - t0)))
 
     def __enter__(self):
         self._t = threading.Thread(target=self._run, daemon=True)
@@ -149,10 +182,9 @@ def job_throughput_gbs(step_bytes: float, ms_per_step: float, world: int) -> flo
 
 
 # ----------------------------------------------------------------------------- CUDA arm
-def build_state(wl, dev, args):
+def build_state(wl, dev, args, variant):
     import torch
     from rank_orthonormalized_optimizer_03_b300 import synth
-    vof = variant_of(args)
     mats = []
     for k, spec in enumerate(wl.mats):
         X0, V0_raw, G = synth.device_matrix_inputs(spec, wl, k, seed=args.seed, device=dev)
@@ -160,23 +192,134 @@ def build_state(wl, dev, args):
         # orthonormalises through orth(M V) itself.
         V0 = (V0_raw / math.sqrt(spec.n)).contiguous()
         mats.append(dict(X=X0, G=G, R=torch.zeros_like(X0), V=V0, eta=spec.eta, beta=spec.beta,
-                         variant=vof(k), scale=spec.scale))
+                         variant=variant(k), scale=spec.scale))
     torch.cuda.synchronize()
     return mats
 
 
-def bench_config(wl, args, world):
+def bench_config(wl, variant_name, world):
     """The workload the line is quoted on (the same for both arms)."""
     state_gb = sum(s.m * s.n for s in wl.mats) * (8 + (2 if wl.g_dtype == "bf16" else 4)) / 1e9
+    ranks = sorted({s.r for s in wl.mats})
     return {"workload": wl.name, "matrices": len(wl.mats), "elements": wl.elems, "g_dtype": wl.g_dtype,
-            "variant": args.variant, "parallelism": f"replica{world}",
-            "l2": f"inputs {state_gb:.0f} GB >> 126 MB L2, no flush"}
+            "ranks": ranks, "variant": variant_name, "parallelism": f"replica{world}",
+            "l2": f"inputs {state_gb:.2f} GB >> 126 MB L2, no flush"}
+
+
+def roofline_entry(bound, achieved, peak, unit, source):
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
+            "frac": round(achieved / peak, 4), "peak_source": source}
+
+
+def measure(wl, args, dev, world, variant_name, peaks, min_timed_s=1.0):
+    """Time K steps of one workload through the C ABI (CUDA events on the launching
+    stream, phase boundaries marked by events) and build its JSON fields."""
+    import torch
+    import torch.distributed as dist
+    from rank_orthonormalized_optimizer_03_b300 import accounting, dion
+
+    vof = (lambda i: ("orth", "dion")[i % 2]) if variant_name == "mixed" else (lambda i: variant_name)
+    mats = build_state(wl, dev, args, vof)
+    plan = dion.Plan(mats)
+    stream = torch.cuda.current_stream()
+    cost = accounting.step_cost(wl.mats, wl.g_dtype, vof)
+    plan.upload()
+    t0 = time.perf_counter()
+    for _ in range(args.warmup):
+        plan.step()
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - t0) / max(1, args.warmup)
+    steps = args.steps
+    if min_timed_s and est * steps < min_timed_s:
+        steps = min(2000, int(math.ceil(min_timed_s / max(est, 1e-5))))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(steps):
+            ev[s][0].record(stream)
+            for ph in range(5):
+                plan.phases(ph, ph)
+                ev[s][ph + 1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    phase_ms = {PHASES[p]: statistics.mean(ev[s][p].elapsed_time(ev[s][p + 1]) for s in range(steps))
+                for p in range(5)}
+    ms_per_step = total_ms / steps
+    status = plan.status()
+    bad = sum(1 for v in status if v & dion.FATAL)
+    shifted = sum(1 for v in status if v & dion.DION_MAT_SHIFTED)
+
+    step = cost["step"]
+    value = job_throughput_gbs(step.bytes, ms_per_step, world)
+    tpeak, tsrc = tensor_peak(peaks)
+    hbm = peaks["hbm_gbs"]
+    hsrc = peaks["source"] + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+
+    # the whole step against max(algorithmic bytes / HBM, algorithmic flops / 3xTF32 peak)
+    t_mem = step.bytes / (hbm * 1e9) * 1e3
+    t_ten = step.flops / (tpeak * 1e12) * 1e3
+    step_roof = {"bound": "hbm" if t_mem >= t_ten else "tensor", "ideal_ms": round(max(t_mem, t_ten), 4),
+                 "hbm_ms": round(t_mem, 4), "tensor_ms": round(t_ten, 4),
+                 "frac": round(max(t_mem, t_ten) / ms_per_step, 4),
+                 "frac_vs_nominal_8tbs": round(max(step.bytes / (NOMINAL_HBM_GBS * 1e9) * 1e3, t_ten) / ms_per_step, 4),
+                 "algorithmic_bytes": step.bytes, "algorithmic_flops": step.flops,
+                 "impl_extra_bytes": round(cost["impl_extra_bytes"])}
+
+    # the dominant phase's kernel against its own schedule's bytes and flops
+    dom = max(phase_ms, key=phase_ms.get)
+    dom_kernel = {"a": "k_stream<0> (P = M V)", "b": "orth(P) chain", "c": "k_stream<1> (W = M^T U)",
+                  "d": "orth(W) chain", "e": "k_epi"}[dom]
+    c = cost[dom]
+    secs = phase_ms[dom] * 1e-3
+    gbs, tfl = c.bytes / secs / 1e9, c.flops / secs / 1e12
+    hbm_roof = roofline_entry("hbm", gbs, hbm, "GB/s", hsrc)
+    hbm_roof["frac_vs_nominal_8tbs"] = round(gbs / NOMINAL_HBM_GBS, 4)
+    ten_roof = roofline_entry("tensor", tfl, tpeak, "TFLOP/s", tsrc)
+    if c.bytes / (hbm * 1e9) >= c.flops / (tpeak * 1e12):
+        roof, other = hbm_roof, ten_roof
+    else:
+        roof, other = ten_roof, hbm_roof
+    traffic = EPI_TRAFFIC_BYTES_PER_ELEM * wl.elems if dom == "e" and EPI_TRAFFIC_CURRENT else None
+    roof.update({"traffic": round(traffic) if traffic else None, "kernel": dom_kernel, "phase": dom,
+                 "per_launch_ms": round(phase_ms[dom], 4),
+                 "algorithmic_per_launch": {"bytes": c.bytes, "flops": c.flops}, "other_roofline": other})
+    if traffic:
+        roof["traffic_note"] = "ncu dram bytes of the GPT-160M k_epi capture, scaled by elements"
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "precision": "fp32 state; contractions as 3xTF32 tensor-core products with fp32 accumulation",
+        "config": bench_config(wl, variant_name, world),
+        "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
+        "tflops": round(world * step.flops / (ms_per_step * 1e-3) / 1e12, 3),
+        "step_roofline": step_roof,
+        "roofline": roof,
+        "peaks": {"hbm_gbs": hbm, "tensor_3xtf32_tflops": round(tpeak, 1),
+                  "tf32_tflops_measured": round(peaks["tf32_tflops"], 1) if peaks.get("tf32_tflops") else None,
+                  "bf16_tflops_burst": peaks["bf16_tflops"]},
+        "clocks": clk.summary(),
+        "gpu_launches": plan.launches_per_step * steps,
+        "status_failed": bad, "status_shifted": shifted,
+    }
+    return out, plan, mats, cost
 
 
 def run_cuda(args):
     import torch
     import torch.distributed as dist
-    from rank_orthonormalized_optimizer_03_b300 import accounting, build, dion, workloads
+    from rank_orthonormalized_optimizer_03_b300 import build, workloads
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -186,133 +329,134 @@ def run_cuda(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build.build()
-    wl = workloads.by_name(args.workload)
-    mats = build_state(wl, dev, args)
-    plan = dion.Plan(mats)
-    stream = torch.cuda.current_stream()
-    cost = accounting.step_cost(wl.mats, wl.g_dtype, variant_of(args))
-    plan.upload()
-    for _ in range(args.warmup):
-        plan.step()
-    torch.cuda.synchronize()
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    # ---- timed region: K steps, phase boundaries marked with events on the launching stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-    barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for s in range(args.steps):
-            ev[s][0].record(stream)
-            for ph in range(5):
-                plan.phases(ph, ph)
-                ev[s][ph + 1].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    phase_ms = {PHASES[p]: statistics.mean(ev[s][p].elapsed_time(ev[s][p + 1]) for s in range(args.steps))
-                for p in range(5)}
-    total_ms = max_over_ranks(total_ms, world, dev)
-    ms_per_step = total_ms / args.steps
-    from rank_orthonormalized_optimizer_03_b300.dion import DION_MAT_SHIFTED, FATAL
-    status = plan.status()
-    bad = sum(1 for v in status if v & FATAL)
-    shifted = sum(1 for v in status if v & DION_MAT_SHIFTED)
-
-    step_bytes = cost["step"].bytes
-    value = job_throughput_gbs(step_bytes, ms_per_step, world)
-
     peaks = load_peaks()
-    # dominant phase: the one with the largest share of the step
-    dom = max(phase_ms, key=phase_ms.get)
-    dom_kernel = {"a": "k_stream<0> (P = M V)", "b": "orth(P) chain", "c": "k_stream<1> (W = M^T U)",
-                  "d": "orth(W) chain", "e": "k_epi"}[dom]
-    c = cost[dom]
-    secs = phase_ms[dom] * 1e-3
-    gbs = c.bytes / secs / 1e9
-    tfl = c.flops / secs / 1e12
-    tpeak = tensor_peak_3xtf32(peaks)
-    hbm_frac = gbs / peaks["hbm_gbs"]
-    ten_frac = tfl / tpeak
-    hbm_roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(hbm_frac, 4),
-                "peak_source": peaks["source"] + " copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
-    ten_roof = {"bound": "tensor", "achieved": round(tfl, 2), "peak": round(tpeak, 1), "unit": "TFLOP/s",
-                "frac": round(ten_frac, 4),
-                "peak_source": peaks["source"] + " sustained bf16 x 1.1/2.25 (tf32) / 3 (3xTF32)"}
-    # the binding roofline is the one whose ideal time is longer
-    if c.bytes / (peaks["hbm_gbs"] * 1e9) >= c.flops / (tpeak * 1e12):
-        roof, other = hbm_roof, ten_roof
+    peaks["tf32_tflops"] = measure_tf32_tflops(dev)
+    if args.configs:
+        run_configs(args, dev, world, rank, peaks)
     else:
-        roof, other = ten_roof, hbm_roof
-    traffic = EPI_TRAFFIC_BYTES_PER_ELEM * wl.elems if dom == "e" else None
-    roof.update({"traffic": round(traffic) if traffic and EPI_TRAFFIC_CURRENT else None, "kernel": dom_kernel,
-                 "phase": dom, "per_launch_ms": round(phase_ms[dom], 4),
-                 "algorithmic_per_launch": {"bytes": c.bytes, "flops": c.flops}, "other_roofline": other})
-    if traffic:
-        roof["traffic_note"] = "ncu dram bytes of the GPT-160M k_epi capture, scaled by elements"
-        if not EPI_TRAFFIC_CURRENT:
-            roof["traffic_earlier_revision"] = round(traffic)
-            roof["traffic_note"] += "; captured on an earlier revision of the kernel"
-    step_roof_ms = max(step_bytes / (peaks["hbm_gbs"] * 1e9), cost["step"].flops / (tpeak * 1e12)) * 1e3
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(args, plan, mats, stream, step_bytes, world)
-
-    out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "precision": "fp32 state; contractions as 3xTF32 tensor-core products with fp32 accumulation",
-        "config": bench_config(wl, args, world),
-        "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
-        "tflops": round(world * cost["step"].flops / (ms_per_step * 1e-3) / 1e12, 3),
-        "step_roofline_ms": round(step_roof_ms, 3),
-        "step_roofline_frac": round(step_roof_ms / ms_per_step, 4),
-        "roofline": roof,
-        "clocks": clk.summary(),
-        "gpu_launches": plan.launches_per_step * args.steps,
-        "status_failed": bad, "status_shifted": shifted,
-        "e2e": e2e,
-    }
-    if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(wl, args, args.cpu_seconds)
-    if rank == 0:
-        print(json.dumps(out), flush=True)
+        wl = workloads.by_name(args.workload)
+        out, plan, mats, cost = measure(wl, args, dev, world, args.variant, peaks, min_timed_s=0)
+        if not args.no_e2e:
+            out["e2e"] = run_e2e(args, mats, cost["step"].bytes, out["ms_per_step"], world)
+        if rank == 0 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(wl, args, args.cpu_seconds)
+        plan.close()
+        if rank == 0:
+            print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def run_e2e(args, plan, mats, stream, step_bytes, world):
+def config_list(which):
+    from rank_orthonormalized_optimizer_03_b300 import workloads
+    out = []
+    if which in ("all", "models"):
+        for name in ("gpt160m_12L_rdiv4", "llama3b_28L_rdiv16", "llama3b_28L_rdiv4"):
+            for v in ("orth", "dion"):
+                out.append((workloads.by_name(name), v))
+    if which in ("all", "sweep"):
+        for shape in workloads.SWEEP_SHAPES:
+            for r in workloads.SWEEP_RANKS:
+                for v in ("orth", "dion"):
+                    out.append((workloads.sweep(shape, r), v))
+    return out
+
+
+def crossover(lines):
+    """Memory -> compute crossover of the rank sweep, per shape and variant: the
+    first rank whose ideal tensor time exceeds its ideal HBM time (from the byte
+    and flop counts), and the first rank whose measured step takes 1.25x the
+    r = 32 step (where the measured time starts to follow the flops)."""
+    out = []
+    groups = {}
+    for ln in lines:
+        wl = ln["config"]["workload"]
+        if not wl.startswith("sweep_"):
+            continue
+        shape = wl[len("sweep_"):].split("_r")[0]
+        groups.setdefault((shape, ln["config"]["variant"]), []).append(ln)
+    for (shape, v), lst in sorted(groups.items()):
+        lst.sort(key=lambda x: x["config"]["ranks"][0])
+        ranks = [x["config"]["ranks"][0] for x in lst]
+        model = next((r for r, x in zip(ranks, lst) if x["step_roofline"]["bound"] == "tensor"), None)
+        base = lst[0]["ms_per_step"]
+        meas = next((r for r, x in zip(ranks, lst) if x["ms_per_step"] > 1.25 * base), None)
+        out.append({"shape": shape, "variant": v, "crossover_rank_model": model, "crossover_rank_measured": meas,
+                    "ms_per_step": {r: x["ms_per_step"] for r, x in zip(ranks, lst)},
+                    "step_roofline_frac": {r: x["step_roofline"]["frac"] for r, x in zip(ranks, lst)}})
+    return out
+
+
+def run_configs(args, dev, world, rank, peaks):
+    """One JSON line per configuration (GPT-160M, Llama-3B at rank min/16 and min/4,
+    the rank sweep; both variants), then one line with the sweep's crossover."""
+    import torch
+    lines = []
+    for wl, v in config_list(args.configs):
+        out, plan, mats, _ = measure(wl, args, dev, world, v, peaks, min_timed_s=1.0)
+        plan.close()
+        del plan, mats
+        torch.cuda.empty_cache()
+        lines.append(out)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+    if rank == 0 and any(x["config"]["workload"].startswith("sweep_") for x in lines):
+        print(json.dumps({"sweep_crossover": crossover(lines)}), flush=True)
+
+
+def h2d_probe_gbs(dev, nbytes=1 << 30, reps=3):
+    """Plain pinned host -> device copy rate of this machine: one transfer of
+    ``nbytes``, best of ``reps`` (CUDA events)."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    best = float("inf")
+    for _ in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d.copy_(h, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del h, d
+    return nbytes / (best * 1e-3) / 1e9
+
+
+def run_e2e(args, mats, step_bytes, device_ms, world):
     """The same step through the public API with host-resident gradients:
-    dion.HostFedStep copies every step's gradients from pinned host memory, in
-    groups whose copy overlaps the previous group's step, and the per-matrix
-    status words are read back (which synchronises)."""
+    dion.HostFedStep copies every step's gradients from pinned host memory (one
+    transfer per group of matrices, each overlapping the previous group's step),
+    and the per-matrix status words are read back (which synchronises).  The
+    state (X, R, V) and the gradients are the workload's."""
+    import torch
     from rank_orthonormalized_optimizer_03_b300 import dion
-    host_g = [d["G"].to("cpu").pin_memory() for d in mats]
     stepper = dion.HostFedStep(mats, groups=args.e2e_groups)
+    for i, d in enumerate(stepper.mats):
+        stepper.host_grad(i).copy_(d["G"].cpu())
     h2d = stepper.h2d_bytes()
     d2h = 4 * len(mats)
-    steps = max(1, min(args.steps, 5))
-    stepper.step(host_g)
+    steps = max(2, min(args.steps, 10))
+    stepper.step()
     stepper.status()
     t0 = time.perf_counter()
     for _ in range(steps):
-        stepper.step(host_g)
+        stepper.step()
         stepper.status()        # device -> host read of the step's result
     dt = (time.perf_counter() - t0) / steps
     groups = len(stepper.plans)
     stepper.close()
+    del stepper
+    torch.cuda.empty_cache()
+    link = h2d_probe_gbs(mats[0]["X"].device)
+    link_ms = h2d / (link * 1e9) * 1e3
     return {"value": round(world * step_bytes / dt / 1e9, 2), "unit": "GB/s", "ms_per_step": round(dt * 1e3, 3),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "api": f"HostFedStep, {groups} groups (copy of group g+1 overlaps the step of group g)"}
+            "api": f"HostFedStep, {groups} groups, one pinned-slab transfer per group "
+                   "(the copy of group g+1 overlaps the step of group g)",
+            "h2d_probe_gbs": round(link, 2), "h2d_link_ms": round(link_ms, 3),
+            "bound_ms": round(max(device_ms, link_ms), 3),
+            "frac_of_bound": round(max(device_ms, link_ms) / (dt * 1e3), 4),
+            "result": "per-matrix status words (the optimizer state stays on the device)"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -345,7 +489,7 @@ def oracle_time(wl, args, idxs):
         t0 = time.perf_counter()
         O.oracle_step(X, G, R, V, spec.eta, spec.beta, vof(i), spec.scale)
         secs += time.perf_counter() - t0
-        nbytes += sum(c.bytes for c in accounting.phase_cost(spec.m, spec.n, spec.r, wl.g_dtype, vof(i)).values())
+        nbytes += accounting.step_algorithmic(spec.m, spec.n, spec.r, wl.g_dtype, vof(i)).bytes
         names.append(spec.name)
     return secs, nbytes, names
 
@@ -365,29 +509,42 @@ def cpu_baseline(wl, args, budget_s):
 
 
 def run_reference(args):
+    """The float64 oracle on the host cores, on this arm's workload and metric.
+    Each step is a bounded sample of the workload: matrices in workload order
+    (rotating) until the step's share of a ~150 s budget is spent, at least one
+    matrix; value = the sample's algorithmic bytes / oracle time."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     from rank_orthonormalized_optimizer_03_b300 import workloads
     wl = workloads.by_name(args.workload)
-    # each step: one matrix group (a layer's worth, 7 matrices or the whole workload if smaller)
-    group = min(7, len(wl.mats))
-    groups = [list(range(k, min(k + group, len(wl.mats)))) for k in range(0, len(wl.mats), group)]
-    for w in range(args.warmup):
-        oracle_time(wl, args, groups[w % len(groups)][:1])
-    secs, nbytes = 0.0, 0.0
-    for s in range(args.steps):
-        t, b, _ = oracle_time(wl, args, groups[s % len(groups)])
-        secs += t
-        nbytes += b
+    per_step = 150.0 / max(1, args.steps + args.warmup)
+    nxt = 0
+
+    def one_step():
+        nonlocal nxt
+        t_all, b_all, count = 0.0, 0.0, 0
+        while count == 0 or t_all < per_step:
+            t, b, _ = oracle_time(wl, args, [nxt])
+            t_all, b_all, count = t_all + t, b_all + b, count + 1
+            nxt = (nxt + 1) % len(wl.mats)
+        return t_all, b_all, count
+
+    for _ in range(args.warmup):
+        one_step()
+    secs, nbytes, nmat = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        t, b, c = one_step()
+        secs, nbytes, nmat = secs + t, nbytes + b, nmat + c
     value = nbytes / secs / 1e9
-    sample = (f"each step: one group of {group} matrices of {wl.name} (rotating), oracle_step once each; "
+    sample = (f"{nmat} matrix steps of {wl.name} over {args.steps} steps (workload order, rotating; "
+              f"~{per_step:.1f} s of oracle time per step), oracle_step once each; "
               f"value = algorithmic bytes of the sample / oracle time")
     out = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 2), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": bench_config(wl, args, world),
+           "config": bench_config(wl, args.variant, world),
            "impl": "reference", "execution": "float64 oracle on the host cores (rank 0 only)",
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
                             "sample": sample},

@@ -200,21 +200,24 @@ DION_API int32_t dion_plan_launches_per_step(const dion_plan* plan);
  *   Q  rows x r fp32 row-major device array (ldq >= r), written; may not overlap A
  *   1 <= r <= min(rows, DION_NOALLOC_MAX_RANK), rows <= DION_NOALLOC_MAX_ROWS
  *
- * Returns DION_ERR_UNSUPPORTED for sizes beyond those limits (nothing is
- * launched), DION_ERR_INVALID_ARG for NULL pointers or bad leading
- * dimensions, DION_ERR_CUDA if a launch fails.  The work is enqueued on
- * `stream`; with status != NULL the call then copies the matrix's status word
- * (DION_MAT_* bits; Q is valid when no bit other than DION_MAT_SHIFTED is set)
- * to *status and synchronises the stream, with status == NULL it returns
- * without waiting.
+ * Returns DION_ERR_UNSUPPORTED for sizes beyond those limits or a device
+ * index of 64 or more (nothing is launched), DION_ERR_INVALID_ARG for NULL
+ * pointers or bad leading dimensions, DION_ERR_CUDA if a launch fails.  The
+ * work is enqueued on `stream`; with status != NULL the call then copies the
+ * matrix's status word (DION_MAT_* bits; Q is valid when no bit other than
+ * DION_MAT_SHIFTED is set) to *status and synchronises the stream, with
+ * status == NULL it returns without waiting.  Pass status == NULL while the
+ * stream is being captured: the copy to pageable host memory and the
+ * synchronisation are not allowed inside a capture.
  *
  * Every call shares the one scratch array and overwrites it (the status word
  * is cleared by each call).  Calls whose work overlaps on the GPU (different
  * streams, different host threads) race on it: order them on one stream.  The
  * first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before starting any
- * stream capture.  The call allocates nothing: no cudaMalloc, no cudaFree, no
- * allocating library routine.
+ * stream capture.  That address is cached and not looked up again after a
+ * cudaDeviceReset().  The call allocates nothing: no cudaMalloc, no cudaFree,
+ * no allocating library routine.
  */
 #define DION_NOALLOC_MAX_ROWS 8192
 #define DION_NOALLOC_MAX_RANK 64

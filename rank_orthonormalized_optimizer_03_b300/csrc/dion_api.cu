@@ -4,6 +4,7 @@
 #include "dion.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -62,6 +63,7 @@ constexpr size_t kSFloats = (size_t)kRankMax * kRankMax + kRankMax + 32 * kRankM
 constexpr size_t kTFloats = (size_t)kRankMax * kRankMax;
 constexpr size_t kQFloats = (size_t)kRowsMax * kRankMax;
 constexpr size_t kBytes = kJobBytes + 4 * (kGpartFloats + kSFloats + kTFloats + 2 * kQFloats);
+constexpr int kMaxDevices = 64;                                // per-device address cache
 }  // namespace noalloc
 static __device__ __align__(256) unsigned char g_noalloc_scratch[noalloc::kBytes];
 
@@ -1034,17 +1036,23 @@ dion_status_t orth_noalloc_impl(const float* A, long long rows, long long r, lon
   if (rows > noalloc::kRowsMax || r > noalloc::kRankMax)
     return fail(DION_ERR_UNSUPPORTED, "%lld x %lld exceeds the fixed scratch (rows <= %d, r <= %d)", rows, r,
                 DION_NOALLOC_MAX_ROWS, DION_NOALLOC_MAX_RANK);
-  // device address of the scratch, looked up once per device with that device current
-  static void* dev_ptr[64] = {};
+  // Device address of the scratch, looked up once per device with that device
+  // current.  Host threads may race on a first call: each entry is an atomic, and a
+  // second lookup of the same device stores the same address.  The cache is not
+  // refreshed after cudaDeviceReset().
+  static std::atomic<void*> dev_ptr[noalloc::kMaxDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cuda_check("device query");
-  if (!dev_ptr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_check("device query");
+  if (dev < 0 || dev >= noalloc::kMaxDevices)
+    return fail(DION_ERR_UNSUPPORTED, "device %d: the scratch address cache covers devices 0..%d", dev,
+                noalloc::kMaxDevices - 1);
+  void* cached = dev_ptr[dev].load(std::memory_order_acquire);
+  if (!cached) {
+    if (cudaGetSymbolAddress(&cached, g_noalloc_scratch) != cudaSuccess || !cached)
       return cuda_check("scratch address lookup");
-    dev_ptr[dev] = ptr;
+    dev_ptr[dev].store(cached, std::memory_order_release);
   }
-  unsigned char* base = static_cast<unsigned char*>(dev_ptr[dev]);
+  unsigned char* base = static_cast<unsigned char*>(cached);
   const long long rp = cdiv(r, kRankGranule) * kRankGranule;
   long long nch = std::min<long long>(noalloc::kChunksMax, std::max<long long>(1, cdiv(rows, 512)));
   const long long chunk = cdiv(cdiv(rows, nch), 64) * 64;

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(NT) k_gram(const OrthJob* __restrict__ jobs,
 // kappa(A) well below u^{-1/2} ~ 4e3; when the unshifted factorisation breaks
 // down or its pivots imply kappa(A) > ~1e3 (min pivot^2 < 1e-6 max diagonal),
 // the Gram is rebuilt with the shift s = 11 (rows r + r (r + 1)) u ||A||_F^2 of
-// shifted CholeskyQR (Fukaya, Kannan, Nakatsukasa, Zhang, Yamamoto 2020) and
+// shifted CholeskyQR (Fukaya, Kannan, Nakatsukasa, Yamamoto, Yanagisawa 2020) and
 // the job is flagged for a third pass.  Every factor stays upper triangular
 // with a positive diagonal, so the final Q is still the unique thin-QR factor.
 // A failure in pass 1 or 2 (or of the shifted pass) marks the matrix and

@@ -150,7 +150,9 @@ def orth_noalloc(A, Q, stream=None, status: bool = True) -> Optional[int]:
 
     A and Q are float32 CUDA tensors (rows x r views with unit column stride).
     With status=True the call waits for the result and returns the matrix's
-    status word; otherwise it returns None without waiting.
+    status word; otherwise it returns None without waiting.  Inside a stream
+    capture pass status=False (the status copy and the wait are not allowed
+    there).
     """
     import torch
     if A.dim() != 2 or Q.dim() != 2 or A.shape != Q.shape:
@@ -158,6 +160,8 @@ def orth_noalloc(A, Q, stream=None, status: bool = True) -> Optional[int]:
     if A.dtype != torch.float32 or Q.dtype != torch.float32 or A.stride(1) != 1 or Q.stride(1) != 1:
         raise ValueError("A and Q must be float32 with unit column stride")
     _check_device((A, Q), ("A", "Q"))
+    if status and torch.cuda.is_current_stream_capturing():
+        raise RuntimeError("orth_noalloc: pass status=False while the stream is being captured")
     rows, r = A.shape
     st = ctypes.c_uint32(0)
     check(lib().dion_orth_noalloc(A.data_ptr(), rows, r, A.stride(0), Q.data_ptr(), Q.stride(0),
@@ -273,50 +277,69 @@ def group_bounds(nbytes: Sequence[int], groups: int) -> List[tuple]:
 
 
 class HostFedStep:
-    """Steps of a batch whose gradients arrive from (pinned) host memory.
+    """Steps of a batch whose gradients arrive from pinned host memory.
 
     The matrices are split into ``groups`` consecutive groups of about equal
-    gradient bytes, each with its own :class:`Plan`.  Every step copies group
-    g's gradients host -> device on a side stream and steps group g on the
-    caller's stream once they are in, so the copy of group g + 1 overlaps the
-    step of group g.  A group's copy waits until the previous step of that group
-    has read its gradients.  Each matrix gets the arithmetic of a plan over the
-    whole batch whenever each group still fills the GPU (the K split of W = M^T U
-    is the only choice that depends on the batch).
+    gradient bytes, each with its own :class:`Plan`.  A group's gradients lie
+    back to back (256-byte aligned) in one device slab and in one pinned host
+    slab of the same layout: the caller writes matrix i's gradient into
+    :meth:`host_grad` (i), and every step copies each group's host slab to its
+    device slab in one transfer on a side stream, then steps the group on the
+    caller's stream once the copy is in, so that the copy of group g + 1
+    overlaps the step of group g.  A group's copy waits until the previous step
+    of that group has read its gradients.  Matrix i's ``G`` in ``self.mats``
+    is its view of the device slab (the caller's original G is copied in once
+    and no longer read).  Each matrix gets the arithmetic of a plan over the
+    whole batch whenever each group still fills the GPU (the K split of
+    W = M^T U is the only choice that depends on the batch).
     """
+
+    ALIGN = 256
 
     def __init__(self, mats: Sequence[dict], groups: int = 8):
         import torch
-        self.mats = list(mats)
+        self.mats = [dict(d) for d in mats]
         sizes = [d["G"].numel() * d["G"].element_size() for d in self.mats]
         self.ranges = group_bounds(sizes, groups)
+        dev = self.mats[0]["X"].device
+        self.dev_slabs, self.host_slabs, self._host_views = [], [], [None] * len(self.mats)
+        for a, b in self.ranges:
+            offs, tot = [], 0
+            for i in range(a, b):
+                offs.append(tot)
+                tot += -(-sizes[i] // self.ALIGN) * self.ALIGN
+            dslab = torch.empty(tot, dtype=torch.uint8, device=dev)
+            hslab = torch.empty(tot, dtype=torch.uint8, pin_memory=True)
+            for k, i in enumerate(range(a, b)):
+                G = self.mats[i]["G"]
+                dv = dslab[offs[k]: offs[k] + sizes[i]].view(G.dtype).view(G.shape)
+                dv.copy_(G)
+                self.mats[i]["G"] = dv
+                self._host_views[i] = hslab[offs[k]: offs[k] + sizes[i]].view(G.dtype).view(G.shape)
+            self.dev_slabs.append(dslab)
+            self.host_slabs.append(hslab)
         self.plans = [Plan(self.mats[a:b]) for a, b in self.ranges]
-        self.copy_stream = torch.cuda.Stream(device=self.mats[0]["X"].device)
+        self.copy_stream = torch.cuda.Stream(device=dev)
         self._read = [None] * len(self.plans)   # per group: event after its last step
-        self._checked = None
+
+    def host_grad(self, i: int):
+        """The pinned host buffer (a tensor view) that matrix i's gradient is read from."""
+        return self._host_views[i]
 
     def h2d_bytes(self) -> int:
-        return sum(d["G"].numel() * d["G"].element_size() for d in self.mats)
+        """Bytes copied host -> device per step (the group slabs, alignment padding included)."""
+        return sum(h.numel() for h in self.host_slabs)
 
-    def step(self, host_grads: Sequence, stream=None):
-        """Copy ``host_grads[i]`` into matrix i's G and step every group (async)."""
+    def step(self, stream=None):
+        """Copy every group's gradients in and step every group (asynchronous)."""
         import torch
-        if len(host_grads) != len(self.mats):
-            raise ValueError("one host gradient per matrix")
-        if self._checked is not host_grads:      # shapes checked once per list of gradients
-            for i, (h, d) in enumerate(zip(host_grads, self.mats)):
-                if h.shape != d["G"].shape or h.dtype != d["G"].dtype:
-                    raise ValueError(f"host gradient {i}: {tuple(h.shape)} {h.dtype}, expected "
-                                     f"{tuple(d['G'].shape)} {d['G'].dtype}")
-            self._checked = host_grads
         cs = stream if stream is not None else torch.cuda.current_stream()
-        for g, ((a, b), plan) in enumerate(zip(self.ranges, self.plans)):
+        for g, (plan, dslab, hslab) in enumerate(zip(self.plans, self.dev_slabs, self.host_slabs)):
             ready = torch.cuda.Event()
             with torch.cuda.stream(self.copy_stream):
                 if self._read[g] is not None:
                     self.copy_stream.wait_event(self._read[g])
-                for i in range(a, b):
-                    self.mats[i]["G"].copy_(host_grads[i], non_blocking=True)
+                dslab.copy_(hslab, non_blocking=True)
                 ready.record(self.copy_stream)
             cs.wait_event(ready)
             plan.step(cs)

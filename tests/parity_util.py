@@ -10,6 +10,7 @@ from oracle import dion_oracle as O
 TOL_STEP = 1e-4      # relative Frobenius error of X and R after one step from identical state
 TOL_CHAIN = 1e-3     # ... after 10 chained steps against the oracle's own float64 trajectory
 TOL_ORTH = 1e-5      # max |U^T U - I|
+TOL_DX = 1e-3        # relative Frobenius error of the update X_{t+1} - X_t (= -eta s U Vbar^T)
 
 
 def rel(a, b) -> float:
@@ -54,21 +55,45 @@ def state_snapshot(d):
     return {k: f64(d[k]) for k in ("X", "R", "V")}
 
 
-def check_step(before, G64, d_after, eta, beta, variant, scale=None, U_gpu=None, tol=TOL_STEP):
+def kappa(A) -> float:
+    """2-norm condition number of a tall matrix (from the eigenvalues of A^T A)."""
+    ev = np.linalg.eigvalsh(A.T @ A)
+    return float(np.sqrt(ev[-1] / max(ev[0], 1e-300)))
+
+
+def factor_tolerance(ref) -> float:
+    """Relative error allowed on the right factor Vbar.
+
+    A thin-QR factor moves by up to kappa times the relative perturbation of its
+    argument, and the GPU's arguments carry fp32 rounding (2^-24): U = orth(P)
+    by kappa(P), and Vbar = orth(W) (or W's unit columns) by kappa(W) on top of
+    the error W inherits from U.  The bound is that sum, times 4, and never
+    below the step tolerance."""
+    return max(TOL_STEP, 4.0 * (kappa(ref["P"]) + kappa(ref["W"])) * 2.0 ** -24)
+
+
+def check_step(before, G64, d_after, eta, beta, variant, scale=None, U_gpu=None, tol=TOL_STEP, qr=None):
     """Compare one GPU step (state ``before`` -> ``d_after``) with the oracle step
-    from the same stored state; returns the oracle's output and the errors."""
-    ref = O.oracle_step(before["X"], G64, before["R"], before["V"], eta, beta, variant, scale)
+    from the same stored state: X and R (relative Frobenius error <= tol), the
+    update X_{t+1} - X_t (<= TOL_DX), the new warm start V = Vbar (within
+    factor_tolerance) and, when given, U^T U = I.  Returns the oracle's output
+    and the errors."""
+    kw = {} if qr is None else {"qr": qr}
+    ref = O.oracle_step(before["X"], G64, before["R"], before["V"], eta, beta, variant, scale, **kw)
     after = state_snapshot(d_after)
     errs = {
         "X": rel(after["X"], ref["X"]),
         "R": rel(after["R"], ref["R"]),
         "dX": rel(after["X"] - before["X"], ref["X"] - before["X"]),
         "V": rel(after["V"], ref["V"]),
+        "tol_V": factor_tolerance(ref),
     }
     if U_gpu is not None:
         U = f64(U_gpu)
         errs["UtU"] = float(np.abs(U.T @ U - np.eye(U.shape[1])).max())
     assert errs["X"] <= tol and errs["R"] <= tol, errs
+    assert errs["dX"] <= TOL_DX, errs
+    assert errs["V"] <= errs["tol_V"], errs
     if "UtU" in errs:
         assert errs["UtU"] <= TOL_ORTH, errs
     return ref, errs

@@ -27,6 +27,7 @@ import math
 import numpy as np
 import pytest
 
+from oracle import dion_oracle as O
 from parity_util import TOL_ORTH, TOL_STEP, check_step, f64, grad_f64, rel, state_snapshot
 from rank_orthonormalized_optimizer_03_b300 import build, dion, synth, workloads
 
@@ -108,7 +109,9 @@ def sweep_case(shape, r, variants):
     scale = spec.scale if spec.scale else math.sqrt(spec.m / spec.n)
     gen = np.random.Generator(np.random.PCG64(r))
     rows, cols = strata(spec.m, 128, gen), strata(spec.n, 128, gen)
-    oracle = r <= 32
+    # element-wise against the oracle at the ends and the middle of the sweep
+    # (LAPACK's QR inside the oracle above r = 32: its textbook loop takes minutes there)
+    oracle = r in (32, 256, 2048)
     if oracle:
         before = [state_snapshot(d) for d in mats]
         G64 = grad_f64(mats[0]["G"])
@@ -122,7 +125,7 @@ def sweep_case(shape, r, variants):
     if oracle:
         for k, v in enumerate(variants):
             _, errs = check_step(before[k], G64, mats[k], spec.eta, spec.beta, v, spec.scale,
-                                 U_gpu=plan.buffer(k, dion.BUF_U))
+                                 U_gpu=plan.buffer(k, dion.BUF_U), qr=None if r <= 32 else O.lapack_qr_pos)
             out.append((v, errs))
         plan.close()
         return out
@@ -162,15 +165,15 @@ def sweep_case(shape, r, variants):
 @pytest.mark.parametrize("r", workloads.SWEEP_RANKS)
 @pytest.mark.parametrize("shape", workloads.SWEEP_SHAPES)
 def test_rank_sweep(dev, shape, r):
-    variants = ("orth", "dion") if r in (32, 2048) else ("orth",)
+    variants = ("orth", "dion") if r in (32, 256, 2048) else ("orth",)
     for v, errs in sweep_case(shape, r, variants):
         print(shape, r, v, errs)
 
 
 def test_llama3b_rdiv4_sampled_matrices(dev):
     """All 196 matrices at r = min(m, n)/4 (768, or 256 for k and v) in one plan,
-    as the step runs; the oracle checks layer 0's q (r = 768) and v (r = 256),
-    both Orth-Dion, and layer 27's k (Dion, r = 256)."""
+    as the step runs; the oracle checks the whole of layer 0 (seven matrices,
+    both variants, r = 256 and 768) and layer 27's k (Dion, r = 256)."""
     import torch
     wl = workloads.llama_3b(4)
     mats = []
@@ -179,7 +182,7 @@ def test_llama3b_rdiv4_sampled_matrices(dev):
         # the raw Gaussian warm start scaled by 1/sqrt(n), as the benchmark steps it
         mats.append(dict(X=X0, G=G, R=torch.zeros_like(X0), V=(V0_raw / math.sqrt(spec.n)).contiguous(),
                          eta=spec.eta, beta=spec.beta, variant=("orth", "dion")[k % 2], scale=spec.scale))
-    idx = [0, 2, 27 * 7 + 1]
+    idx = list(range(7)) + [27 * 7 + 1]
     before = {i: state_snapshot(mats[i]) for i in idx}
     G64 = {i: grad_f64(mats[i]["G"]) for i in idx}
     plan = dion.Plan(mats)
@@ -190,6 +193,6 @@ def test_llama3b_rdiv4_sampled_matrices(dev):
     for i in idx:
         spec = wl.mats[i]
         _, errs = check_step(before[i], G64[i], mats[i], spec.eta, spec.beta, mats[i]["variant"], spec.scale,
-                             U_gpu=plan.buffer(i, dion.BUF_U))
+                             U_gpu=plan.buffer(i, dion.BUF_U), qr=O.lapack_qr_pos)
         print(spec.name, mats[i]["variant"], errs)
     plan.close()

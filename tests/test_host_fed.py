@@ -44,22 +44,26 @@ def test_host_fed_groups_match_one_plan():
 
     ref = state()
     fed = state()
-    host_g = [d["G"].to("cpu").pin_memory() for d in fed]
-    for d in fed:
-        d["G"].zero_()            # the host copy must bring the gradient in
     plan = dion.Plan(ref)
     # two groups of six layers each still fill the GPU, so every matrix gets
     # the same K split of W = M^T U as in the single plan
     stepper = dion.HostFedStep(fed, groups=2)
-    assert len(stepper.plans) == 2
+    assert len(stepper.plans) == 2 and len(stepper.host_slabs) == 2
+    for i, d in enumerate(fed):
+        stepper.host_grad(i).copy_(d["G"].cpu())
+        assert stepper.host_grad(i).is_pinned()
+    for slab in stepper.dev_slabs:
+        slab.zero_()              # the host copy must bring the gradients in
     for _ in range(2):            # the second step waits for the first one's reads
         plan.step()
-        stepper.step(host_g)
+        stepper.step()
     torch.cuda.synchronize()
     assert plan.failures() == [0] * len(ref)
     assert [v & dion.FATAL for v in stepper.status()] == [0] * len(fed)
+    for i, d in enumerate(ref):
+        assert torch.equal(stepper.mats[i]["G"], d["G"])
     worst = 0.0
-    for a, b in zip(ref, fed):
+    for a, b in zip(ref, stepper.mats):
         for key in ("X", "R", "V"):
             worst = max(worst, rel(f64(b[key]), f64(a[key])))
     assert worst <= 1e-6, worst

@@ -112,6 +112,95 @@ def test_gpt160m_all_matrices(dev):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("variant", ["orth", "dion"])
+def test_gpt160m_chain_10_steps(dev, variant):
+    """All 72 GPT-160M matrices stepped 10 times in one plan with fresh gradients
+    every step (seeds 0..9).  Layers 0 and 11 (12 matrices) are checked every
+    step from identical state (check_step) and, after 10 steps, against the
+    oracle's own float64 trajectory from the same initial state (<= TOL_CHAIN)."""
+    import torch
+    wl = workloads.gpt_160m(4)
+    mats = device_plan(wl, dev, (variant,))
+    idx = list(range(0, 6)) + list(range(66, 72))
+    plan = dion.Plan(mats)
+    traj = {i: state_snapshot(mats[i]) for i in idx}
+    worst = {}
+    for t in range(10):
+        if t > 0:
+            for k, spec in enumerate(wl.mats):
+                mats[k]["G"].copy_(synth.device_matrix_inputs(spec, wl, k, seed=t, device=dev)[2])
+        torch.cuda.synchronize()
+        before = {i: state_snapshot(mats[i]) for i in idx}
+        G64 = {i: grad_f64(mats[i]["G"]) for i in idx}
+        plan.step()
+        torch.cuda.synchronize()
+        assert plan.failures() == [0] * len(mats)
+        for i in idx:
+            spec = wl.mats[i]
+            _, errs = check_step(before[i], G64[i], mats[i], spec.eta, spec.beta, variant, spec.scale,
+                                 U_gpu=plan.buffer(i, dion.BUF_U), qr=O.lapack_qr_pos)
+            for k, v in errs.items():
+                worst[k] = max(worst.get(k, 0.0), v)
+            ref = O.oracle_step(traj[i]["X"], G64[i], traj[i]["R"], traj[i]["V"], spec.eta, spec.beta, variant,
+                                spec.scale, qr=O.lapack_qr_pos)
+            traj[i] = dict(X=ref["X"], R=ref["R"], V=ref["V"])
+    chain = {}
+    for i in idx:
+        after = state_snapshot(mats[i])
+        chain[i] = (rel(after["X"], traj[i]["X"]), rel(after["R"], traj[i]["R"]))
+        assert chain[i][0] <= TOL_CHAIN and chain[i][1] <= TOL_CHAIN, (wl.mats[i].name, chain[i])
+    print(variant, "worst single-step", worst, "worst chain", max(max(v) for v in chain.values()))
+    plan.close()
+
+
+def ill_conditioned_case(m, n, r, kappa, seed):
+    """A matrix whose warm-started P = M V has condition number ~kappa: M's top-r
+    singular values fall geometrically from 1 to 1/kappa above a noise floor of
+    0.05 in the remaining directions, and V spans the top-r right singular
+    vectors.  The gradient is fp32 (bf16 rounding would bury the smallest
+    singular values)."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    Ua, _ = np.linalg.qr(g.standard_normal((m, n)))
+    Vb, _ = np.linalg.qr(g.standard_normal((n, n)))
+    s = np.concatenate([np.geomspace(1.0, 1.0 / kappa, r), np.full(n - r, 0.05)])
+    M = (Ua * s[None, :]) @ Vb.T
+    V = Vb[:, :r]
+    return M.astype(np.float32), V.astype(np.float32), g.normal(0, 0.02, (m, n)).astype(np.float32)
+
+
+@pytest.mark.parametrize("variant", ["orth", "dion"])
+def test_shifted_choleskyqr3_on_ill_conditioned_p(dev, variant):
+    """kappa(P) ~ 1e4 is beyond fp32 CholeskyQR2 (kappa^2 u ~ 6): the first
+    Cholesky's pivots must send orth() down the shifted CholeskyQR3 branch,
+    which reports DION_MAT_SHIFTED and still returns the positive-diagonal Q
+    factor; X, R, the update and Vbar against the oracle.  For Orth-Dion,
+    W = M^T U is as ill conditioned and takes the same branch."""
+    import torch
+    m, n, r = 1024, 512, 32
+    G, V, X = ill_conditioned_case(m, n, r, 1e4, seed=31)
+    d = dict(X=to_dev(X, dev), G=to_dev(G, dev), R=torch.zeros((m, n), device=dev), V=to_dev(V, dev),
+             eta=0.02, beta=0.95, variant=variant)
+    # a well-conditioned neighbour in the same plan must take the ordinary path
+    g = np.random.Generator(np.random.PCG64(5))
+    nb = dict(X=to_dev(g.normal(0, 0.02, (256, 128)), dev), G=to_dev(g.standard_normal((256, 128)), dev),
+              R=torch.zeros((256, 128), device=dev), V=to_dev(orth_v0(g.standard_normal((128, 16))), dev),
+              eta=0.02, beta=0.95, variant=variant)
+    plan = dion.Plan([d, nb])
+    before = [state_snapshot(d), state_snapshot(nb)]
+    plan.step()
+    torch.cuda.synchronize()
+    st = plan.status()
+    assert st[0] & dion.DION_MAT_SHIFTED and not st[0] & dion.FATAL, st
+    assert st[1] == 0, st
+    ref, errs = check_step(before[0], f64(d["G"]), d, 0.02, 0.95, variant, U_gpu=plan.buffer(0, dion.BUF_U))
+    from parity_util import kappa
+    assert kappa(ref["P"]) > 5e3, kappa(ref["P"])
+    check_step(before[1], f64(nb["G"]), nb, 0.02, 0.95, variant, U_gpu=plan.buffer(1, dion.BUF_U))
+    print(variant, "kappa(P)", kappa(ref["P"]), "kappa(W)", kappa(ref["W"]), errs)
+    plan.close()
+
+
+@pytest.mark.slow
 def test_llama3b_rdiv16_layers_0_and_27(dev):
     wl = workloads.llama_3b(16)
     idx = list(range(0, 7)) + list(range(27 * 7, 28 * 7))

@@ -5,13 +5,16 @@ that owns every device byte cannot give the library a workspace.  This entry
 point keeps its scratch in a fixed array inside libdion.so.  The test calls it
 through the C ABI twice in a row, each time on the P of a plan-based step, and
 checks the result against the U = orth(P) that the plan-based entry point
-produced from the same P, with the tolerances of the other parity tests.  It
-also checks that a request beyond the fixed scratch is refused cleanly.  The
-file is collected last so that a failure here cannot hide the other tests.
+produced from the same P and against the oracle's Householder Q factor, with
+the tolerances of the other parity tests.  An ill-conditioned argument
+(kappa ~ 1e4) must take the shifted CholeskyQR3 branch through the same fixed
+scratch.  A request beyond the fixed scratch is refused cleanly.  The file is
+collected last so that a failure here cannot hide the other tests.
 """
 import numpy as np
 import pytest
 
+from oracle import dion_oracle as O
 from parity_util import TOL_ORTH, f64, grad_to_device, rel
 from rank_orthonormalized_optimizer_03_b300 import build, dion, synth
 
@@ -55,8 +58,34 @@ def test_orth_noalloc_matches_plan_orth_on_two_calls(dev):
         sv = np.linalg.svd(Ph, compute_uv=False)
         tol = max(1e-4, 4.0 * (sv[0] / sv[-1]) * 2.0 ** -24)
         assert rel(Qh, Uh) < tol
+        assert rel(Qh, O.householder_qr_pos(Ph)[0]) < tol
         assert np.abs(Qh.T @ Qh - np.eye(r)).max() < TOL_ORTH
         plan.close()
+
+
+def test_orth_noalloc_ill_conditioned_takes_shifted_path(dev):
+    """kappa(A) ~ 1e4: the first Cholesky's pivots send the call down shifted
+    CholeskyQR3 (status DION_MAT_SHIFTED), whose second factor Q2 also lives in
+    the fixed scratch; Q still equals the oracle's positive-diagonal Q factor."""
+    import torch
+    rows, r = 1000, 48
+    g = np.random.Generator(np.random.PCG64(41))
+    Qa, _ = np.linalg.qr(g.standard_normal((rows, r)))
+    Z, _ = np.linalg.qr(g.standard_normal((r, r)))
+    A = ((Qa * np.geomspace(1.0, 1e-4, r)[None, :]) @ Z.T).astype(np.float32)
+    Ad = torch.from_numpy(A).to(dev)
+    Ah = A.astype(np.float64)
+    ref = O.householder_qr_pos(Ah)[0]
+    sv = np.linalg.svd(Ah, compute_uv=False)
+    assert sv[0] / sv[-1] > 5e3
+    tol = max(1e-4, 4.0 * (sv[0] / sv[-1]) * 2.0 ** -24)
+    for _ in range(2):
+        Q = torch.full((rows, r), float("nan"), dtype=torch.float32, device=dev)
+        st = dion.orth_noalloc(Ad, Q)
+        assert st & dion.DION_MAT_SHIFTED and not st & dion.FATAL, st
+        Qh = f64(Q)
+        assert np.abs(Qh.T @ Qh - np.eye(r)).max() < TOL_ORTH
+        assert rel(Qh, ref) < tol
 
 
 def test_orth_noalloc_refuses_sizes_beyond_its_scratch(dev):
