@@ -32,7 +32,7 @@ def nvcc_path() -> str:
 
 def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
-                  + glob.glob(os.path.join(INCLUDE, "*.h")))
+                  + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def needs_build() -> bool:
@@ -47,7 +47,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         return LIB
     cmd = [nvcc_path(), "-O3", "-std=c++17", *ARCH_FLAGS, "-lineinfo", "-Xcompiler", "-fPIC",
            "-Xcompiler", "-fvisibility=hidden", "-shared", "-I", INCLUDE, "-I", CSRC,
-           "-o", LIB + ".tmp", os.path.join(CSRC, "dion_api.cu")]
+           "-o", LIB + ".tmp", *sorted(glob.glob(os.path.join(CSRC, "*.cu"))), "-lcublas"]
     if ptxas_info:
         cmd.insert(1, "-Xptxas=-v")
     if verbose:

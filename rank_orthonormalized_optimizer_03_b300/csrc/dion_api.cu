@@ -15,6 +15,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include "common.cuh"
+#include "host_errors.h"
 #include "simt.cuh"
 #include "tc_epilogue.cuh"
 #include "tc_split.cuh"
@@ -24,10 +25,12 @@
 using namespace dion;
 
 namespace {
-
 thread_local std::string g_err;
+}  // namespace
 
-dion_status_t fail(dion_status_t s, const char* fmt, ...) {
+// Error text of the calling host thread, shared by every translation unit of the
+// library (host_errors.h).
+dion_status_t dion_fail(dion_status_t s, const char* fmt, ...) {
   char buf[512];
   va_list ap;
   va_start(ap, fmt);
@@ -37,10 +40,16 @@ dion_status_t fail(dion_status_t s, const char* fmt, ...) {
   return s;
 }
 
-dion_status_t ok() {
+dion_status_t dion_ok() {
   g_err.clear();
   return DION_OK;
 }
+
+namespace {
+
+template <class... A>
+dion_status_t fail(dion_status_t s, const char* fmt, A... a) { return dion_fail(s, fmt, a...); }
+dion_status_t ok() { return dion_ok(); }
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -21,9 +21,12 @@
 // converter warps, between conversions, add finished slices into registers in
 // round-to-nearest fp32; the bias then stays near 2e-6.
 //
-// Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2..17 converters
-// (four groups of four, alternating chunks) and slice drain.  One CTA per SM, persistent over (row tile, K range, column
-// block) items of every matrix.
+// Warp roles: 0 TMA producer of the staged G / R tiles, 1 TMEM allocator + MMA
+// issuer, 2..17 converters (four groups of four, alternating chunks) and slice
+// drain, 18 TMA producer of the B operand halves.  The two producers run
+// independently, so a full operand ring never holds back the HBM loads of the
+// staging ring (and the other way round).  One CTA per SM, persistent over
+// (row tile, K range, column block) items of every matrix.
 #pragma once
 
 #include "common.cuh"
@@ -41,7 +44,8 @@ constexpr int OSTAGES = 4;           // operand stages (A hi/lo written by the c
 constexpr int SSTAGES = 4;           // staging slots of G and R (HBM latency)
 constexpr int NCONV = 16;            // converter / drain warps: four groups of four
 constexpr int NGROUP = 4;            // converter groups; group g converts the chunks numbered g (mod 4)
-constexpr int NTHREADS = (2 + NCONV) * 32;
+constexpr int BWARP = 2 + NCONV;      // warp of the B-operand producer
+constexpr int NTHREADS = (3 + NCONV) * 32;
 constexpr int BN_MAX = 192;          // widest column block (TMEM: 2 x 192 <= 512)
 constexpr int QMAX = BN_MAX / 4;     // accumulator columns per converter thread (one column quarter)
 constexpr uint32_t TMEM_COLS = 512;
@@ -151,18 +155,16 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
   int failed = -1;
 
   if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ TMA producer
-    int os = 0, ss = 0; uint32_t oph = 0, sph = 0;
-    uint32_t olast[OSTAGES], slast[SSTAGES];
-    bool oused[OSTAGES], sused[SSTAGES];
-    for (int i = 0; i < OSTAGES; ++i) { olast[i] = 0; oused[i] = false; }
+    // ------------------------------------------------------------ TMA producer: staged G / R
+    int ss = 0; uint32_t sph = 0;
+    uint32_t slast[SSTAGES];
+    bool sused[SSTAGES];
     for (int i = 0; i < SSTAGES; ++i) { slast[i] = 0; sused[i] = false; }
     for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
       const Item it = items[t];
       const SJob& j = jobs[it.job];
       if (skip(j)) continue;
       const uint32_t gbytes = j.gmode == G_NONE ? 0u : BM * BK * (j.gmode == G_BF16 ? 2 : 4);
-      const uint32_t bbytes = j.bn * BK * 4;
       for (int kc = 0; kc < it.nk; ++kc) {
         const int k = it.k0 + kc * BK;
         // staging: G and R tiles of M
@@ -185,23 +187,37 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
         }
         sused[ss] = true; slast[ss] = sph;
         if (++ss == SSTAGES) { ss = 0; sph ^= 1; }
+      }
+    }
+  prod_done:
+    if (*abort_flag)
+      for (int i = 0; i < SSTAGES; ++i) if (sused[i]) mbar_wait_drain(&s_full[i], slast[i]);
+  } else if (warp == BWARP && lane == 0) {
+    // ------------------------------------------------------------ TMA producer: B operand halves
+    int os = 0; uint32_t oph = 0;
+    uint32_t olast[OSTAGES];
+    bool oused[OSTAGES];
+    for (int i = 0; i < OSTAGES; ++i) { olast[i] = 0; oused[i] = false; }
+    for (int t = blockIdx.x; t < nitems; t += gridDim.x) {
+      const Item it = items[t];
+      const SJob& j = jobs[it.job];
+      if (skip(j)) continue;
+      const uint32_t bbytes = j.bn * BK * 4;
+      for (int kc = 0; kc < it.nk; ++kc) {
+        const int k = it.k0 + kc * BK;
         // operand stage: the B half (already split), bn rows
-        if (!mbar_wait(&o_empty[os], oph ^ 1, abort_flag)) { failed = it.job; goto prod_done; }
+        if (!mbar_wait(&o_empty[os], oph ^ 1, abort_flag)) { failed = it.job; goto bprod_done; }
         mbar_arrive_expect_tx(&o_full[os], 2 * bbytes);
-        {
-          unsigned char* b = ost + os * OST_BYTES + 2 * A_BYTES;
-          tma_load_2d(b, &j.mBh, &o_full[os], k, it.c0);
-          tma_load_2d(b + B_BYTES_MAX, &j.mBl, &o_full[os], k, it.c0);
-        }
+        unsigned char* b = ost + os * OST_BYTES + 2 * A_BYTES;
+        tma_load_2d(b, &j.mBh, &o_full[os], k, it.c0);
+        tma_load_2d(b + B_BYTES_MAX, &j.mBl, &o_full[os], k, it.c0);
         oused[os] = true; olast[os] = oph;
         if (++os == OSTAGES) { os = 0; oph ^= 1; }
       }
     }
-  prod_done:
-    if (*abort_flag) {
-      for (int i = 0; i < SSTAGES; ++i) if (sused[i]) mbar_wait_drain(&s_full[i], slast[i]);
+  bprod_done:
+    if (*abort_flag)
       for (int i = 0; i < OSTAGES; ++i) if (oused[i]) mbar_wait_drain(&o_full[i], olast[i]);
-    }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     int os = 0; uint32_t oph = 0; int b = 0; uint32_t aph[2] = {0, 0};
@@ -239,7 +255,7 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
     }
   mma_done:
     if (*abort_flag && issued) { mma_commit(drain); mbar_wait_drain(drain, 0); }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < BWARP) {
     // ------------------------------------------------------------ converters + slice drain
     // Four groups of four warps; group g converts the chunks whose sequence number
     // is g mod 4, so four chunks are in conversion at once.  For the drain every

@@ -14,7 +14,8 @@ from typing import List, Optional, Sequence
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libdion.so")
-HEADER = os.path.join(os.path.dirname(PKG), "include", "dion.h")
+INCLUDE = os.path.join(os.path.dirname(PKG), "include")
+HEADER = os.path.join(INCLUDE, "dion.h")
 
 DION_OK, DION_ERR_INVALID_ARG, DION_ERR_CUDA, DION_ERR_WORKSPACE, DION_ERR_UNSUPPORTED = range(5)
 DION_MAT_OK, DION_MAT_CHOL_BREAKDOWN, DION_MAT_NONFINITE, DION_MAT_TIMEOUT, DION_MAT_SHIFTED = 0, 1, 2, 4, 8
@@ -34,6 +35,18 @@ class MatrixDesc(ctypes.Structure):
         ("eta", ctypes.c_float), ("beta", ctypes.c_float), ("scale", ctypes.c_float),
         ("reserved", ctypes.c_float),
     ]
+
+
+class MuonDesc(ctypes.Structure):
+    _fields_ = [
+        ("X", ctypes.c_void_p), ("G", ctypes.c_void_p), ("B", ctypes.c_void_p),
+        ("m", ctypes.c_int64), ("n", ctypes.c_int64),
+        ("ld_x", ctypes.c_int64), ("ld_g", ctypes.c_int64), ("ld_b", ctypes.c_int64),
+        ("g_dtype", ctypes.c_int32), ("eta", ctypes.c_float), ("mu", ctypes.c_float), ("scale", ctypes.c_float),
+    ]
+
+
+MUON_PRECISION = {"bf16": 0, "tf32": 1, "fp32": 2}
 
 
 class DionError(RuntimeError):
@@ -66,6 +79,10 @@ def _declare(L):
         "dion_plan_get_status": (I32, [P, P, SZ, ctypes.POINTER(ctypes.c_uint32), P]),
         "dion_plan_launches_per_step": (I32, [P]),
         "dion_orth_noalloc": (I32, [P, I64, I64, I64, P, I64, ctypes.POINTER(ctypes.c_uint32), P]),
+        "muon_plan_create": (I32, [ctypes.POINTER(MuonDesc), I32, I32, I32, ctypes.POINTER(SZ), ctypes.POINTER(P)]),
+        "muon_step_batched": (I32, [P, P, SZ, P]),
+        "muon_plan_launches_per_step": (I32, [P]),
+        "muon_plan_destroy": (None, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -86,9 +103,13 @@ def lib():
 
 
 def header_functions() -> List[str]:
-    """Names of the functions declared in include/dion.h."""
-    txt = open(HEADER).read()
-    return sorted(set(re.findall(r"DION_API\s+[\w\s\*]+?\b(dion_\w+)\s*\(", txt)))
+    """Names of the functions declared in the headers under include/."""
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            txt = open(os.path.join(INCLUDE, h)).read()
+            names |= set(re.findall(r"DION_API\s+[\w\s\*]+?\b((?:dion|muon)_\w+)\s*\(", txt))
+    return sorted(names)
 
 
 def check(code: int, where: str):
@@ -259,6 +280,71 @@ class Plan:
         nbytes = rows.value * ld.value * 4
         raw = self.workspace[off.value: off.value + nbytes]
         return raw.view(torch.float32).view(rows.value, ld.value)[:, : cols.value]
+
+
+class MuonPlan:
+    """The Muon comparator (include/muon.h) over a batch of matrices.
+
+    ``mats`` is a sequence of dicts with keys X, G, B (CUDA tensors owned by the
+    caller; X and the momentum B are float32 and updated in place, G float32 or
+    bfloat16) and eta, mu, optional scale (<= 0 or missing: sqrt(m/n)).
+    ``iters`` Newton-Schulz iterations in ``precision`` "bf16" | "tf32" | "fp32".
+    """
+
+    def __init__(self, mats: Sequence[dict], iters: int = 5, precision: str = "bf16", workspace=None):
+        import torch
+        L = lib()
+        if len(mats) == 0:
+            raise ValueError("a plan needs at least one matrix")
+        if precision not in MUON_PRECISION:
+            raise ValueError(f"precision must be one of {sorted(MUON_PRECISION)}")
+        descs = []
+        dev0 = mats[0]["X"].device
+        for k, d in enumerate(mats):
+            X, G, B = d["X"], d["G"], d["B"]
+            _check_device((X, G, B), ("X", "G", "B"), dev0)
+            if X.dim() != 2 or G.shape != X.shape or B.shape != X.shape:
+                raise ValueError(f"matrix {k}: X, G, B must be m x n matrices of one shape")
+            if X.stride(1) != 1 or G.stride(1) != 1 or B.stride(1) != 1:
+                raise ValueError(f"matrix {k}: X, G, B must be row-major views")
+            if X.dtype != torch.float32 or B.dtype != torch.float32 or G.dtype not in (torch.float32, torch.bfloat16):
+                raise ValueError(f"matrix {k}: X, B float32 and G float32 or bfloat16")
+            m, n = X.shape
+            descs.append(MuonDesc(X.data_ptr(), G.data_ptr(), B.data_ptr(), m, n, X.stride(0), G.stride(0),
+                                  B.stride(0), DTYPE_BF16 if G.dtype == torch.bfloat16 else DTYPE_F32,
+                                  float(d["eta"]), float(d["mu"]), float(d.get("scale", 0.0))))
+        self._keep = [(d["X"], d["G"], d["B"]) for d in mats]
+        self._descs = (MuonDesc * len(descs))(*descs)
+        ws = ctypes.c_size_t(0)
+        plan = ctypes.c_void_p()
+        check(L.muon_plan_create(self._descs, len(descs), int(iters), MUON_PRECISION[precision], ctypes.byref(ws),
+                                 ctypes.byref(plan)), "muon_plan_create")
+        self._plan = plan
+        self.ws_bytes = ws.value
+        if workspace is None:
+            workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev0)
+        if workspace.dtype != torch.uint8 or workspace.dim() != 1 or workspace.numel() < self.ws_bytes:
+            raise ValueError("workspace must be a 1-D uint8 tensor of at least ws_bytes")
+        self.workspace = workspace
+
+    @property
+    def launches_per_step(self) -> int:
+        return lib().muon_plan_launches_per_step(self._plan)
+
+    def step(self, stream=None):
+        check(lib().muon_step_batched(self._plan, self.workspace.data_ptr(), self.ws_bytes, _stream_ptr(stream)),
+              "muon_step_batched")
+
+    def close(self):
+        if getattr(self, "_plan", None):
+            lib().muon_plan_destroy(self._plan)
+            self._plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def group_bounds(nbytes: Sequence[int], groups: int) -> List[tuple]:

@@ -171,3 +171,37 @@ def test_work_tables_pass_their_check_for_odd_batches(L):
             shapes.append((m, n, r, int(g.integers(0, 2)), int(g.integers(0, 2))))
         code, _, msg = plan_of(L, shapes)
         assert code == dion.DION_OK, (shapes, msg)
+
+
+def muon_desc(k, m=64, n=32, **kw):
+    d = dict(X=BASE + (3 * k) * SLOT, G=BASE + (3 * k + 1) * SLOT, B=BASE + (3 * k + 2) * SLOT, m=m, n=n,
+             ld_x=n, ld_g=n, ld_b=n, g_dtype=dion.DTYPE_BF16, eta=0.01, mu=0.95, scale=0.0)
+    d.update(kw)
+    return dion.MuonDesc(**d)
+
+
+def muon_create(L, descs, iters=5, precision=0):
+    arr = (dion.MuonDesc * len(descs))(*descs)
+    ws = ctypes.c_size_t(0)
+    plan = ctypes.c_void_p()
+    code = L.muon_plan_create(arr, len(descs), iters, precision, ctypes.byref(ws), ctypes.byref(plan))
+    return code, ws.value, plan
+
+
+def test_muon_plan_groups_shapes_and_validates(L):
+    descs = [muon_desc(0), muon_desc(1), muon_desc(2, m=32, n=64), muon_desc(3, g_dtype=dion.DTYPE_F32)]
+    code, ws, plan = muon_create(L, descs, iters=5)
+    assert code == dion.DION_OK, L.dion_last_error()
+    # two groups of equal shape (64 x 32: matrices 0, 1, 3; 32 x 64: matrix 2):
+    # 4 streaming launches + 5 iterations x (2 GEMMs + diagonal) x 2 groups
+    assert L.muon_plan_launches_per_step(plan) == 4 + 5 * 3 * 2
+    # two ping-pong Y buffers (bf16) of 4 matrices of 2048 elements, the Grams, 32 MB of GEMM scratch
+    assert ws >= (32 << 20) + 2 * 2 * 4 * 2048
+    L.muon_plan_destroy(plan)
+    for bad, kw in [("precision", dict(precision=3)), ("iters", dict(iters=-1))]:
+        code, _, _ = muon_create(L, descs, **kw)
+        assert code == dion.DION_ERR_INVALID_ARG, bad
+    for kw in [dict(X=0), dict(ld_b=16), dict(g_dtype=7), dict(m=0)]:
+        code, _, _ = muon_create(L, [muon_desc(0, **kw)])
+        assert code == dion.DION_ERR_INVALID_ARG, kw
+    L.muon_plan_destroy(None)
