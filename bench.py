@@ -387,11 +387,52 @@ def crossover(lines):
     return out
 
 
+MUON_ITERS = 5
+
+
+def measure_muon(wl, args, dev, precision, iters=MUON_ITERS, min_timed_s=1.0):
+    """The Muon comparator on the same matrices (momentum + `iters` cubic
+    Newton-Schulz iterations + update), timed like the Dion step."""
+    import torch
+    from rank_orthonormalized_optimizer_03_b300 import dion, synth
+    mats = []
+    for k, spec in enumerate(wl.mats):
+        X0, _, G = synth.device_matrix_inputs(spec, wl, k, seed=args.seed, device=dev)
+        mats.append(dict(X=X0, G=G, B=torch.zeros_like(X0), eta=spec.eta, mu=0.95, scale=spec.scale))
+    plan = dion.MuonPlan(mats, iters=iters, precision=precision)
+    stream = torch.cuda.current_stream()
+    t0 = time.perf_counter()
+    for _ in range(args.warmup):
+        plan.step()
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - t0) / max(1, args.warmup)
+    steps = max(args.steps, min(2000, int(math.ceil(min_timed_s / max(est, 1e-5)))))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        plan.step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    # flops of the iteration: two GEMMs of 2 k^2 l each (k = min, l = max side) per matrix
+    fl = iters * sum(4.0 * min(s.m, s.n) ** 2 * max(s.m, s.n) for s in wl.mats)
+    out = {"comparator": "muon", "workload": wl.name, "precision": precision, "ns_iters": iters,
+           "ms_per_step": round(ms, 4), "steps": steps, "ns_tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+           "launches_per_step": plan.launches_per_step}
+    plan.close()
+    del plan, mats
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_configs(args, dev, world, rank, peaks):
     """One JSON line per configuration (GPT-160M, Llama-3B at rank min/16 and min/4,
-    the rank sweep; both variants), then one line with the sweep's crossover."""
+    the rank sweep; both variants), then one line with the sweep's crossover.  The
+    model workloads also get a line of the Muon comparator on the same matrices
+    (bf16 and tf32 Newton-Schulz) with the Dion / Muon step-time ratio."""
     import torch
     lines = []
+    muon_done = {}
     for wl, v in config_list(args.configs):
         out, plan, mats, _ = measure(wl, args, dev, world, v, peaks, min_timed_s=1.0)
         plan.close()
@@ -400,6 +441,13 @@ def run_configs(args, dev, world, rank, peaks):
         lines.append(out)
         if rank == 0:
             print(json.dumps(out), flush=True)
+        if not wl.name.startswith("sweep_") and wl.name not in muon_done:
+            muon_done[wl.name] = [measure_muon(wl, args, dev, p) for p in ("bf16", "tf32")]
+        if wl.name in muon_done and rank == 0:
+            for mu in muon_done[wl.name]:
+                print(json.dumps(dict(mu, dion_variant=v, dion_ms_per_step=out["ms_per_step"],
+                                      muon_over_dion=round(mu["ms_per_step"] / out["ms_per_step"], 3))),
+                      flush=True)
     if rank == 0 and any(x["config"]["workload"].startswith("sweep_") for x in lines):
         print(json.dumps({"sweep_crossover": crossover(lines)}), flush=True)
 

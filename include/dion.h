@@ -184,6 +184,37 @@ DION_API dion_status_t dion_plan_get_status(dion_plan* plan, const void* workspa
 DION_API int32_t dion_plan_launches_per_step(const dion_plan* plan);
 
 /*
+ * Row-sharded step (the sharded setting of the Dion abstract, searcharxiv
+ * 2504.05295, "integrating cleanly with weight sharding"; Orth-Dion abstract,
+ * thelatestinai.com 2605.16341: the same per-step communication as Dion).
+ *
+ * Every rank makes a plan over its own rows of each matrix (the descriptors
+ * hold the local m; n, r, variant and the hyper-parameters are the same on
+ * every rank, and `scale` must be set explicitly to s of the whole matrix,
+ * e.g. sqrt(m_total / n)); V is replicated.  One step is five stages, with the
+ * caller summing a workspace region over all ranks (an all-reduce, e.g. NCCL)
+ * after stages 0, 1, 2 (region DION_EXCHANGE_GRAM: the r x r Grams of every
+ * CholeskyQR pass of orth(P)) and 3 (region DION_EXCHANGE_W: every W = M^T U):
+ *   0  P = M V over the local rows, its Gram       -> all-reduce GRAM
+ *   1  CholeskyQR pass 1 on the summed Gram        -> all-reduce GRAM
+ *   2  CholeskyQR pass 2 (U, unless shifted)       -> all-reduce GRAM
+ *   3  shifted pass (if any), W over local rows    -> all-reduce W
+ *   4  Vbar = orth(W) | colnorm(W), X and R update of the local rows, V <- Vbar
+ * On one rank with no exchange, stages 0..4 compute the same step as
+ * dion_step_batched().  Asynchronous on `stream`; the caller's all-reduce must
+ * be ordered after the stage on that stream.  The per-matrix status words are
+ * the same as for the fused step.
+ */
+enum { DION_EXCHANGE_GRAM = 0, DION_EXCHANGE_W = 1 };
+DION_API dion_status_t dion_shard_stage(dion_plan* plan, void* workspace, size_t ws_bytes, int32_t stage,
+                                        void* stream);
+
+/* Byte offset from the workspace base and size of exchange region `which`
+ * (DION_EXCHANGE_GRAM: the matrices' rp x rp fp32 Grams back to back; DION_EXCHANGE_W:
+ * their n x rp fp32 W back to back; rp = r rounded up to 32).  Host only. */
+DION_API dion_status_t dion_plan_exchange(const dion_plan* plan, int32_t which, size_t* byte_offset, size_t* bytes);
+
+/*
  * orth() of one matrix for callers that cannot allocate device memory.
  *
  * Some callers may not call cudaMalloc at all: code running inside a CUDA

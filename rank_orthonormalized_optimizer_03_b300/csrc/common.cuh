@@ -56,6 +56,7 @@ struct OrthJob {
   long long ldo;
   long long out_cols;  // columns written to out (rp in the workspace, r into V)
   float* gpart;        // nchunk x rp x rp Gram partial sums
+  float* gsum;         // rp x rp: their sum (k_gram_reduce), read by a reduced Cholesky
   float* S;            // rp x rp Gram / Cholesky factor
   float* T;            // rp x rp inverse of the Cholesky factor
   float* Tt_hi;        // rp x rp: T^T split into tf32 halves (B operand of the tensor-core A T)

@@ -86,6 +86,13 @@ struct dion_plan {
 
   // workspace layout (byte offsets from the workspace base)
   size_t ws_bytes = 0;
+  // exchange regions of the row-sharded step: the reduced Grams of orth(P) of every
+  // matrix, and every W, each back to back (dion_plan_exchange)
+  size_t off_gx = 0, gx_bytes = 0, off_wx = 0, wx_bytes = 0;
+  std::vector<size_t> off_gsum;
+  // tf32 halves of W recomputed from the exchanged W (row-sharded stage 4)
+  size_t t_wsplit = 0, t_ts_wsplit = 0;
+  std::vector<int> ts_wsplit;
   size_t off_tables = 0, tables_bytes = 0, off_status = 0;
   std::vector<size_t> off_P, off_Q, off_Q2, off_U, off_W, off_Wpart, off_gpart, off_S, off_T, off_Vo;
 
@@ -282,6 +289,7 @@ void layout(dion_plan* p) {
       return cdiv(rows * p->rp[i], tcsplit::ELEMS_PER_CTA);
     });
   }
+  prefix(p->ts_wsplit, all, [&](int i) { return cdiv(D(i).n * p->rp[i], tcsplit::ELEMS_PER_CTA); });
   prefix(p->ts_tv, all, [&](int i) { return cdiv(D(i).n, 32) * cdiv(p->rp[i], 32); });
   prefix(p->ts_tu, all, [&](int i) { return cdiv(D(i).m, 32) * cdiv(p->rp[i], 32); });
   {
@@ -381,6 +389,8 @@ void layout(dion_plan* p) {
   p->t_sj_c = take(sizeof(tcstream::SJob) * cnt);
   p->t_epi = take(sizeof(tcepi::EpiMat) * cnt);
   p->t_split = take(sizeof(tcsplit::SplitJob) * std::max(1, p->n_split));
+  p->t_wsplit = take(sizeof(tcsplit::SplitJob) * cnt);
+  p->t_ts_wsplit = take(4 * p->ts_wsplit.size());
   p->t_ts_split = take(4 * p->ts_split.size());
   p->t_tj_v = take(sizeof(tcsplit::TJob) * cnt);
   p->t_tj_u = take(sizeof(tcsplit::TJob) * cnt);
@@ -410,14 +420,33 @@ void layout(dion_plan* p) {
   p->off_Q2.resize(cnt);
   p->off_P.resize(cnt); p->off_Q.resize(cnt); p->off_U.resize(cnt); p->off_W.resize(cnt);
   p->off_Wpart.resize(cnt); p->off_gpart.resize(cnt); p->off_S.resize(cnt); p->off_T.resize(cnt);
-  p->off_Vo.resize(cnt);
+  p->off_Vo.resize(cnt); p->off_gsum.resize(cnt);
+  // every W (n x rp, a multiple of 128 bytes) and every reduced Gram of orth(P)
+  // (rp x rp) back to back: one exchange region each
+  {
+    size_t wb = 0, gb = 0;
+    for (int i = 0; i < cnt; ++i) {
+      wb += 4 * (size_t)(D(i).n * p->rp[i]);
+      gb += 4 * (size_t)(p->rp[i] * p->rp[i]);
+    }
+    p->off_wx = region(wb);
+    p->wx_bytes = wb;
+    p->off_gx = region(gb);
+    p->gx_bytes = gb;
+    size_t wo = p->off_wx, go = p->off_gx;
+    for (int i = 0; i < cnt; ++i) {
+      p->off_W[i] = wo;
+      wo += 4 * (size_t)(D(i).n * p->rp[i]);
+      p->off_gsum[i] = go;
+      go += 4 * (size_t)(p->rp[i] * p->rp[i]);
+    }
+  }
   for (int i = 0; i < cnt; ++i) {
     const long long m = D(i).m, n = D(i).n, rp = p->rp[i];
     p->off_P[i] = region(4 * (size_t)(m * rp));
     p->off_Q[i] = region(4 * (size_t)(std::max(m, n) * rp));
     p->off_Q2[i] = region(4 * (size_t)(std::max(m, n) * rp));
     p->off_U[i] = region(4 * (size_t)(m * rp));
-    p->off_W[i] = region(4 * (size_t)(n * rp));
     p->off_Wpart[i] = region(p->ksplit[i] > 1 ? 4 * (size_t)p->ksplit[i] * (size_t)(n * rp) : 4);
     p->off_gpart[i] = region(4 * (size_t)std::max(p->nchunk_p[i], p->nchunk_w[i]) * (size_t)(rp * rp));
     p->off_S[i] = region(4 * (size_t)(rp * rp + rp + 32 * rp));
@@ -635,6 +664,7 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
       o.Q2 = reinterpret_cast<float*>(base + p->off_Q2[i]);
       o.out = out; o.ldo = ldo; o.out_cols = ocols;
       o.gpart = reinterpret_cast<float*>(base + p->off_gpart[i]);
+      o.gsum = o.gpart;
       o.S = reinterpret_cast<float*>(base + p->off_S[i]);
       o.T = reinterpret_cast<float*>(base + p->off_T[i]);
       o.Tt_hi = p->tc_orth ? reinterpret_cast<float*>(base + p->off_Tth[i]) : nullptr;
@@ -645,12 +675,14 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     };
     job(jp[i], x.P, x.m, x.U, x.rp, x.rp, p->nchunk_p[i], p->chunk_p[i]);
     jp[i].flag = status + cnt + i;
+    jp[i].gsum = reinterpret_cast<float*>(base + p->off_gsum[i]);   // the exchange region
   }
   for (size_t k = 0; k < p->orth_idx.size(); ++k) {
     const int i = p->orth_idx[k];
     const MatDev& x = mats[i];
     OrthJob& o = jw[k];
     o = jp[i];
+    o.gsum = o.gpart;
     o.A = x.W; o.lda = x.rp; o.rows = x.n;
     o.out = x.V; o.ldo = x.r; o.out_cols = x.r;
     o.nchunk = p->nchunk_w[i]; o.chunk = p->chunk_w[i];
@@ -661,6 +693,7 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     const MatDev& x = mats[i];
     OrthJob& o = jv[k];
     o = jp[i];
+    o.gsum = o.gpart;
     o.A = p->tc_orth ? x.Vin : x.V; o.lda = p->tc_orth ? x.rp : x.r; o.rows = x.n;
     o.out = const_cast<float*>(x.Vin); o.ldo = x.rp; o.out_cols = x.rp;
     o.nchunk = p->nchunk_w[i]; o.chunk = p->chunk_w[i];
@@ -853,6 +886,14 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
   put(p->image, p->t_epi, epi.data(), epi.size());
   put(p->image, p->t_split, sj.data(), sj.size());
   put(p->image, p->t_ts_split, p->ts_split.data(), p->ts_split.size());
+  {
+    std::vector<tcsplit::SplitJob> ws(cnt);
+    for (int i = 0; i < cnt; ++i)
+      ws[i] = tcsplit::SplitJob{mats[i].W, p->rp[i], mats[i].Wh, mats[i].Wl, p->rp[i], p->descs[i].n,
+                                p->descs[i].r, mats[i].status};
+    put(p->image, p->t_wsplit, ws.data(), ws.size());
+    put(p->image, p->t_ts_wsplit, p->ts_wsplit.data(), p->ts_wsplit.size());
+  }
   return DION_OK;
 }
 
@@ -1022,6 +1063,103 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
   return ok();
 }
 
+// ---- row-sharded step: the step of phases (a)-(e) cut at its three exchange points
+//
+// A rank holds rows of X, G and R (V replicated).  P's rows are local, but orth(P)
+// needs the Gram P^T P of all rows, and W = M^T U sums over all rows; so the
+// step stops after every Gram of orth(P)'s CholeskyQR passes (the reduced Grams in
+// the exchange region, all-reduced by the caller between stages) and after the
+// local W (the W region).  Stage k:
+//   0  status reset, orth(V) (Dion), P = M V, Gram of P (pass 0)
+//   1  Cholesky + inverse of the exchanged Gram, Q1 = P T, Gram of Q1 (pass 1)
+//   2  Cholesky + inverse, U = Q1 T2 (or Q2 for a shifted job), Gram of Q2 (shifted jobs)
+//   3  Cholesky + inverse and U = Q2 T3 (shifted jobs), W = M^T U over the local rows
+//   4  W's tf32 halves from the exchanged W, Vbar = orth(W) | colnorm(W), X and R update
+// Every rank computes the same Cholesky factors and Vbar from the same exchanged
+// data (the kernels are deterministic), and the shifted-pass decision with them.
+dion_status_t run_shard_stage(dion_plan* p, void* workspace, size_t ws_bytes, int stage, void* stream) {
+  dion_status_t st = check_ws(p, workspace, ws_bytes);
+  if (st) return st;
+  if (stage < 0 || stage > 4) return fail(DION_ERR_INVALID_ARG, "shard stage %d outside 0..4", stage);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned char* base = static_cast<unsigned char*>(workspace);
+  if (p->dirty || p->uploaded_ws != workspace) {
+    st = dion_plan_upload(p, workspace, ws_bytes, stream);
+    if (st) return st;
+  }
+  const int cnt = p->count;
+  const MatDev* mats = tab<MatDev>(p, base, p->t_mats);
+  const OrthJob* jobs = tab<OrthJob>(p, base, p->t_jobs_p);
+  long long rmax = 0;
+  for (int i = 0; i < cnt; ++i) rmax = std::max<long long>(rmax, p->descs[i].r);
+  const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax + 32 * rmax) * 4);
+  const bool use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
+  // pieces of orth(P) (list 0), one CholeskyQR pass at a time
+  auto gram = [&](int ps) {
+    if (p->tc_orth) {
+      const int ng = (int)p->it_g[0].size();
+      tcgram::k_gram<<<std::min(ng, p->num_sms), tcgram::NTHREADS, tcgram::SMEM_BYTES, s>>>(
+          tab<tcgram::GJob>(p, base, p->t_gj[0][ps]), tab<tcgram::GItem>(p, base, p->t_it_g[0]), ng);
+    } else {
+      simt::k_gram<<<p->ts_gram_p[cnt], simt::NT, 0, s>>>(jobs, tab<int>(p, base, p->t_ts_gram_p), cnt, ps);
+    }
+    simt::k_gram_reduce<<<p->ts_gred[0][cnt], 256, 0, s>>>(jobs, tab<int>(p, base, p->t_ts_gred[0]), cnt, ps);
+  };
+  auto chol = [&](int ps) {
+    const int* order = p->tc_orth ? tab<int>(p, base, p->t_chol_order[0]) : nullptr;
+    if (use_smem)
+      simt::k_chol_inv<true><<<cnt, simt::CHOL_NT, chol_smem, s>>>(jobs, ps, 1, order);
+    else
+      simt::k_chol_inv<false><<<cnt, simt::CHOL_NT, 0, s>>>(jobs, ps, 1, order);
+  };
+  auto apply_t = [&](int ps) {
+    if (p->tc_orth) {
+      const int nt = (int)p->it_tr[0].size();
+      tcstream::k_stream<false><<<std::min(nt, p->num_sms), tcstream::NTHREADS, tcstream::SMEM_BYTES, s>>>(
+          tab<tcstream::SJob>(p, base, p->t_tj[0][ps]), tab<tcstream::Item>(p, base, p->t_it_tr[0]), nt);
+    } else {
+      simt::k_trmm<<<p->ts_trmm_p[cnt], simt::NT, 0, s>>>(jobs, tab<int>(p, base, p->t_ts_trmm_p), cnt, ps);
+    }
+  };
+  switch (stage) {
+    case 0: {
+      // phase (a) as in the fused step, then the first Gram into the exchange region
+      st = run_phases(p, workspace, ws_bytes, 0, 0, stream);
+      if (st) return st;
+      gram(0);
+      break;
+    }
+    case 1:
+    case 2:
+      chol(stage - 1);
+      apply_t(stage - 1);
+      gram(stage);
+      break;
+    case 3:
+      chol(2);
+      apply_t(2);
+      if (!p->tc_orth)
+        tcsplit::k_tsplit<<<p->ts_tu[cnt], tcsplit::NT, 0, s>>>(
+            tab<tcsplit::TJob>(p, base, p->t_tj_u), tab<int>(p, base, p->t_ts_tu), cnt);
+      tcstream::k_stream<true><<<std::min((int)p->it_sc.size(), p->num_sms), tcstream::NTHREADS,
+                                 tcstream::SMEM_BYTES, s>>>(tab<tcstream::SJob>(p, base, p->t_sj_c),
+                                                            tab<tcstream::Item>(p, base, p->t_it_sc),
+                                                            (int)p->it_sc.size());
+      if (p->any_split)
+        simt::k_wreduce<<<p->ts_wred[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_wred), cnt);
+      break;
+    case 4:
+      tcsplit::k_split<<<p->ts_wsplit[cnt], tcsplit::NT, 0, s>>>(
+          tab<tcsplit::SplitJob>(p, base, p->t_wsplit), tab<int>(p, base, p->t_ts_wsplit), cnt);
+      st = cuda_check("shard stage launch");
+      if (st) return st;
+      return run_phases(p, workspace, ws_bytes, 3, 4, stream);
+  }
+  st = cuda_check("shard stage launch");
+  if (st) return st;
+  return ok();
+}
+
 // ---- dion_orth_noalloc: one orth() on the CUDA-core kernels, scratch in g_noalloc_scratch
 
 // Writes the job and its launch tables into the scratch and clears the status
@@ -1081,6 +1219,7 @@ dion_status_t orth_noalloc_impl(const float* A, long long rows, long long r, lon
   job.status = reinterpret_cast<unsigned*>(base + 256 + 32);
   job.flag = job.status + 1;
   job.Tt_hi = job.Tt_lo = nullptr;
+  job.gsum = job.gpart;
   const long long nt = cdiv(rp, simt::TN);
   const int ngram = (int)(nch * nt * nt);
   const int ntrmm = (int)(cdiv(rows, simt::TM) * nt);
@@ -1248,6 +1387,20 @@ int32_t dion_plan_launches_per_step(const dion_plan* plan) {
   n += plan->n_split > 0 ? 1 : 0;              // phase (d): tf32 halves left to split
   n += (int)plan->it_epi.size();               // phase (e): tensor-core update, one launch per K pass
   return n;
+}
+
+dion_status_t dion_shard_stage(dion_plan* plan, void* workspace, size_t ws_bytes, int32_t stage, void* stream) {
+  return run_shard_stage(plan, workspace, ws_bytes, stage, stream);
+}
+
+dion_status_t dion_plan_exchange(const dion_plan* plan, int32_t which, size_t* byte_offset, size_t* bytes) {
+  if (!plan || !byte_offset || !bytes) return fail(DION_ERR_INVALID_ARG, "NULL argument");
+  switch (which) {
+    case DION_EXCHANGE_GRAM: *byte_offset = plan->off_gx; *bytes = plan->gx_bytes; break;
+    case DION_EXCHANGE_W: *byte_offset = plan->off_wx; *bytes = plan->wx_bytes; break;
+    default: return fail(DION_ERR_INVALID_ARG, "unknown exchange region %d", which);
+  }
+  return ok();
 }
 
 dion_status_t dion_orth_noalloc(const float* A, int64_t rows, int64_t r, int64_t lda, float* Q, int64_t ldq,

@@ -138,8 +138,8 @@ __global__ void __launch_bounds__(NT) k_gram(const OrthJob* __restrict__ jobs,
 constexpr int CHOL_NT = 512;
 constexpr int CHOL_SMEM_MAX = 200 * 1024;
 
-// Sum of the Gram partials of every job, in a fixed order, into partial 0
-// (gpart[0] = sum_c gpart[c]); one thread per Gram element over the whole GPU,
+// Sum of the Gram partials of every job, in a fixed order, into gsum
+// (gsum = sum_c gpart[c]); one thread per Gram element over the whole GPU,
 // four partials in flight per thread.
 constexpr int GRED_ELEMS = 1024;
 __global__ void __launch_bounds__(256) k_gram_reduce(const OrthJob* __restrict__ jobs,
@@ -162,18 +162,22 @@ __global__ void __launch_bounds__(256) k_gram_reduce(const OrthJob* __restrict__
       s3 += g[(long long)(c + 3) * rp2];
     }
     for (; c < o.nchunk; ++c) s0 += g[(long long)c * rp2];
-    o.gpart[idx] = (s0 + s1) + (s2 + s3);
+    o.gsum[idx] = (s0 + s1) + (s2 + s3);
   }
 }
 
-__device__ void chol_load(const OrthJob& o, int nchunk, float* S, int lds, float shift, float* s_trace) {
+// The job's Gram into S (r x lds): the reduced sum gsum when `reduced`, else the
+// sum of its nchunk partials.
+__device__ void chol_load(const OrthJob& o, int reduced, float* S, int lds, float shift, float* s_trace) {
   const int tid = threadIdx.x, nth = blockDim.x;
   const int r = o.r, rp = o.rp;
   float tr = 0.f;
   for (int e = tid; e < r * r; e += nth) {
     const int a = e / r, b = e % r;
     float v = 0.f;
-    for (int c = 0; c < nchunk; ++c) v += o.gpart[(long long)c * rp * rp + a * rp + b];
+    if (reduced) v = o.gsum[a * rp + b];
+    else
+      for (int c = 0; c < o.nchunk; ++c) v += o.gpart[(long long)c * rp * rp + a * rp + b];
     if (a == b) { tr += v; v += shift; }
     S[a * lds + b] = v;
   }
@@ -345,15 +349,14 @@ __global__ void __launch_bounds__(CHOL_NT, 1) k_chol_inv(const OrthJob* __restri
   const int lds = SMEM ? r + 1 : rp;
   float* tdiag = S + r * lds;
   float* scratch = tdiag + r;
-  const int nchunk = reduced ? 1 : o.nchunk;
-  chol_load(o, nchunk, S, lds, 0.f, s_trace);
+  chol_load(o, reduced, S, lds, 0.f, s_trace);
   int bad = chol_factor(S, lds, r, tdiag, scratch, &s_bad, &s_min, &s_max);
   if (pass == 0 && (bad || s_min < 1e-6f * s_max)) {
     float trace = 0.f;
     for (int w = 0; w < nth / 32; ++w) trace += s_trace[w];
     const float shift = 11.f * ((float)o.rows * (float)r + (float)r * (float)(r + 1)) * 5.9604645e-8f * trace;
     __syncthreads();
-    chol_load(o, nchunk, S, lds, shift, s_trace);
+    chol_load(o, reduced, S, lds, shift, s_trace);
     bad = chol_factor(S, lds, r, tdiag, scratch, &s_bad, &s_min, &s_max);
     if (!bad && tid == 0) { *o.flag = 1u; atomicOr(o.status, ST_SHIFTED); }
   }

@@ -79,6 +79,8 @@ def _declare(L):
         "dion_plan_get_status": (I32, [P, P, SZ, ctypes.POINTER(ctypes.c_uint32), P]),
         "dion_plan_launches_per_step": (I32, [P]),
         "dion_orth_noalloc": (I32, [P, I64, I64, I64, P, I64, ctypes.POINTER(ctypes.c_uint32), P]),
+        "dion_shard_stage": (I32, [P, P, SZ, I32, P]),
+        "dion_plan_exchange": (I32, [P, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
         "muon_plan_create": (I32, [ctypes.POINTER(MuonDesc), I32, I32, I32, ctypes.POINTER(SZ), ctypes.POINTER(P)]),
         "muon_step_batched": (I32, [P, P, SZ, P]),
         "muon_plan_launches_per_step": (I32, [P]),
