@@ -76,7 +76,19 @@ enum {
                                    (kappa > ~1e3) and took shifted CholeskyQR3; the update is complete */
 };
 
-typedef enum { DION_VARIANT_DION = 0, DION_VARIANT_ORTH = 1 } dion_variant_t;
+/*
+ * Right factor and state of a matrix:
+ *   DION_VARIANT_DION          Vbar = colnorm(W); R is the error-feedback residual (above)
+ *   DION_VARIANT_ORTH          Vbar = orth(W);    R is the error-feedback residual (above)
+ *   DION_VARIANT_LOWRANK_MUON  low-rank Muon, this library's reading of the
+ *       low-rank orthogonalisation abstract quoted on thelatestinai.com
+ *       (2605.16341 listing; the algorithm is not on the pages): R holds Muon's
+ *       momentum and V a fresh Gaussian sketch written by the caller before
+ *       every step; with mu = the descriptor's `beta`,
+ *           M = G + mu R;  U = orth(M V);  W = M^T U;  Vbar = orth(W);
+ *           X <- X - eta s U Vbar^T;  R <- M;  V <- Vbar
+ */
+typedef enum { DION_VARIANT_DION = 0, DION_VARIANT_ORTH = 1, DION_VARIANT_LOWRANK_MUON = 2 } dion_variant_t;
 typedef enum { DION_DTYPE_F32 = 0, DION_DTYPE_BF16 = 1 } dion_dtype_t;
 
 /* One weight matrix and its optimizer state (all device pointers, caller-owned).
@@ -92,7 +104,7 @@ typedef struct {
   int32_t g_dtype;   /* dion_dtype_t */
   int32_t variant;   /* dion_variant_t */
   float eta;         /* learning rate                                             */
-  float beta;        /* error-feedback coefficient                                */
+  float beta;        /* error-feedback coefficient (momentum mu for LOWRANK_MUON)  */
   float scale;       /* s; <= 0 selects sqrt(m / n)                               */
   float reserved;    /* must be 0                                                 */
 } dion_matrix_desc;

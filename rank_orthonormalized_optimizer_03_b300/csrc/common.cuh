@@ -30,6 +30,7 @@ struct MatDev {
   int variant;         // 0 Dion (colnorm), 1 Orth-Dion (QR)
   float eta_s;         // eta * s
   float beta;
+  float mu;            // M = G + mu R (1, or the momentum coefficient of the low-rank Muon variant)
   float* P;            // m x rp   P = M V
   float* U;            // m x rp   U = orth(P)
   float* W;            // n x rp   W = M^T U

@@ -160,7 +160,7 @@ dion_status_t validate(const dion_matrix_desc* d, int count) {
       return fail(DION_ERR_INVALID_ARG, "matrix %d: leading dimension below n", i);
     if (x.g_dtype != DION_DTYPE_F32 && x.g_dtype != DION_DTYPE_BF16)
       return fail(DION_ERR_INVALID_ARG, "matrix %d: unknown g_dtype %d", i, x.g_dtype);
-    if (x.variant != DION_VARIANT_DION && x.variant != DION_VARIANT_ORTH)
+    if (x.variant != DION_VARIANT_DION && x.variant != DION_VARIANT_ORTH && x.variant != DION_VARIANT_LOWRANK_MUON)
       return fail(DION_ERR_INVALID_ARG, "matrix %d: unknown variant %d", i, x.variant);
     if (!std::isfinite(x.eta) || !std::isfinite(x.beta) || !std::isfinite(x.scale))
       return fail(DION_ERR_INVALID_ARG, "matrix %d: non-finite eta / beta / scale", i);
@@ -204,7 +204,7 @@ void layout(dion_plan* p) {
   for (int i = 0; i < cnt; ++i) {
     const auto& d = p->descs[i];
     p->rp[i] = cdiv(d.r, kRankGranule) * kRankGranule;
-    (d.variant == DION_VARIANT_ORTH ? p->orth_idx : p->dion_idx).push_back(i);
+    (d.variant == DION_VARIANT_DION ? p->dion_idx : p->orth_idx).push_back(i);
   }
   // column blocks of the streaming kernels (TMEM holds two slices of bn <= 192 columns)
   p->ncb.resize(cnt); p->bn.resize(cnt); p->ldt_n.resize(cnt); p->ldt_m.resize(cnt);
@@ -648,6 +648,7 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     const float s = d.scale > 0.f ? d.scale : (float)std::sqrt((double)d.m / (double)d.n);
     x.eta_s = d.eta * s;
     x.beta = d.beta;
+    x.mu = d.variant == DION_VARIANT_LOWRANK_MUON ? d.beta : 1.f;
     x.P = reinterpret_cast<float*>(base + p->off_P[i]);
     x.U = reinterpret_cast<float*>(base + p->off_U[i]);
     x.W = reinterpret_cast<float*>(base + p->off_W[i]);
@@ -748,6 +749,11 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     if (!okm) return fail(DION_ERR_CUDA, "matrix %d: cuTensorMapEncodeTiled failed", i);
     e.m = (int)d.m; e.n = (int)d.n; e.rp = (int)rp; e.g_bf16 = x.g_bf16;
     e.eta_s = x.eta_s; e.beta = x.beta; e.status = x.status;
+    // low-rank Muon: M = G + mu R with the descriptor's beta as mu, and R <- M
+    const bool momentum = d.variant == DION_VARIANT_LOWRANK_MUON;
+    e.mu = x.mu;
+    e.gamma = momentum ? 0.f : 1.f;
+    if (momentum) e.beta = 1.f;
   }
   // split jobs: U (workspace, ld rp), Vbar (= V after phase (d), ld r)
   for (int k = 0; k < p->n_split; ++k) {
@@ -790,6 +796,7 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     a.ksplit = 1; a.kchunk = (int)(cdiv(d.n, 32) * 32); a.ncb = p->ncb[i]; a.bn = p->bn[i];
     a.rp = (int)rp; a.gmode = gb ? tcstream::G_BF16 : tcstream::G_F32; a.status = x.status;
     a.pass = -1; a.out_cols = (int)rp;
+    a.mu = x.mu;
     tcstream::SJob& c = sc[i];
     std::memset(&c, 0, sizeof c);
     okm &= make_map(&c.mG, gdt, d.G, d.n, d.m, gpitch, gb ? 64 : 32, tcstream::BK, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -801,6 +808,7 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     c.rows = (int)d.n; c.kdim = (int)d.m; c.ksplit = p->ksplit[i]; c.kchunk = p->kchunk[i];
     c.ncb = p->ncb[i]; c.bn = p->bn[i]; c.rp = (int)rp; c.gmode = gb ? tcstream::G_BF16 : tcstream::G_F32;
     c.status = x.status; c.pass = -1; c.out_cols = (int)rp;
+    c.mu = x.mu;
     if (p->ksplit[i] == 1) {
       // W written whole by this launch: its halves too (else by the reduction)
       c.sh = x.Wh; c.sl = x.Wl; c.hcols = (int)d.r;

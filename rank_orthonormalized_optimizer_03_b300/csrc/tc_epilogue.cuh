@@ -5,6 +5,10 @@
 //     T1 = U Vbar^T,  T2 = U W^T            (K = r, 3xTF32, fp32 accumulation in TMEM)
 //     X <- X - eta s T1,   R <- beta (G + R - T2)
 //
+// (In the momentum form of the low-rank Muon variant M = G + mu R and R <- M:
+// the kernel computes R <- beta (G + mu R - gamma T2) with mu = beta = gamma = 1
+// for Dion and mu = momentum, beta = 1, gamma = 0 for that variant.)
+//
 // The tensor core's fp32 accumulation truncates (its bias grows with the number
 // of accumulation steps, about -1e-5 relative per 1024 of K), and R can be a
 // small difference of large terms.  So one launch accumulates at most KPASS of
@@ -60,7 +64,8 @@ struct EpiMat {
   int m, n, rp, g_bf16;
   float eta_s, beta;
   unsigned* status;
-  int pad[10];
+  float mu, gamma;      // M = G + mu R;  R <- beta (M - gamma U W^T)
+  int pad[8];
 };
 static_assert(sizeof(EpiMat) % 64 == 0, "EpiMat must keep 64-byte alignment of its maps");
 
@@ -220,7 +225,7 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
       if (!named_sync_all(1, 128, ok)) break;
       tc_fence_after();
       const int ns = nsub(e, tl.j0);
-      const float eta_s = e.eta_s, beta = e.beta;
+      const float eta_s = e.eta_s, beta = e.beta, mu = e.mu, gamma = e.gamma;
       for (int sc = 0; sc < ns; ++sc) {
         ok = mbar_wait(&q_full[q], ph, abort_flag);
         if (!ok) failed_mat = tl.mat;
@@ -269,15 +274,15 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
           x.z = fmaf(-eta_s, t1[k + 2], x.z);
           x.w = fmaf(-eta_s, t1[k + 3], x.w);
           if (kpass == 0) {
-            r.x = beta * ((g[k] + r.x) - t2[k]);
-            r.y = beta * ((g[k + 1] + r.y) - t2[k + 1]);
-            r.z = beta * ((g[k + 2] + r.z) - t2[k + 2]);
-            r.w = beta * ((g[k + 3] + r.w) - t2[k + 3]);
+            r.x = beta * (fmaf(mu, r.x, g[k]) - gamma * t2[k]);
+            r.y = beta * (fmaf(mu, r.y, g[k + 1]) - gamma * t2[k + 1]);
+            r.z = beta * (fmaf(mu, r.z, g[k + 2]) - gamma * t2[k + 2]);
+            r.w = beta * (fmaf(mu, r.w, g[k + 3]) - gamma * t2[k + 3]);
           } else {
-            r.x = fmaf(-beta, t2[k], r.x);
-            r.y = fmaf(-beta, t2[k + 1], r.y);
-            r.z = fmaf(-beta, t2[k + 2], r.z);
-            r.w = fmaf(-beta, t2[k + 3], r.w);
+            r.x = fmaf(-beta * gamma, t2[k], r.x);
+            r.y = fmaf(-beta * gamma, t2[k + 1], r.y);
+            r.z = fmaf(-beta * gamma, t2[k + 2], r.z);
+            r.w = fmaf(-beta * gamma, t2[k + 3], r.w);
           }
           *reinterpret_cast<float4*>(rb + off) = r;
           *reinterpret_cast<float4*>(xb + off) = x;

@@ -91,6 +91,7 @@ struct SJob {
   float* tl;
   long long ld_t;
   int hcols;
+  float mu;                       // M = G + mu R: 1 for Dion / Orth-Dion, the momentum coefficient otherwise
 };
 static_assert(sizeof(SJob) % 64 == 0, "SJob must keep 64-byte alignment of its maps");
 
@@ -299,6 +300,7 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
         const unsigned char* rsrc = gsrc + SST_R;
         unsigned char* ahp = ost + os * OST_BYTES;
         unsigned char* alp = ahp + A_BYTES;
+        const float mu = j.mu;                // M = G + mu R (mu = 1: the error-feedback buffer)
         if (!TRANS) {
           // row `row` of M, the chunk's 16 K elements (64-byte rows, 64-byte swizzle)
           float mv[16];
@@ -315,15 +317,18 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
               const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                mv[8 * c + 2 * k] += __uint_as_float(w[k] << 16);
-                mv[8 * c + 2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+                mv[8 * c + 2 * k] = fmaf(mu, mv[8 * c + 2 * k], __uint_as_float(w[k] << 16));
+                mv[8 * c + 2 * k + 1] = fmaf(mu, mv[8 * c + 2 * k + 1], __uint_as_float(w[k] & 0xFFFF0000u));
               }
             }
           } else if (j.gmode == G_F32) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const float4 gv = *reinterpret_cast<const float4*>(gsrc + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
-              mv[4 * c] += gv.x; mv[4 * c + 1] += gv.y; mv[4 * c + 2] += gv.z; mv[4 * c + 3] += gv.w;
+              mv[4 * c] = fmaf(mu, mv[4 * c], gv.x);
+              mv[4 * c + 1] = fmaf(mu, mv[4 * c + 1], gv.y);
+              mv[4 * c + 2] = fmaf(mu, mv[4 * c + 2], gv.z);
+              mv[4 * c + 3] = fmaf(mu, mv[4 * c + 3], gv.w);
             }
           }
 #pragma unroll
@@ -353,13 +358,14 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
             for (int i = 0; i < 16; ++i) {
               const uint16_t gv = *reinterpret_cast<const uint16_t*>(
                   gsrc + gb * 2048 + i * 128 + ((((gj >> 3) ^ i) & 7) << 4) + ((gj & 7) << 1));
-              mv[i] += __uint_as_float((uint32_t)gv << 16);
+              mv[i] = fmaf(mu, mv[i], __uint_as_float((uint32_t)gv << 16));
             }
           } else if (j.gmode == G_F32) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              mv[i] += *reinterpret_cast<const float*>(gsrc + jb * 2048 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4) +
-                                                       ((jj & 3) << 2));
+              mv[i] = fmaf(mu, mv[i],
+                           *reinterpret_cast<const float*>(gsrc + jb * 2048 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4) +
+                                                           ((jj & 3) << 2)));
           }
 #pragma unroll
           for (int c = 0; c < 4; ++c) {

@@ -21,7 +21,7 @@ DION_OK, DION_ERR_INVALID_ARG, DION_ERR_CUDA, DION_ERR_WORKSPACE, DION_ERR_UNSUP
 DION_MAT_OK, DION_MAT_CHOL_BREAKDOWN, DION_MAT_NONFINITE, DION_MAT_TIMEOUT, DION_MAT_SHIFTED = 0, 1, 2, 4, 8
 # bits that mean the matrix was not updated (DION_MAT_SHIFTED is informational)
 FATAL = DION_MAT_CHOL_BREAKDOWN | DION_MAT_NONFINITE | DION_MAT_TIMEOUT
-VARIANT = {"dion": 0, "orth": 1}
+VARIANT = {"dion": 0, "orth": 1, "lowrank_muon": 2}
 DTYPE_F32, DTYPE_BF16 = 0, 1
 BUF_P, BUF_U, BUF_W = 0, 1, 2
 
