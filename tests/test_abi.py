@@ -84,7 +84,7 @@ def test_valid_plan_and_layout(L):
     (dict(m=1 << 31), dion.DION_ERR_INVALID_ARG),      # rows index as int32 on the device
     (dict(ld_x=16), dion.DION_ERR_INVALID_ARG),         # ld < n
     (dict(g_dtype=7), dion.DION_ERR_INVALID_ARG),
-    (dict(variant=2), dion.DION_ERR_INVALID_ARG),
+    (dict(variant=3), dion.DION_ERR_INVALID_ARG),
     (dict(eta=float("inf")), dion.DION_ERR_INVALID_ARG),
     (dict(reserved=1.0), dion.DION_ERR_INVALID_ARG),
     (dict(X=0), dion.DION_ERR_INVALID_ARG),
