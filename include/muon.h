@@ -62,9 +62,27 @@ typedef struct muon_plan muon_plan;
  * Validate `count` descriptors and build a plan (host only).  ns_iters >= 0
  * Newton-Schulz iterations; precision a muon_precision_t.  *workspace_bytes
  * receives the device workspace every step needs.
+ *
+ * row_fraction in (0, 1] selects the Dion3 row-selection variant when below 1
+ * (searcharxiv 2608.11612 "Dion3" abstract: only a fraction of the momentum
+ * matrix's rows is orthogonalised at each step; the rule is not on the pages,
+ * this library's reading): after the momentum update the k = ceil(row_fraction
+ * m) rows of B with the largest Euclidean norms (ties: the lower row index) are
+ * taken, the iteration runs on that k x n block normalised by its own Frobenius
+ * norm, and only those rows of X are updated.  row_fraction = 1 is Muon itself.
+ * The variant needs m <= DION3_MAX_ROWS (DION_ERR_UNSUPPORTED otherwise).
  */
+#define DION3_MAX_ROWS 16384
 DION_API dion_status_t muon_plan_create(const muon_matrix_desc* descs, int32_t count, int32_t ns_iters,
-                                        int32_t precision, size_t* workspace_bytes, muon_plan** out);
+                                        int32_t precision, float row_fraction, size_t* workspace_bytes,
+                                        muon_plan** out);
+
+/*
+ * Rows selected by the last step for matrix `idx` (row-selection variant):
+ * byte offset from the workspace base of k int32 row indices, in increasing
+ * order, and k.  Host only; DION_ERR_INVALID_ARG for a plan without selection.
+ */
+DION_API dion_status_t muon_plan_selected_rows(const muon_plan* plan, int32_t idx, size_t* byte_offset, int64_t* k);
 
 /* One Muon step of every matrix of the plan, enqueued on `stream` (no host sync). */
 DION_API dion_status_t muon_step_batched(muon_plan* plan, void* workspace, size_t ws_bytes, void* stream);

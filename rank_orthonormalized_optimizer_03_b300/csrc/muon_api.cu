@@ -15,6 +15,13 @@
 //     k_add_diag     A <- A + 1.5 I
 //     Y' = A Y  or  Y A                                                  (= 1.5 Y - 0.5 Y Y^T Y)
 //   k_update         X <- X - eta s Y_K
+//
+// Row-selection variant (row_fraction < 1, the Dion3 reading in include/muon.h):
+// k_rownorm (row norms of B, one warp per row, fixed order), k_select (per
+// matrix: bitonic sort of (norm, row) in shared memory, the k largest rows in
+// increasing row order, 1 / Frobenius norm of that block), k_gather (Y_0 = the
+// selected rows / their norm), the same iteration on k x n blocks, and
+// k_update_rows (only the selected rows of X).
 #include "muon.h"
 
 #include <cublas_v2.h>
@@ -45,6 +52,9 @@ struct MuMat {
   const void* G;
   float* B;
   long long m, n, ldx, ldg, ldb;
+  long long kr;        // rows orthogonalised: m, or k of the row-selection variant
+  int* sel;            // row-selection variant: the k selected rows, increasing
+  float* rownorm;      // row-selection variant: sum of squares of each row of B
   void* Y[2];          // this matrix's slot in its group's ping-pong buffers (dense, ld n)
   float* partial;      // per-block partial sums of B^2
   float* inv_norm;     // 1 / ||B||_F
@@ -160,8 +170,127 @@ __global__ void __launch_bounds__(NT) k_update(const MuMat* __restrict__ mats, c
   }
 }
 
+// Sum of squares of every row of every B (one warp per row, fixed order).
+__global__ void __launch_bounds__(NT) k_rownorm(const MuMat* __restrict__ mats, const int* __restrict__ rs, int nmat,
+                                                long long total_rows) {
+  const long long w = ((long long)blockIdx.x * NT + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= total_rows) return;
+  const int j = find_mat(rs, nmat, (int)w);
+  const MuMat& d = mats[j];
+  const long long row = w - rs[j];
+  const float* b = d.B + row * d.ldb;
+  float s = 0.f;
+  for (long long c = lane; c < d.n; c += 32) s = fmaf(b[c], b[c], s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) d.rownorm[row] = s;
+}
+
+// One CTA per matrix: the kr rows with the largest norms (ties: lower row first)
+// by a bitonic sort of (norm, row) in shared memory, written in increasing row
+// order to sel; inv_norm = 1 / sqrt(sum of their squares), summed in row order.
+constexpr int SEL_NT = 1024;
+__global__ void __launch_bounds__(SEL_NT) k_select(const MuMat* __restrict__ mats) {
+  extern __shared__ unsigned char sm[];
+  const MuMat& d = mats[blockIdx.x];
+  int P = 1;
+  while (P < d.m) P <<= 1;
+  float* key = reinterpret_cast<float*>(sm);
+  int* idx = reinterpret_cast<int*>(sm + 4 * (size_t)P);
+  for (int i = threadIdx.x; i < P; i += SEL_NT) {
+    key[i] = i < d.m ? d.rownorm[i] : -1.f;
+    idx[i] = i;
+  }
+  __syncthreads();
+  // descending by key, ascending by row on ties
+  for (int k = 2; k <= P; k <<= 1)
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int i = threadIdx.x; i < P; i += SEL_NT) {
+        const int l = i ^ jj;
+        if (l > i) {
+          const bool first_before = key[i] > key[l] || (key[i] == key[l] && idx[i] < idx[l]);
+          const bool up = (i & k) == 0;
+          if (up != first_before) {
+            const float tk = key[i]; key[i] = key[l]; key[l] = tk;
+            const int ti = idx[i]; idx[i] = idx[l]; idx[l] = ti;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  // the first kr rows, now sorted by row index
+  const int kr = (int)d.kr;
+  int Q = 1;
+  while (Q < kr) Q <<= 1;
+  for (int i = kr + threadIdx.x; i < Q; i += SEL_NT) idx[i] = 0x7fffffff;
+  __syncthreads();
+  for (int k = 2; k <= Q; k <<= 1)
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int i = threadIdx.x; i < Q; i += SEL_NT) {
+        const int l = i ^ jj;
+        if (l > i) {
+          const bool up = (i & k) == 0;
+          if (up == (idx[i] > idx[l])) { const int t = idx[i]; idx[i] = idx[l]; idx[l] = t; }
+        }
+      }
+      __syncthreads();
+    }
+  __shared__ float red[SEL_NT / 32];
+  float acc = 0.f;
+  for (int i = threadIdx.x; i < kr; i += SEL_NT) {
+    d.sel[i] = idx[i];
+    acc += d.rownorm[idx[i]];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < SEL_NT / 32; ++w) t += red[w];
+    *d.inv_norm = t > 0.f ? 1.f / sqrtf(t) : 0.f;
+  }
+}
+
+// Y_0 = the selected rows of B * inv_norm (kr x n, dense).
+__global__ void __launch_bounds__(NT) k_gather(const MuMat* __restrict__ mats, const int* __restrict__ ts, int nmat,
+                                               int bf16) {
+  const int j = find_mat(ts, nmat, blockIdx.x);
+  const MuMat& d = mats[j];
+  const long long lb = blockIdx.x - ts[j];
+  const long long tot = d.kr * d.n;
+  const float s = *d.inv_norm;
+  for (int k = 0; k < EPB / NT; ++k) {
+    const long long e = lb * EPB + (long long)k * NT + threadIdx.x;
+    if (e < tot) {
+      const float y = d.B[(long long)d.sel[e / d.n] * d.ldb + e % d.n] * s;
+      if (bf16) static_cast<__nv_bfloat16*>(d.Y[0])[e] = __float2bfloat16_rn(y);
+      else static_cast<float*>(d.Y[0])[e] = y;
+    }
+  }
+}
+
+// X[sel[i], :] <- X[sel[i], :] - eta s Y_K[i, :].
+__global__ void __launch_bounds__(NT) k_update_rows(const MuMat* __restrict__ mats, const int* __restrict__ ts,
+                                                    int nmat, int which, int bf16) {
+  const int j = find_mat(ts, nmat, blockIdx.x);
+  const MuMat& d = mats[j];
+  const long long lb = blockIdx.x - ts[j];
+  const long long tot = d.kr * d.n;
+  for (int k = 0; k < EPB / NT; ++k) {
+    const long long e = lb * EPB + (long long)k * NT + threadIdx.x;
+    if (e < tot) {
+      const float y = bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(d.Y[which])[e])
+                           : static_cast<const float*>(d.Y[which])[e];
+      float* xp = d.X + (long long)d.sel[e / d.n] * d.ldx + e % d.n;
+      *xp = fmaf(-d.eta_s, y, *xp);
+    }
+  }
+}
+
 struct Group {
-  long long m, n, k;       // shape and the side of the Gram (min(m, n))
+  long long m, n, k;       // shape of the orthogonalised block (kr x n) and the side of its Gram
   std::vector<int> mats;   // plan indices, in order
   size_t off_Y[2], off_A;  // workspace offsets
 };
@@ -171,8 +300,16 @@ struct Group {
 struct muon_plan {
   std::vector<muon_matrix_desc> descs;
   int count = 0, iters = 0, precision = 0;
+  float row_fraction = 1.f;
+  bool select = false;                 // row-selection variant
+  std::vector<long long> kr;           // rows orthogonalised per matrix
   std::vector<Group> groups;
-  std::vector<int> ts;                 // block prefix sums of the streaming kernels
+  std::vector<int> ts;                 // block prefix sums of the streaming kernels (m x n)
+  std::vector<int> ts_sel;             // ... over the selected blocks (kr x n)
+  std::vector<int> rs;                 // row prefix sums (k_rownorm)
+  std::vector<size_t> off_sel, off_rownorm;
+  size_t t_ts_sel = 0, t_rs = 0;
+  int max_rows = 0;
   std::vector<size_t> off_partial;
   size_t off_tables = 0, off_norm = 0, off_cublas = 0, ws_bytes = 0;
   size_t t_mats = 0, t_ts = 0, tables_bytes = 0;
@@ -201,8 +338,11 @@ dion_status_t upload(muon_plan* p, unsigned char* base, cudaStream_t s) {
       MuMat& x = mats[i];
       x.X = d.X; x.G = d.G; x.B = d.B;
       x.m = d.m; x.n = d.n; x.ldx = d.ld_x; x.ldg = d.ld_g; x.ldb = d.ld_b;
+      x.kr = p->kr[i];
+      x.sel = p->select ? reinterpret_cast<int*>(base + p->off_sel[i]) : nullptr;
+      x.rownorm = p->select ? reinterpret_cast<float*>(base + p->off_rownorm[i]) : nullptr;
       for (int b = 0; b < 2; ++b)
-        x.Y[b] = base + gr.off_Y[b] + k * (size_t)(d.m * d.n) * esize(p->precision);
+        x.Y[b] = base + gr.off_Y[b] + k * (size_t)(x.kr * d.n) * esize(p->precision);
       x.partial = reinterpret_cast<float*>(base + p->off_partial[i]);
       x.inv_norm = reinterpret_cast<float*>(base + p->off_norm) + i;
       x.g_bf16 = d.g_dtype == DION_DTYPE_BF16;
@@ -215,6 +355,8 @@ dion_status_t upload(muon_plan* p, unsigned char* base, cudaStream_t s) {
   p->image.assign(p->tables_bytes, 0);
   std::memcpy(p->image.data() + p->t_mats, mats.data(), sizeof(MuMat) * mats.size());
   std::memcpy(p->image.data() + p->t_ts, p->ts.data(), sizeof(int) * p->ts.size());
+  std::memcpy(p->image.data() + p->t_ts_sel, p->ts_sel.data(), sizeof(int) * p->ts_sel.size());
+  std::memcpy(p->image.data() + p->t_rs, p->rs.data(), sizeof(int) * p->rs.size());
   if (cudaMemcpyAsync(base + p->off_tables, p->image.data(), p->image.size(), cudaMemcpyHostToDevice, s) !=
       cudaSuccess)
     return cuda_err("muon table upload");
@@ -227,13 +369,16 @@ dion_status_t upload(muon_plan* p, unsigned char* base, cudaStream_t s) {
 extern "C" {
 
 dion_status_t muon_plan_create(const muon_matrix_desc* descs, int32_t count, int32_t ns_iters, int32_t precision,
-                               size_t* workspace_bytes, muon_plan** out) {
+                               float row_fraction, size_t* workspace_bytes, muon_plan** out) {
   if (!descs || !workspace_bytes || !out) return dion_fail(DION_ERR_INVALID_ARG, "NULL argument");
   *out = nullptr;
   if (count < 1 || count > (1 << 20)) return dion_fail(DION_ERR_INVALID_ARG, "count %d outside [1, 2^20]", count);
   if (ns_iters < 0 || ns_iters > 1000) return dion_fail(DION_ERR_INVALID_ARG, "ns_iters %d outside [0, 1000]", ns_iters);
   if (precision < MUON_NS_BF16 || precision > MUON_NS_FP32)
     return dion_fail(DION_ERR_INVALID_ARG, "unknown precision %d", precision);
+  if (!(row_fraction > 0.f && row_fraction <= 1.f))
+    return dion_fail(DION_ERR_INVALID_ARG, "row_fraction %g outside (0, 1]", (double)row_fraction);
+  long long rows_total = 0;
   for (int i = 0; i < count; ++i) {
     const muon_matrix_desc& d = descs[i];
     if (!d.X || !d.G || !d.B) return dion_fail(DION_ERR_INVALID_ARG, "matrix %d: NULL pointer", i);
@@ -245,16 +390,29 @@ dion_status_t muon_plan_create(const muon_matrix_desc* descs, int32_t count, int
       return dion_fail(DION_ERR_INVALID_ARG, "matrix %d: unknown g_dtype", i);
     if (!std::isfinite(d.eta) || !std::isfinite(d.mu) || !std::isfinite(d.scale))
       return dion_fail(DION_ERR_INVALID_ARG, "matrix %d: non-finite eta / mu / scale", i);
+    if (row_fraction < 1.f && d.m > DION3_MAX_ROWS)
+      return dion_fail(DION_ERR_UNSUPPORTED, "matrix %d: row selection needs m <= %d", i, DION3_MAX_ROWS);
+    rows_total += d.m;
   }
+  if (rows_total >= (1LL << 31)) return dion_fail(DION_ERR_UNSUPPORTED, "more than 2^31 rows in one plan");
   muon_plan* p = new muon_plan();
   p->descs.assign(descs, descs + count);
   p->count = count;
   p->iters = ns_iters;
   p->precision = precision;
-  // groups of equal shape, in order of first appearance
+  p->row_fraction = row_fraction;
+  p->select = row_fraction < 1.f;
+  p->kr.resize(count);
+  for (int i = 0; i < count; ++i) {
+    const long long m = descs[i].m;
+    p->kr[i] = p->select ? std::min<long long>(m, std::max<long long>(1, (long long)std::ceil((double)row_fraction * m)))
+                         : m;
+    p->max_rows = std::max<int>(p->max_rows, (int)m);
+  }
+  // groups of equal orthogonalised shape (kr x n), in order of first appearance
   std::map<std::pair<long long, long long>, int> gid;
   for (int i = 0; i < count; ++i) {
-    const auto key = std::make_pair((long long)descs[i].m, (long long)descs[i].n);
+    const auto key = std::make_pair(p->kr[i], (long long)descs[i].n);
     auto it = gid.find(key);
     if (it == gid.end()) {
       gid[key] = (int)p->groups.size();
@@ -266,12 +424,20 @@ dion_status_t muon_plan_create(const muon_matrix_desc* descs, int32_t count, int
     p->groups[it->second].mats.push_back(i);
   }
   p->ts.assign(count + 1, 0);
-  for (int i = 0; i < count; ++i) p->ts[i + 1] = p->ts[i] + (int)cdiv(descs[i].m * descs[i].n, EPB);
+  p->ts_sel.assign(count + 1, 0);
+  p->rs.assign(count + 1, 0);
+  for (int i = 0; i < count; ++i) {
+    p->ts[i + 1] = p->ts[i] + (int)cdiv(descs[i].m * descs[i].n, EPB);
+    p->ts_sel[i + 1] = p->ts_sel[i] + (int)cdiv(p->kr[i] * descs[i].n, EPB);
+    p->rs[i + 1] = p->rs[i] + (int)descs[i].m;
+  }
   // tables
   size_t off = 0;
   auto take = [&](size_t b) { size_t o = off; off = align_up(off + b, 128); return o; };
   p->t_mats = take(sizeof(MuMat) * count);
   p->t_ts = take(sizeof(int) * (count + 1));
+  p->t_ts_sel = take(sizeof(int) * (count + 1));
+  p->t_rs = take(sizeof(int) * (count + 1));
   p->tables_bytes = off;
   // workspace
   size_t ws = 0;
@@ -280,6 +446,14 @@ dion_status_t muon_plan_create(const muon_matrix_desc* descs, int32_t count, int
   p->off_norm = region(4 * (size_t)count);
   p->off_partial.resize(count);
   for (int i = 0; i < count; ++i) p->off_partial[i] = region(4 * (size_t)(p->ts[i + 1] - p->ts[i]));
+  if (p->select) {
+    p->off_sel.resize(count);
+    p->off_rownorm.resize(count);
+    for (int i = 0; i < count; ++i) {
+      p->off_sel[i] = region(4 * (size_t)p->kr[i]);
+      p->off_rownorm[i] = region(4 * (size_t)descs[i].m);
+    }
+  }
   const size_t es = esize(precision);
   for (Group& g : p->groups) {
     const size_t c = g.mats.size();
@@ -302,8 +476,18 @@ void muon_plan_destroy(muon_plan* plan) {
 
 int32_t muon_plan_launches_per_step(const muon_plan* plan) {
   if (!plan) return -1;
-  // momentum, norm, start, update; per iteration and group two GEMMs and the diagonal
-  return 4 + plan->iters * 3 * (int)plan->groups.size();
+  // momentum, norm, start, update (row selection: momentum, row norms, select, gather,
+  // update); per iteration and group two GEMMs and the diagonal
+  return (plan->select ? 5 : 4) + plan->iters * 3 * (int)plan->groups.size();
+}
+
+dion_status_t muon_plan_selected_rows(const muon_plan* plan, int32_t idx, size_t* byte_offset, int64_t* k) {
+  if (!plan || !byte_offset || !k) return dion_fail(DION_ERR_INVALID_ARG, "NULL argument");
+  if (!plan->select) return dion_fail(DION_ERR_INVALID_ARG, "the plan selects no rows (row_fraction = 1)");
+  if (idx < 0 || idx >= plan->count) return dion_fail(DION_ERR_INVALID_ARG, "index %d outside the plan", idx);
+  *byte_offset = plan->off_sel[idx];
+  *k = plan->kr[idx];
+  return dion_ok();
 }
 
 dion_status_t muon_step_batched(muon_plan* p, void* workspace, size_t ws_bytes, void* stream) {
@@ -315,6 +499,9 @@ dion_status_t muon_step_batched(muon_plan* p, void* workspace, size_t ws_bytes, 
   unsigned char* base = static_cast<unsigned char*>(workspace);
   if (!p->handle) {
     if (cublasCreate(&p->handle) != CUBLAS_STATUS_SUCCESS) return dion_fail(DION_ERR_CUDA, "cublasCreate failed");
+    if (p->select && cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 * DION3_MAX_ROWS) !=
+                         cudaSuccess)
+      return cuda_err("kernel attributes");
   }
   if (p->uploaded_ws != workspace) {
     const dion_status_t st = upload(p, base, s);
@@ -327,9 +514,20 @@ dion_status_t muon_step_batched(muon_plan* p, void* workspace, size_t ws_bytes, 
   const int* ts = reinterpret_cast<const int*>(base + p->off_tables + p->t_ts);
   const int nblk = p->ts[p->count];
   const int bf16 = p->precision == MUON_NS_BF16;
+  const int* ts_sel = reinterpret_cast<const int*>(base + p->off_tables + p->t_ts_sel);
   k_momentum<<<nblk, NT, 0, s>>>(mats, ts, p->count);
-  k_norm<<<p->count, NT, 0, s>>>(mats);
-  k_start<<<nblk, NT, 0, s>>>(mats, ts, p->count, bf16);
+  if (p->select) {
+    const long long rows = p->rs[p->count];
+    k_rownorm<<<(int)cdiv(rows * 32, NT), NT, 0, s>>>(
+        mats, reinterpret_cast<const int*>(base + p->off_tables + p->t_rs), p->count, rows);
+    int P = 1;
+    while (P < p->max_rows) P <<= 1;
+    k_select<<<p->count, SEL_NT, 8 * (size_t)P, s>>>(mats);
+    k_gather<<<p->ts_sel[p->count], NT, 0, s>>>(mats, ts_sel, p->count, bf16);
+  } else {
+    k_norm<<<p->count, NT, 0, s>>>(mats);
+    k_start<<<nblk, NT, 0, s>>>(mats, ts, p->count, bf16);
+  }
   dion_status_t st = cuda_err("muon launch");
   if (st) return st;
   const cudaDataType_t dt = bf16 ? CUDA_R_16BF : CUDA_R_32F;
@@ -368,7 +566,10 @@ dion_status_t muon_step_batched(muon_plan* p, void* workspace, size_t ws_bytes, 
         return dion_fail(DION_ERR_CUDA, "cuBLAS GEMM failed (%d, %d)", (int)r1, (int)r2);
     }
   }
-  k_update<<<nblk, NT, 0, s>>>(mats, ts, p->count, p->iters & 1, bf16);
+  if (p->select)
+    k_update_rows<<<p->ts_sel[p->count], NT, 0, s>>>(mats, ts_sel, p->count, p->iters & 1, bf16);
+  else
+    k_update<<<nblk, NT, 0, s>>>(mats, ts, p->count, p->iters & 1, bf16);
   st = cuda_err("muon launch");
   if (st) return st;
   return dion_ok();

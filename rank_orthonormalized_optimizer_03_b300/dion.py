@@ -81,7 +81,9 @@ def _declare(L):
         "dion_orth_noalloc": (I32, [P, I64, I64, I64, P, I64, ctypes.POINTER(ctypes.c_uint32), P]),
         "dion_shard_stage": (I32, [P, P, SZ, I32, P]),
         "dion_plan_exchange": (I32, [P, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
-        "muon_plan_create": (I32, [ctypes.POINTER(MuonDesc), I32, I32, I32, ctypes.POINTER(SZ), ctypes.POINTER(P)]),
+        "muon_plan_create": (I32, [ctypes.POINTER(MuonDesc), I32, I32, I32, F, ctypes.POINTER(SZ),
+                                   ctypes.POINTER(P)]),
+        "muon_plan_selected_rows": (I32, [P, I32, ctypes.POINTER(SZ), ctypes.POINTER(I64)]),
         "muon_step_batched": (I32, [P, P, SZ, P]),
         "muon_plan_launches_per_step": (I32, [P]),
         "muon_plan_destroy": (None, [P]),
@@ -291,9 +293,12 @@ class MuonPlan:
     caller; X and the momentum B are float32 and updated in place, G float32 or
     bfloat16) and eta, mu, optional scale (<= 0 or missing: sqrt(m/n)).
     ``iters`` Newton-Schulz iterations in ``precision`` "bf16" | "tf32" | "fp32".
+    ``row_fraction`` < 1 selects the Dion3 row-selection variant (only the
+    ceil(row_fraction m) rows of largest norm are orthogonalised and updated).
     """
 
-    def __init__(self, mats: Sequence[dict], iters: int = 5, precision: str = "bf16", workspace=None):
+    def __init__(self, mats: Sequence[dict], iters: int = 5, precision: str = "bf16", workspace=None,
+                 row_fraction: float = 1.0):
         import torch
         L = lib()
         if len(mats) == 0:
@@ -319,8 +324,8 @@ class MuonPlan:
         self._descs = (MuonDesc * len(descs))(*descs)
         ws = ctypes.c_size_t(0)
         plan = ctypes.c_void_p()
-        check(L.muon_plan_create(self._descs, len(descs), int(iters), MUON_PRECISION[precision], ctypes.byref(ws),
-                                 ctypes.byref(plan)), "muon_plan_create")
+        check(L.muon_plan_create(self._descs, len(descs), int(iters), MUON_PRECISION[precision],
+                                 float(row_fraction), ctypes.byref(ws), ctypes.byref(plan)), "muon_plan_create")
         self._plan = plan
         self.ws_bytes = ws.value
         if workspace is None:
@@ -332,6 +337,14 @@ class MuonPlan:
     @property
     def launches_per_step(self) -> int:
         return lib().muon_plan_launches_per_step(self._plan)
+
+    def selected_rows(self, idx: int):
+        """int32 view of the rows of matrix idx that the last step selected (row-selection variant)."""
+        import torch
+        off, k = ctypes.c_size_t(), ctypes.c_int64()
+        check(lib().muon_plan_selected_rows(self._plan, idx, ctypes.byref(off), ctypes.byref(k)),
+              "muon_plan_selected_rows")
+        return self.workspace[off.value: off.value + 4 * k.value].view(torch.int32)
 
     def step(self, stream=None):
         check(lib().muon_step_batched(self._plan, self.workspace.data_ptr(), self.ws_bytes, _stream_ptr(stream)),

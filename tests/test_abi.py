@@ -180,11 +180,11 @@ def muon_desc(k, m=64, n=32, **kw):
     return dion.MuonDesc(**d)
 
 
-def muon_create(L, descs, iters=5, precision=0):
+def muon_create(L, descs, iters=5, precision=0, row_fraction=1.0):
     arr = (dion.MuonDesc * len(descs))(*descs)
     ws = ctypes.c_size_t(0)
     plan = ctypes.c_void_p()
-    code = L.muon_plan_create(arr, len(descs), iters, precision, ctypes.byref(ws), ctypes.byref(plan))
+    code = L.muon_plan_create(arr, len(descs), iters, precision, row_fraction, ctypes.byref(ws), ctypes.byref(plan))
     return code, ws.value, plan
 
 
@@ -205,3 +205,22 @@ def test_muon_plan_groups_shapes_and_validates(L):
         code, _, _ = muon_create(L, [muon_desc(0, **kw)])
         assert code == dion.DION_ERR_INVALID_ARG, kw
     L.muon_plan_destroy(None)
+
+
+def test_row_selection_plan(L):
+    descs = [muon_desc(0, m=100, n=32), muon_desc(1, m=64, n=32)]
+    code, ws, plan = muon_create(L, descs, iters=3, row_fraction=0.25)
+    assert code == dion.DION_OK, L.dion_last_error()
+    # k = ceil(0.25 m): 25 and 16 rows -> two groups (25 x 32, 16 x 32)
+    assert L.muon_plan_launches_per_step(plan) == 5 + 3 * 3 * 2
+    off, k = ctypes.c_size_t(), ctypes.c_int64()
+    assert L.muon_plan_selected_rows(plan, 0, ctypes.byref(off), ctypes.byref(k)) == dion.DION_OK and k.value == 25
+    assert L.muon_plan_selected_rows(plan, 1, ctypes.byref(off), ctypes.byref(k)) == dion.DION_OK and k.value == 16
+    assert L.muon_plan_selected_rows(plan, 2, ctypes.byref(off), ctypes.byref(k)) == dion.DION_ERR_INVALID_ARG
+    L.muon_plan_destroy(plan)
+    for rf in (0.0, 1.5, float("nan")):
+        assert muon_create(L, descs, row_fraction=rf)[0] == dion.DION_ERR_INVALID_ARG, rf
+    assert muon_create(L, [muon_desc(0, m=20000, n=32)], row_fraction=0.5)[0] == dion.DION_ERR_UNSUPPORTED
+    code, _, plan = muon_create(L, descs)
+    assert L.muon_plan_selected_rows(plan, 0, ctypes.byref(off), ctypes.byref(k)) == dion.DION_ERR_INVALID_ARG
+    L.muon_plan_destroy(plan)
