@@ -70,7 +70,7 @@ enum {
   DION_MAT_OK = 0,
   DION_MAT_CHOL_BREAKDOWN = 1,  /* orth(): non-positive Cholesky pivot (rank-deficient argument) */
   DION_MAT_NONFINITE = 2,       /* orth(): non-finite value met (NaN / Inf in the inputs)        */
-  DION_MAT_TIMEOUT = 4,         /* a pipeline wait inside a tensor-core kernel gave up after 2 s;
+  DION_MAT_TIMEOUT = 4,         /* a pipeline wait inside a tensor-core kernel gave up (after 2 s);
                                    the kernel returned early and this matrix's update is incomplete */
   DION_MAT_SHIFTED = 8          /* informational: an orth() of this matrix was ill conditioned
                                    (kappa > ~1e3) and took shifted CholeskyQR3; the update is complete */
@@ -220,6 +220,19 @@ DION_API int32_t dion_plan_launches_per_step(const dion_plan* plan);
 enum { DION_EXCHANGE_GRAM = 0, DION_EXCHANGE_W = 1 };
 DION_API dion_status_t dion_shard_stage(dion_plan* plan, void* workspace, size_t ws_bytes, int32_t stage,
                                         void* stream);
+
+/*
+ * Testing hook for the bounded waits (no counterpart on the pages).  Sets, on
+ * `stream`, the limit after which every pipeline wait of the tensor-core
+ * kernels gives up (limit_ns <= 0 restores the default of 2 s), and makes the
+ * update kernel's operand producer stop issuing at the first tile of plan
+ * matrix `withhold_matrix` (-1: off), so that a consumer's wait on it runs
+ * out: the kernel raises its abort flag, drains its own copies, frees its
+ * TMEM, returns, and marks DION_MAT_TIMEOUT on every matrix the aborting CTA
+ * had work for.  Both settings are process-wide for the current device and
+ * stay until changed; for tests only.
+ */
+DION_API dion_status_t dion_debug_expire_wait(int64_t limit_ns, int32_t withhold_matrix, void* stream);
 
 /* Byte offset from the workspace base and size of exchange region `which`
  * (DION_EXCHANGE_GRAM: the matrices' rp x rp fp32 Grams back to back; DION_EXCHANGE_W:

@@ -1397,6 +1397,17 @@ int32_t dion_plan_launches_per_step(const dion_plan* plan) {
   return n;
 }
 
+dion_status_t dion_debug_expire_wait(int64_t limit_ns, int32_t withhold_matrix, void* stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const unsigned long long lim = limit_ns > 0 ? (unsigned long long)limit_ns : tc::kWaitNs;
+  const int wm = withhold_matrix >= 0 ? withhold_matrix : -1;
+  if (cudaMemcpyToSymbolAsync(tc::g_wait_limit_ns, &lim, sizeof lim, 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyToSymbolAsync(tcepi::g_withhold_epi_matrix, &wm, sizeof wm, 0, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess)
+    return cuda_check("debug hook");
+  return ok();
+}
+
 dion_status_t dion_shard_stage(dion_plan* plan, void* workspace, size_t ws_bytes, int32_t stage, void* stream) {
   return run_shard_stage(plan, workspace, ws_bytes, stage, stream);
 }

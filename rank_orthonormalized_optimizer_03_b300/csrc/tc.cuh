@@ -2,9 +2,10 @@
 // waits, TMA tile loads/stores, and the 5th-generation tensor core (tcgen05:
 // TMEM allocation, MMA from shared-memory descriptors, commit, TMEM loads).
 //
-// Every wait here gives up after kWaitNs of wall time (the global timer), sets
-// a shared abort flag and reports failure to its caller, so that no kernel of
-// this library can spin forever; callers turn that into a status bit.
+// Every wait here gives up after g_wait_limit_ns of wall time (the global timer,
+// 2 s by default), sets a shared abort flag and reports failure to its caller, so
+// that no kernel of this library can spin forever; callers turn that into a
+// status bit.
 #pragma once
 
 #include <cuda.h>
@@ -15,6 +16,10 @@ namespace dion {
 namespace tc {
 
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s: any legitimate wait is microseconds
+
+// Limit of every bounded wait of the tensor-core kernels (ns): kWaitNs, unless a
+// test lowers it through dion_debug_expire_wait() to make a wait run out quickly.
+static __device__ unsigned long long g_wait_limit_ns = kWaitNs;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,7 +62,7 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity of `bar` has completed.
-// Returns false (and raises *abort) after kWaitNs, or at once if *abort is set.
+// Returns false (and raises *abort) after g_wait_limit_ns, or at once if *abort is set.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
@@ -65,7 +70,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_test(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitNs) {
+      if (global_ns() - t0 > g_wait_limit_ns) {
         *abort = 1;
         return false;
       }
@@ -85,7 +90,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   const unsigned long long t0 = global_ns();
   while (!mbar_test(bar, parity))
-    if (global_ns() - t0 > kWaitNs) return false;
+    if (global_ns() - t0 > g_wait_limit_ns) return false;
   return true;
 }
 

@@ -77,6 +77,10 @@ struct Tile {
 
 __device__ __forceinline__ bool skip(const EpiMat& e) { return (*e.status & ST_FATAL) != 0; }
 
+// Testing hook (dion_debug_expire_wait): the operand producer stops issuing at the
+// first tile of this matrix, so that the MMA issuer's wait on it runs out (-1: off).
+static __device__ int g_withhold_epi_matrix = -1;
+
 __device__ __forceinline__ int nsub(const EpiMat& e, int j0) {
   const int left = e.n - j0;
   return left >= BNJ ? BNJ / SUB : (left + SUB - 1) / SUB;
@@ -127,6 +131,7 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
       const Tile tl = tiles[t];
       const EpiMat& e = mats[tl.mat];
       if (skip(e) || kc0 * BK >= e.rp) continue;
+      if (tl.mat == g_withhold_epi_matrix) goto prod_done;
       const int kc1 = min((e.rp + BK - 1) / BK, kc0 + KPASS / BK);
       for (int kc = kc0; kc < kc1; ++kc) {
         if (!mbar_wait(&op_empty[s], ph ^ 1, abort_flag)) { failed_mat = tl.mat; goto prod_done; }
@@ -317,6 +322,9 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
   __syncthreads();
   if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, TMEM_COLS); }
   if (failed_mat >= 0) atomicOr(mats[failed_mat].status, ST_TIMEOUT);
+  // after an abort this CTA left tiles unfinished: every matrix it had tiles of is incomplete
+  if (threadIdx.x == 0 && *abort_flag)
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) atomicOr(mats[tiles[t].mat].status, ST_TIMEOUT);
 }
 
 }  // namespace tcepi

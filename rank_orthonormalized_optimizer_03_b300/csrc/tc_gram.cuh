@@ -234,6 +234,9 @@ k_gram(const GJob* __restrict__ jobs, const GItem* __restrict__ items, int nitem
   __syncthreads();
   if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, TMEM_COLS); }
   if (failed >= 0) atomicOr(jobs[failed].status, ST_TIMEOUT);
+  // after an abort this CTA left items unfinished: every job it had items of is incomplete
+  if (threadIdx.x == 0 && *abort_flag)
+    for (int t = blockIdx.x; t < nitems; t += gridDim.x) atomicOr(jobs[items[t].job].status, ST_TIMEOUT);
 }
 
 }  // namespace tcgram

@@ -79,6 +79,7 @@ def _declare(L):
         "dion_plan_get_status": (I32, [P, P, SZ, ctypes.POINTER(ctypes.c_uint32), P]),
         "dion_plan_launches_per_step": (I32, [P]),
         "dion_orth_noalloc": (I32, [P, I64, I64, I64, P, I64, ctypes.POINTER(ctypes.c_uint32), P]),
+        "dion_debug_expire_wait": (I32, [I64, I32, P]),
         "dion_shard_stage": (I32, [P, P, SZ, I32, P]),
         "dion_plan_exchange": (I32, [P, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
         "muon_plan_create": (I32, [ctypes.POINTER(MuonDesc), I32, I32, I32, F, ctypes.POINTER(SZ),
@@ -164,6 +165,14 @@ def make_desc(X, G, R, V, eta, beta, variant="orth", scale=0.0) -> MatrixDesc:
         X.stride(0), G.stride(0), R.stride(0),
         DTYPE_BF16 if G.dtype == torch.bfloat16 else DTYPE_F32, VARIANT[variant],
         float(eta), float(beta), float(scale), 0.0)
+
+
+def debug_expire_wait(limit_ns: int = 0, withhold_matrix: int = -1, stream=None):
+    """Testing hook of the bounded waits (dion_debug_expire_wait): wait limit in ns
+    (<= 0: the 2 s default) and the plan matrix whose update operands the update
+    kernel withholds (-1: none).  Process-wide; reset with debug_expire_wait()."""
+    check(lib().dion_debug_expire_wait(int(limit_ns), int(withhold_matrix), _stream_ptr(stream)),
+          "dion_debug_expire_wait")
 
 
 NOALLOC_MAX_ROWS, NOALLOC_MAX_RANK = 8192, 64
