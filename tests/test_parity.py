@@ -153,19 +153,20 @@ def test_gpt160m_chain_10_steps(dev, variant):
     plan.close()
 
 
-def ill_conditioned_case(m, n, r, kappa, seed):
-    """A matrix whose warm-started P = M V has condition number ~kappa: M's top-r
-    singular values fall geometrically from 1 to 1/kappa above a noise floor of
-    0.05 in the remaining directions, and V spans the top-r right singular
-    vectors.  The gradient is fp32 (bf16 rounding would bury the smallest
-    singular values)."""
+def ill_conditioned_case(m, n, r, eps, seed):
+    """A step whose P = M V is ill conditioned (kappa ~ 8e3 for eps = 1e-2) through the warm start:
+    V is orthonormal except that its second column is the first one plus eps times
+    a unit vector orthogonal to it, so P's first two columns are nearly parallel
+    while M itself is an ordinary gradient (rank-4 signal plus noise).  span(P)
+    stays well determined, so the fp32 result can match the float64 oracle to
+    kappa(P) u.  (A P made ill conditioned by M's own spectrum instead -- singular
+    values falling below M's noise floor -- leaves W = M^T U ill determined in
+    fp32 whatever the algorithm.)"""
     g = np.random.Generator(np.random.PCG64(seed))
-    Ua, _ = np.linalg.qr(g.standard_normal((m, n)))
-    Vb, _ = np.linalg.qr(g.standard_normal((n, n)))
-    s = np.concatenate([np.geomspace(1.0, 1.0 / kappa, r), np.full(n - r, 0.05)])
-    M = (Ua * s[None, :]) @ Vb.T
-    V = Vb[:, :r]
-    return M.astype(np.float32), V.astype(np.float32), g.normal(0, 0.02, (m, n)).astype(np.float32)
+    G = (g.standard_normal((m, 4)) @ g.standard_normal((4, n)) + 0.1 * g.standard_normal((m, n)))
+    V, _ = np.linalg.qr(g.standard_normal((n, r)))
+    V[:, 1] = V[:, 0] + eps * V[:, 1]
+    return G.astype(np.float32), V.astype(np.float32), g.normal(0, 0.02, (m, n)).astype(np.float32)
 
 
 @pytest.mark.parametrize("variant", ["orth", "dion"])
@@ -173,11 +174,12 @@ def test_shifted_choleskyqr3_on_ill_conditioned_p(dev, variant):
     """kappa(P) ~ 1e4 is beyond fp32 CholeskyQR2 (kappa^2 u ~ 6): the first
     Cholesky's pivots must send orth() down the shifted CholeskyQR3 branch,
     which reports DION_MAT_SHIFTED and still returns the positive-diagonal Q
-    factor; X, R, the update and Vbar against the oracle.  For Orth-Dion,
-    W = M^T U is as ill conditioned and takes the same branch."""
+    factor; X, R, the update and Vbar against the oracle.  For Dion, phase (a)
+    first orthonormalises the warm start (orth(M V) = orth(M orth(V))), and it is
+    that orth(V) which takes the shifted branch."""
     import torch
     m, n, r = 1024, 512, 32
-    G, V, X = ill_conditioned_case(m, n, r, 1e4, seed=31)
+    G, V, X = ill_conditioned_case(m, n, r, 1e-2, seed=31)
     d = dict(X=to_dev(X, dev), G=to_dev(G, dev), R=torch.zeros((m, n), device=dev), V=to_dev(V, dev),
              eta=0.02, beta=0.95, variant=variant)
     # a well-conditioned neighbour in the same plan must take the ordinary path
