@@ -21,6 +21,7 @@
 #include "tc_split.cuh"
 #include "tc_stream.cuh"
 #include "tc_gram.cuh"
+#include "bchol.cuh"
 
 using namespace dion;
 
@@ -119,7 +120,15 @@ struct dion_plan {
   size_t t_sj_a = 0, t_sj_c = 0, t_tj_v = 0, t_tj_u = 0, t_ts_tv = 0, t_ts_tu = 0;
   std::vector<int> ts_tv, ts_tu;
   // tensor-core orth(): per list (0 = P, 1 = W, 2 = V) and pass, Gram and A T jobs
-  bool tc_orth = false;
+  bool tc_orth = true;
+  // ranks above 192: Gram by the streaming kernel (transposed mode, K split over rows),
+  // blocked Cholesky + inverse, T^T halves by the transposed split
+  bool big_orth = false;
+  std::vector<int> gks[3], gkc[3];                 // per list and job: K split and chunk of the Gram
+  std::vector<tcstream::Item> it_gs[3];            // Gram work items per list
+  size_t t_gsj[3][3] = {}, t_it_gs[3] = {}, t_atj[3] = {}, t_ts_atj[3] = {}, t_ttj[3] = {}, t_ts_ttj[3] = {};
+  std::vector<int> ts_atj[3], ts_ttj[3];
+  long long rmax_l[3] = {0, 0, 0};                 // largest rank of each list
   bool any_g_f32 = false;   // a gradient in fp32: larger staging slots
   std::vector<size_t> off_Tth, off_Ttl;
   size_t t_gj[3][3] = {}, t_tj[3][3] = {};
@@ -229,25 +238,54 @@ void layout(dion_plan* p) {
     p->ksplit[i] = (int)cdiv(m, ch);
     if (p->ksplit[i] > 1) p->any_split = true;
   }
-  auto chunks = [](long long rows, int* nch, int* ch) {
-    long long n = std::min<long long>(32, std::max<long long>(1, cdiv(rows, 512)));
-    long long c = cdiv(cdiv(rows, n), 64) * 64;
-    *ch = (int)c;
-    *nch = (int)cdiv(rows, c);
-  };
   p->any_g_f32 = false;
   for (int i = 0; i < cnt; ++i) p->any_g_f32 = p->any_g_f32 || p->descs[i].g_dtype == DION_DTYPE_F32;
   p->tc_orth = true;
-  for (int i = 0; i < cnt; ++i) p->tc_orth = p->tc_orth && p->rp[i] <= tcgram::RP_MAX;
+  p->big_orth = false;
+  for (int i = 0; i < cnt; ++i) p->big_orth = p->big_orth || p->rp[i] > tcgram::RP_MAX;
   for (int i = 0; i < cnt; ++i) {
-    if (p->tc_orth) {
-      // tensor-core Gram: one partial per 256 rows
-      p->chunk_p[i] = p->chunk_w[i] = tcgram::CHUNK_ROWS;
-      p->nchunk_p[i] = (int)cdiv(p->descs[i].m, tcgram::CHUNK_ROWS);
-      p->nchunk_w[i] = (int)cdiv(p->descs[i].n, tcgram::CHUNK_ROWS);
-    } else {
-      chunks(p->descs[i].m, &p->nchunk_p[i], &p->chunk_p[i]);
-      chunks(p->descs[i].n, &p->nchunk_w[i], &p->chunk_w[i]);
+    // tensor-core Gram of ranks <= 192: one partial per 256 rows
+    p->chunk_p[i] = p->chunk_w[i] = tcgram::CHUNK_ROWS;
+    p->nchunk_p[i] = (int)cdiv(p->descs[i].m, tcgram::CHUNK_ROWS);
+    p->nchunk_w[i] = (int)cdiv(p->descs[i].n, tcgram::CHUNK_ROWS);
+  }
+  {
+    const std::vector<int>* lists[3] = {nullptr, &p->orth_idx, &p->dion_idx};
+    for (int L = 0; L < 3; ++L) {
+      const size_t nj = L == 0 ? (size_t)cnt : lists[L]->size();
+      auto mat = [&](size_t k) { return L == 0 ? (int)k : (*lists[L])[k]; };
+      p->rmax_l[L] = 0;
+      for (size_t k = 0; k < nj; ++k) p->rmax_l[L] = std::max<long long>(p->rmax_l[L], p->descs[mat(k)].r);
+      p->gks[L].assign(nj, 1);
+      p->gkc[L].assign(nj, 0);
+      p->it_gs[L].clear();
+      if (!p->big_orth) continue;
+      // Gram by the streaming kernel: output rows rp (128-row tiles) x column blocks, the
+      // rows of the factor as K, split into ranges of at most 2048 until the GPU is full
+      long long items = 0;
+      for (size_t k = 0; k < nj; ++k) items += cdiv(p->rp[mat(k)], tcstream::BM) * p->ncb[mat(k)];
+      const long long want = 2LL * 148;
+      const long long split = items >= want ? 1 : cdiv(want, std::max<long long>(1, items));
+      for (size_t k = 0; k < nj; ++k) {
+        const int i = mat(k);
+        const long long rows = L == 0 ? p->descs[i].m : p->descs[i].n;
+        long long ch = cdiv(cdiv(rows, split), 256) * 256;
+        ch = std::min<long long>(ch, 2048);
+        ch = std::min<long long>(ch, cdiv(rows, 32) * 32);
+        p->gkc[L][k] = (int)ch;
+        p->gks[L][k] = (int)cdiv(rows, ch);
+        (L == 0 ? p->nchunk_p[i] : p->nchunk_w[i]) = p->gks[L][k];
+        (L == 0 ? p->chunk_p[i] : p->chunk_w[i]) = (int)ch;
+        for (long long r0 = 0; r0 < p->rp[i]; r0 += tcstream::BM)
+          for (int ks = 0; ks < p->gks[L][k]; ++ks)
+            for (int cb = 0; cb < p->ncb[i]; ++cb) {
+              const long long k0 = (long long)ks * ch, k1 = std::min<long long>(rows, k0 + ch);
+              p->it_gs[L].push_back(tcstream::Item{(int)k, (int)r0, ks, cb * p->bn[i], (int)k0,
+                                                   (int)cdiv(k1 - k0, tcstream::BK), 0, 0});
+            }
+      }
+      std::stable_sort(p->it_gs[L].begin(), p->it_gs[L].end(), [](const tcstream::Item& a, const tcstream::Item& b) {
+        return a.nk > b.nk; });
     }
   }
 
@@ -275,10 +313,8 @@ void layout(dion_plan* p) {
   // tf32 halves for the update: the tensor-core orth() writes those of U and of an
   // Orth-Dion Vbar itself, phase (c) those of W; the rest come from k_split
   p->split_list.clear();
-  for (int i = 0; i < cnt; ++i) {
-    if (!p->tc_orth) p->split_list.push_back({i, 0});
-    if (!p->tc_orth || D(i).variant == DION_VARIANT_DION) p->split_list.push_back({i, 1});
-  }
+  for (int i = 0; i < cnt; ++i)
+    if (D(i).variant == DION_VARIANT_DION) p->split_list.push_back({i, 1});
   p->n_split = (int)p->split_list.size();
   {
     std::vector<int> jobs(p->n_split);
@@ -383,6 +419,20 @@ void layout(dion_plan* p) {
       std::stable_sort(p->chol_order[L].begin(), p->chol_order[L].end(), [&](int a, int b) {
         return D((*lists[L])[a]).r > D((*lists[L])[b]).r; });
       p->t_chol_order[L] = take(4 * std::max<size_t>(1, nj));
+    }
+    // ranks above 192: Gram jobs and items, transposed splits of A (pass 0) and of T
+    for (int L = 0; L < 3; ++L) {
+      const size_t nj = std::max<size_t>(1, lists[L]->size());
+      for (int ps = 0; ps < 3; ++ps) p->t_gsj[L][ps] = take(sizeof(tcstream::SJob) * nj);
+      p->t_it_gs[L] = take(sizeof(tcstream::Item) * std::max<size_t>(1, p->it_gs[L].size()));
+      p->t_atj[L] = take(sizeof(tcsplit::TJob) * nj);
+      p->t_ttj[L] = take(sizeof(tcsplit::TJob) * nj);
+      prefix(p->ts_atj[L], *lists[L], [&](int i) {
+        const long long rows = L == 0 ? D(i).m : D(i).n;
+        return cdiv(rows, 32) * cdiv(p->rp[i], 32); });
+      prefix(p->ts_ttj[L], *lists[L], [&](int i) { return cdiv(p->rp[i], 32) * cdiv(p->rp[i], 32); });
+      p->t_ts_atj[L] = take(4 * p->ts_atj[L].size());
+      p->t_ts_ttj[L] = take(4 * p->ts_ttj[L].size());
     }
   }
   p->t_sj_a = take(sizeof(tcstream::SJob) * cnt);
@@ -598,6 +648,30 @@ std::string verify_tables(const dion_plan* p) {
       }
     }
   }
+  // Gram items of ranks above 192 (streaming kernel, transposed mode): rows rp in
+  // tiles of 128 x K ranges x column blocks, every K range on a multiple of 256 rows
+  for (int L = 0; L < 3 && p->big_orth; ++L) {
+    const std::vector<int>* lists[3] = {nullptr, &p->orth_idx, &p->dion_idx};
+    const size_t nj = L == 0 ? (size_t)cnt : lists[L]->size();
+    auto mat = [&](size_t k) { return L == 0 ? (int)k : (*lists[L])[k]; };
+    std::vector<std::vector<int>> seen(nj);
+    for (size_t k = 0; k < nj; ++k)
+      seen[k].assign(cdiv(p->rp[mat(k)], tcstream::BM) * p->gks[L][k] * p->ncb[mat(k)], 0);
+    for (const auto& it : p->it_gs[L]) {
+      if (it.job < 0 || (size_t)it.job >= nj) return bad("Gram item of an unknown job", it.job);
+      const int i = mat(it.job);
+      const long long rows = L == 0 ? p->descs[i].m : p->descs[i].n;
+      const int ks = it.ks, ch = p->gkc[L][it.job];
+      if (it.row0 % tcstream::BM || it.row0 >= p->rp[i] || it.c0 % p->bn[i] || it.c0 >= p->rp[i] || ks < 0 ||
+          ks >= p->gks[L][it.job] || it.k0 != (long long)ks * ch || it.k0 % 256 ||
+          (long long)it.nk != cdiv(std::min<long long>(rows, (long long)it.k0 + ch) - it.k0, tcstream::BK))
+        return bad("Gram item out of range", i);
+      if (++seen[it.job][((it.row0 / tcstream::BM) * p->gks[L][it.job] + ks) * p->ncb[i] + it.c0 / p->bn[i]] != 1)
+        return bad("Gram tile covered twice", i);
+    }
+    for (size_t k = 0; k < nj; ++k)
+      for (int v : seen[k]) if (v != 1) return bad("Gram tile not covered", mat(k));
+  }
   // (e): every K pass covers the m x n tiles of exactly the matrices with rp > KPASS * pass
   for (size_t k = 0; k < p->it_epi.size(); ++k) {
     std::vector<std::vector<int>> seen(cnt);
@@ -668,8 +742,8 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
       o.gsum = o.gpart;
       o.S = reinterpret_cast<float*>(base + p->off_S[i]);
       o.T = reinterpret_cast<float*>(base + p->off_T[i]);
-      o.Tt_hi = p->tc_orth ? reinterpret_cast<float*>(base + p->off_Tth[i]) : nullptr;
-      o.Tt_lo = p->tc_orth ? reinterpret_cast<float*>(base + p->off_Ttl[i]) : nullptr;
+      o.Tt_hi = reinterpret_cast<float*>(base + p->off_Tth[i]);
+      o.Tt_lo = reinterpret_cast<float*>(base + p->off_Ttl[i]);
       o.rows = rows; o.r = x.r; o.rp = x.rp;
       o.nchunk = nch; o.chunk = ch;
       o.status = x.status;
@@ -695,7 +769,7 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     OrthJob& o = jv[k];
     o = jp[i];
     o.gsum = o.gpart;
-    o.A = p->tc_orth ? x.Vin : x.V; o.lda = p->tc_orth ? x.rp : x.r; o.rows = x.n;
+    o.A = x.Vin; o.lda = x.rp; o.rows = x.n;
     o.out = const_cast<float*>(x.Vin); o.ldo = x.rp; o.out_cols = x.rp;
     o.nchunk = p->nchunk_w[i]; o.chunk = p->chunk_w[i];
     o.flag = status + 3 * cnt + i;
@@ -854,17 +928,73 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
             t.tl = reinterpret_cast<float*>(base + p->off_UTl[i]);
             t.ld_t = p->ldt_m[i];
             t.hcols = (int)p->descs[i].r;
-          } else if (L == 1) {
-            // Orth-Dion Vbar: halves for the update
-            t.sh = reinterpret_cast<float*>(base + p->off_Vh[i]);
-            t.sl = reinterpret_cast<float*>(base + p->off_Vl[i]);
-            t.hcols = (int)p->descs[i].r;
+            t.tr_fin = 1;
+            t.tr_inter = p->big_orth;
+          } else {
+            if (L == 1) {
+              // Orth-Dion Vbar: halves for the update
+              t.sh = reinterpret_cast<float*>(base + p->off_Vh[i]);
+              t.sl = reinterpret_cast<float*>(base + p->off_Vl[i]);
+              t.hcols = (int)p->descs[i].r;
+            }
+            if (p->big_orth) {
+              // transposed halves of the intermediate factors, read by the next pass's
+              // Gram: V^T's halves buffers are free while W and V are orthonormalised
+              t.th = reinterpret_cast<float*>(base + p->off_VTh[i]);
+              t.tl = reinterpret_cast<float*>(base + p->off_VTl[i]);
+              t.ld_t = p->ldt_n[i];
+              t.hcols = (int)p->descs[i].r;
+              t.tr_fin = 0;
+              t.tr_inter = 1;
+            }
           }
         }
         put(p->image, p->t_gj[L][ps], gj.data(), gj.size());
         put(p->image, p->t_tj[L][ps], tj.data(), tj.size());
       }
       put(p->image, p->t_ts_gred[L], p->ts_gred[L].data(), p->ts_gred[L].size());
+    }
+    // ranks above 192: Gram jobs of the streaming kernel (transposed mode: output rows
+    // = the factor's columns, K = its rows, B = its transposed halves), the split of
+    // the pass-0 argument into those halves, and the split of T into T^T halves
+    for (int L = 0; L < 3 && p->big_orth; ++L) {
+      const size_t nj = L == 0 ? (size_t)cnt : lists[L]->size();
+      std::vector<tcsplit::TJob> at(std::max<size_t>(1, nj)), tt(std::max<size_t>(1, nj));
+      for (int ps = 0; ps < 3; ++ps) {
+        std::vector<tcstream::SJob> gs(std::max<size_t>(1, nj));
+        for (size_t k = 0; k < nj; ++k) {
+          const int i = L == 0 ? (int)k : (*lists[L])[k];
+          const OrthJob& o = (*ojs[L])[k];
+          const long long rp = p->rp[i];
+          const long long ldt = L == 0 ? p->ldt_m[i] : p->ldt_n[i];
+          float* Th = reinterpret_cast<float*>(base + (L == 0 ? p->off_UTh[i] : p->off_VTh[i]));
+          float* Tl = reinterpret_cast<float*>(base + (L == 0 ? p->off_UTl[i] : p->off_VTl[i]));
+          const float* src = ps == 0 ? o.A : (ps == 1 ? o.Q : o.Q2);
+          const long long lds = ps == 0 ? o.lda : rp;
+          tcstream::SJob& g = gs[k];
+          std::memset(&g, 0, sizeof g);
+          bool okm = make_map(&g.mR, F32, src, rp, o.rows, lds * 4, 32, tcstream::BK, CU_TENSOR_MAP_SWIZZLE_128B);
+          okm &= make_map(&g.mBh, F32, Th, o.rows, rp, ldt * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_64B);
+          okm &= make_map(&g.mBl, F32, Tl, o.rows, rp, ldt * 4, tcstream::BK, p->bn[i], CU_TENSOR_MAP_SWIZZLE_64B);
+          if (!okm) return fail(DION_ERR_CUDA, "matrix %d: cuTensorMapEncodeTiled failed (Gram maps)", i);
+          g.out = o.gpart; g.ld_out = rp; g.split_stride = rp * rp;
+          g.flag = o.flag;
+          g.pass = ps == 2 ? -2 : -1;   // -2: the Gram of a third (shifted) pass, flagged jobs only
+          g.out_cols = (int)rp; g.rows = (int)rp; g.kdim = (int)o.rows;
+          g.ksplit = p->gks[L][k]; g.kchunk = p->gkc[L][k]; g.ncb = p->ncb[i]; g.bn = p->bn[i];
+          g.rp = (int)rp; g.gmode = tcstream::G_NONE; g.status = o.status; g.mu = 1.f;
+          if (ps == 0) {
+            at[k] = tcsplit::TJob{o.A, o.lda, Th, Tl, ldt, o.rows, p->descs[i].r, rp, o.status};
+            tt[k] = tcsplit::TJob{o.T, rp, o.Tt_hi, o.Tt_lo, rp, rp, rp, rp, o.status};
+          }
+        }
+        put(p->image, p->t_gsj[L][ps], gs.data(), gs.size());
+      }
+      put(p->image, p->t_atj[L], at.data(), at.size());
+      put(p->image, p->t_ttj[L], tt.data(), tt.size());
+      put(p->image, p->t_ts_atj[L], p->ts_atj[L].data(), p->ts_atj[L].size());
+      put(p->image, p->t_ts_ttj[L], p->ts_ttj[L].data(), p->ts_ttj[L].size());
+      if (!p->it_gs[L].empty()) put(p->image, p->t_it_gs[L], p->it_gs[L].data(), p->it_gs[L].size());
     }
     std::vector<tcsplit::SplitJob> vc(std::max<size_t>(1, p->dion_idx.size()));
     for (size_t k = 0; k < p->dion_idx.size(); ++k) {
@@ -925,54 +1055,118 @@ const T* tab(const dion_plan* p, unsigned char* base, size_t off) {
   return reinterpret_cast<const T*>(base + p->off_tables + off);
 }
 
-// orth() of every job of one list: CholeskyQR2 = two rounds of
-// (Gram partials, reduce + Cholesky + inverse, A T).
-dion_status_t launch_orth(const dion_plan* p, unsigned char* base, cudaStream_t s, size_t t_jobs,
-                          size_t t_ts_gram, size_t t_ts_trmm, const std::vector<int>& ts_gram,
-                          const std::vector<int>& ts_trmm, int njob) {
-  if (njob == 0) return DION_OK;
-  const OrthJob* jobs = tab<OrthJob>(p, base, t_jobs);
-  const int* tg = tab<int>(p, base, t_ts_gram);
-  const int* tt = tab<int>(p, base, t_ts_trmm);
-  // the largest rank of the list decides whether the Cholesky works in shared memory
-  long long rmax = 0;
-  for (int i = 0; i < p->count; ++i) rmax = std::max<long long>(rmax, p->descs[i].r);
-  const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax + 32 * rmax) * 4);
-  const int use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
-  for (int pass = 0; pass < 3; ++pass) {
-    simt::k_gram<<<ts_gram[njob], simt::NT, 0, s>>>(jobs, tg, njob, pass);
-    if (use_smem)
-      simt::k_chol_inv<true><<<njob, simt::CHOL_NT, chol_smem, s>>>(jobs, pass, 0, nullptr);
-    else
-      simt::k_chol_inv<false><<<njob, simt::CHOL_NT, 0, s>>>(jobs, pass, 0, nullptr);
-    simt::k_trmm<<<ts_trmm[njob], simt::NT, 0, s>>>(jobs, tt, njob, pass);
+// One CholeskyQR pass `ps` of orth() over list L (0: P, 1: W, 2: V) is three
+// pieces, kept apart so that the row-sharded step can exchange the Gram between them:
+//   orth_gram   the Gram of the pass's argument, summed into each job's gsum
+//   orth_chol   Cholesky + inverse of gsum, and T^T's tf32 halves for the tensor core
+//   orth_apply  argument T on the tensor core: the next factor, or the result
+// Ranks up to 192: tensor-core Gram partials per 256 rows and the one-CTA Cholesky.
+// Above 192 (any job of the plan): the Gram on the streaming kernel (transposed mode)
+// and the blocked Cholesky of bchol.cuh.  A pass-2 piece only works on jobs whose
+// pass 0 took the shifted branch.
+struct OrthList {
+  const OrthJob* jobs;
+  int njob;
+};
+
+OrthList orth_list(const dion_plan* p, unsigned char* base, int L) {
+  const size_t t = L == 0 ? p->t_jobs_p : (L == 1 ? p->t_jobs_w : p->t_jobs_v);
+  const int n = L == 0 ? p->count : (int)(L == 1 ? p->orth_idx.size() : p->dion_idx.size());
+  return OrthList{tab<OrthJob>(p, base, t), n};
+}
+
+void orth_gram(const dion_plan* p, unsigned char* base, cudaStream_t s, int L, int ps) {
+  const OrthList ol = orth_list(p, base, L);
+  if (ol.njob == 0) return;
+  if (p->big_orth) {
+    if (ps == 0)   // the argument's transposed halves (later passes get them from the A T drain)
+      tcsplit::k_tsplit<<<p->ts_atj[L][ol.njob], tcsplit::NT, 0, s>>>(
+          tab<tcsplit::TJob>(p, base, p->t_atj[L]), tab<int>(p, base, p->t_ts_atj[L]), ol.njob);
+    const int ni = (int)p->it_gs[L].size();
+    tcstream::k_stream<true><<<std::min(ni, p->num_sms), tcstream::NTHREADS, tcstream::SMEM_BYTES, s>>>(
+        tab<tcstream::SJob>(p, base, p->t_gsj[L][ps]), tab<tcstream::Item>(p, base, p->t_it_gs[L]), ni);
+  } else {
+    const int ng = (int)p->it_g[L].size();
+    tcgram::k_gram<<<std::min(ng, p->num_sms), tcgram::NTHREADS, tcgram::SMEM_BYTES, s>>>(
+        tab<tcgram::GJob>(p, base, p->t_gj[L][ps]), tab<tcgram::GItem>(p, base, p->t_it_g[L]), ng);
+  }
+  simt::k_gram_reduce<<<p->ts_gred[L][ol.njob], 256, 0, s>>>(ol.jobs, tab<int>(p, base, p->t_ts_gred[L]),
+                                                              ol.njob, ps);
+}
+
+void orth_chol(const dion_plan* p, unsigned char* base, cudaStream_t s, int L, int ps) {
+  const OrthList ol = orth_list(p, base, L);
+  if (ol.njob == 0) return;
+  const OrthJob* jobs = ol.jobs;
+  const int njob = ol.njob;
+  if (!p->big_orth) {
+    const long long rmax = std::max<long long>(1, p->rmax_l[L]);
+    const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax + 32 * rmax) * 4);
+    simt::k_chol_inv<true><<<njob, simt::CHOL_NT, chol_smem, s>>>(jobs, ps, 1, tab<int>(p, base, p->t_chol_order[L]));
+    return;
+  }
+  const long long rmax = p->rmax_l[L];
+  long long rpmax = 0;
+  for (int k = 0; k < njob; ++k) {
+    const int i = L == 0 ? k : (L == 1 ? p->orth_idx[k] : p->dion_idx[k]);
+    rpmax = std::max<long long>(rpmax, p->rp[i]);
+  }
+  const int np = (int)cdiv(rmax, bchol::NB);
+  const int ncopy = (int)cdiv(rpmax * rpmax, bchol::COPY_ELEMS);
+  auto factor = [&](int retry) {
+    bchol::k_stats<<<njob, bchol::NT, 0, s>>>(jobs, ps, retry);
+    bchol::k_copy<<<njob * ncopy, bchol::NT, 0, s>>>(jobs, ps, retry, ncopy);
+    for (int pp = 0; pp < np; ++pp) {
+      bchol::k_diag<<<njob, bchol::DIAG_NT, bchol::DIAG_SMEM, s>>>(jobs, ps, retry, pp);
+      const long long trail = rmax - (long long)(pp + 1) * bchol::NB;   // columns right of the panel
+      if (trail <= 0) continue;
+      const int nslab = (int)cdiv(trail, bchol::SLAB);
+      const int tdim = (int)cdiv(trail, simt::TM);
+      bchol::k_panel<<<njob * nslab, bchol::NT, bchol::PANEL_SMEM, s>>>(jobs, ps, retry, pp, nslab);
+      bchol::k_update<<<njob * (tdim * (tdim + 1) / 2), simt::NT, 0, s>>>(jobs, ps, retry, pp,
+                                                                          tdim * (tdim + 1) / 2);
+    }
+    bchol::k_check<<<(int)cdiv(njob, 128), 128, 0, s>>>(jobs, njob, ps, retry);
+  };
+  factor(0);
+  if (ps == 0) factor(1);   // the shifted repetition, for the jobs whose pivots asked for it
+  for (int d = 1; d < np; ++d) {
+    const int nitem = (np - d) * (bchol::NB / bchol::SLAB);
+    bchol::k_inv<<<njob * nitem, bchol::NT, bchol::INV_SMEM, s>>>(jobs, ps, d, nitem);
+  }
+  tcsplit::k_tsplit<<<p->ts_ttj[L][njob], tcsplit::NT, 0, s>>>(tab<tcsplit::TJob>(p, base, p->t_ttj[L]),
+                                                               tab<int>(p, base, p->t_ts_ttj[L]), njob);
+}
+
+void orth_apply(const dion_plan* p, unsigned char* base, cudaStream_t s, int L, int ps) {
+  const OrthList ol = orth_list(p, base, L);
+  if (ol.njob == 0) return;
+  const int nt = (int)p->it_tr[L].size();
+  tcstream::k_stream<false><<<std::min(nt, p->num_sms), tcstream::NTHREADS, tcstream::SMEM_BYTES, s>>>(
+      tab<tcstream::SJob>(p, base, p->t_tj[L][ps]), tab<tcstream::Item>(p, base, p->t_it_tr[L]), nt);
+}
+
+// orth() of every job of list L: up to three CholeskyQR passes.
+dion_status_t launch_orth(const dion_plan* p, unsigned char* base, cudaStream_t s, int L) {
+  for (int ps = 0; ps < 3; ++ps) {
+    orth_gram(p, base, s, L, ps);
+    orth_chol(p, base, s, L, ps);
+    orth_apply(p, base, s, L, ps);
   }
   return cuda_check("orth launch");
 }
 
-// orth() of list L (0: P, 1: W, 2: V) on the tensor core: up to three CholeskyQR
-// passes of (Gram partials, Cholesky + inverse, A T).
-dion_status_t launch_orth_tc(const dion_plan* p, unsigned char* base, cudaStream_t s, int L, size_t t_jobs, int njob) {
-  if (njob == 0) return DION_OK;
-  const OrthJob* jobs = tab<OrthJob>(p, base, t_jobs);
-  long long rmax = 0;
-  for (int i = 0; i < p->count; ++i) rmax = std::max<long long>(rmax, p->descs[i].r);
-  const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax + 32 * rmax) * 4);
-  const int use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
-  const int ng = (int)p->it_g[L].size(), nt = (int)p->it_tr[L].size();
-  const int* order = tab<int>(p, base, p->t_chol_order[L]);
-  for (int ps = 0; ps < 3; ++ps) {
-    tcgram::k_gram<<<std::min(ng, p->num_sms), tcgram::NTHREADS, tcgram::SMEM_BYTES, s>>>(
-        tab<tcgram::GJob>(p, base, p->t_gj[L][ps]), tab<tcgram::GItem>(p, base, p->t_it_g[L]), ng);
-    simt::k_gram_reduce<<<p->ts_gred[L][njob], 256, 0, s>>>(jobs, tab<int>(p, base, p->t_ts_gred[L]), njob, ps);
-    if (use_smem)
-      simt::k_chol_inv<true><<<njob, simt::CHOL_NT, chol_smem, s>>>(jobs, ps, 1, order);
-    else
-      simt::k_chol_inv<false><<<njob, simt::CHOL_NT, 0, s>>>(jobs, ps, 1, order);
-    tcstream::k_stream<false><<<std::min(nt, p->num_sms), tcstream::NTHREADS, tcstream::SMEM_BYTES, s>>>(
-        tab<tcstream::SJob>(p, base, p->t_tj[L][ps]), tab<tcstream::Item>(p, base, p->t_it_tr[L]), nt);
-  }
-  return cuda_check("orth launch");
+// Kernel launches of launch_orth(L) (a pass-2 launch returns at once for jobs
+// without the shifted branch).
+int orth_launches(const dion_plan* p, int L) {
+  const int njob = L == 0 ? p->count : (int)(L == 1 ? p->orth_idx.size() : p->dion_idx.size());
+  if (njob == 0) return 0;
+  if (!p->big_orth) return 3 * 4;
+  const int np = (int)cdiv(p->rmax_l[L], bchol::NB);
+  int fac = 2 + 1;                                       // stats, copy, check
+  for (int pp = 0; pp < np; ++pp) fac += (p->rmax_l[L] > (long long)(pp + 1) * bchol::NB) ? 3 : 1;
+  const int chol = fac + (np - 1) + 1;                   // + inverse diagonals + T^T split
+  return 3 * (2 + chol + 1) + 1 + fac;                   // gram + reduce, chol, apply; pass-0 split and repetition
 }
 
 dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int first, int last,
@@ -1003,18 +1197,14 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
       case 0:
         if (cudaMemsetAsync(base + p->off_status, 0, 16 * (size_t)cnt, s) != cudaSuccess)
           return cuda_check("status reset");
-        if (p->tc_orth) {
-          if (!p->dion_idx.empty()) {
-            tcsplit::k_split<<<p->ts_vcopy[p->dion_idx.size()], tcsplit::NT, 0, s>>>(
-                tab<tcsplit::SplitJob>(p, base, p->t_vcopy), tab<int>(p, base, p->t_ts_vcopy),
-                (int)p->dion_idx.size());
-          }
-          st = launch_orth_tc(p, base, s, 2, p->t_jobs_v, (int)p->dion_idx.size());
-        } else {
-          st = launch_orth(p, base, s, p->t_jobs_v, p->t_ts_gram_v, p->t_ts_trmm_v, p->ts_gram_v,
-                           p->ts_trmm_v, (int)p->dion_idx.size());
+        if (!p->dion_idx.empty()) {
+          // Dion's warm start: a padded copy of V, orthonormalised (orth(M V) = orth(M orth(V)))
+          tcsplit::k_split<<<p->ts_vcopy[p->dion_idx.size()], tcsplit::NT, 0, s>>>(
+              tab<tcsplit::SplitJob>(p, base, p->t_vcopy), tab<int>(p, base, p->t_ts_vcopy),
+              (int)p->dion_idx.size());
+          st = launch_orth(p, base, s, 2);
+          if (st) return st;
         }
-        if (st) return st;
         tcsplit::k_tsplit<<<p->ts_tv[cnt], tcsplit::NT, 0, s>>>(
             tab<tcsplit::TJob>(p, base, p->t_tj_v), tab<int>(p, base, p->t_ts_tv), cnt);
         tcstream::k_stream<false><<<std::min((int)p->it_sa.size(), p->num_sms), tcstream::NTHREADS,
@@ -1023,15 +1213,11 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
                                                                (int)p->it_sa.size());
         break;
       case 1:
-        st = p->tc_orth ? launch_orth_tc(p, base, s, 0, p->t_jobs_p, cnt)
-                        : launch_orth(p, base, s, p->t_jobs_p, p->t_ts_gram_p, p->t_ts_trmm_p, p->ts_gram_p,
-                                      p->ts_trmm_p, cnt);
+        st = launch_orth(p, base, s, 0);
         if (st) return st;
         break;
       case 2:
-        if (!p->tc_orth)   // else the last A T pass of orth(P) wrote U^T's halves
-          tcsplit::k_tsplit<<<p->ts_tu[cnt], tcsplit::NT, 0, s>>>(
-              tab<tcsplit::TJob>(p, base, p->t_tj_u), tab<int>(p, base, p->t_ts_tu), cnt);
+        // (the last A T pass of orth(P) wrote U^T's halves)
         tcstream::k_stream<true><<<std::min((int)p->it_sc.size(), p->num_sms), tcstream::NTHREADS,
                                    tcstream::SMEM_BYTES, s>>>(tab<tcstream::SJob>(p, base, p->t_sj_c),
                                                               tab<tcstream::Item>(p, base, p->t_it_sc),
@@ -1040,9 +1226,7 @@ dion_status_t run_phases(dion_plan* p, void* workspace, size_t ws_bytes, int fir
           simt::k_wreduce<<<p->ts_wred[cnt], simt::NT, 0, s>>>(mats, tab<int>(p, base, p->t_ts_wred), cnt);
         break;
       case 3:
-        st = p->tc_orth ? launch_orth_tc(p, base, s, 1, p->t_jobs_w, (int)p->orth_idx.size())
-                        : launch_orth(p, base, s, p->t_jobs_w, p->t_ts_gram_w, p->t_ts_trmm_w, p->ts_gram_w,
-                                      p->ts_trmm_w, (int)p->orth_idx.size());
+        st = launch_orth(p, base, s, 1);
         if (st) return st;
         if (!p->dion_idx.empty())
           simt::k_colnorm<<<p->ts_coln[p->dion_idx.size()], simt::NT, 0, s>>>(
@@ -1097,58 +1281,23 @@ dion_status_t run_shard_stage(dion_plan* p, void* workspace, size_t ws_bytes, in
   }
   const int cnt = p->count;
   const MatDev* mats = tab<MatDev>(p, base, p->t_mats);
-  const OrthJob* jobs = tab<OrthJob>(p, base, p->t_jobs_p);
-  long long rmax = 0;
-  for (int i = 0; i < cnt; ++i) rmax = std::max<long long>(rmax, p->descs[i].r);
-  const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax + 32 * rmax) * 4);
-  const bool use_smem = chol_smem <= (size_t)simt::CHOL_SMEM_MAX;
-  // pieces of orth(P) (list 0), one CholeskyQR pass at a time
-  auto gram = [&](int ps) {
-    if (p->tc_orth) {
-      const int ng = (int)p->it_g[0].size();
-      tcgram::k_gram<<<std::min(ng, p->num_sms), tcgram::NTHREADS, tcgram::SMEM_BYTES, s>>>(
-          tab<tcgram::GJob>(p, base, p->t_gj[0][ps]), tab<tcgram::GItem>(p, base, p->t_it_g[0]), ng);
-    } else {
-      simt::k_gram<<<p->ts_gram_p[cnt], simt::NT, 0, s>>>(jobs, tab<int>(p, base, p->t_ts_gram_p), cnt, ps);
-    }
-    simt::k_gram_reduce<<<p->ts_gred[0][cnt], 256, 0, s>>>(jobs, tab<int>(p, base, p->t_ts_gred[0]), cnt, ps);
-  };
-  auto chol = [&](int ps) {
-    const int* order = p->tc_orth ? tab<int>(p, base, p->t_chol_order[0]) : nullptr;
-    if (use_smem)
-      simt::k_chol_inv<true><<<cnt, simt::CHOL_NT, chol_smem, s>>>(jobs, ps, 1, order);
-    else
-      simt::k_chol_inv<false><<<cnt, simt::CHOL_NT, 0, s>>>(jobs, ps, 1, order);
-  };
-  auto apply_t = [&](int ps) {
-    if (p->tc_orth) {
-      const int nt = (int)p->it_tr[0].size();
-      tcstream::k_stream<false><<<std::min(nt, p->num_sms), tcstream::NTHREADS, tcstream::SMEM_BYTES, s>>>(
-          tab<tcstream::SJob>(p, base, p->t_tj[0][ps]), tab<tcstream::Item>(p, base, p->t_it_tr[0]), nt);
-    } else {
-      simt::k_trmm<<<p->ts_trmm_p[cnt], simt::NT, 0, s>>>(jobs, tab<int>(p, base, p->t_ts_trmm_p), cnt, ps);
-    }
-  };
   switch (stage) {
     case 0: {
       // phase (a) as in the fused step, then the first Gram into the exchange region
       st = run_phases(p, workspace, ws_bytes, 0, 0, stream);
       if (st) return st;
-      gram(0);
+      orth_gram(p, base, s, 0, 0);
       break;
     }
     case 1:
     case 2:
-      chol(stage - 1);
-      apply_t(stage - 1);
-      gram(stage);
+      orth_chol(p, base, s, 0, stage - 1);
+      orth_apply(p, base, s, 0, stage - 1);
+      orth_gram(p, base, s, 0, stage);
       break;
     case 3:
-      chol(2);
-      apply_t(2);
-      if (!p->tc_orth)
-        tcsplit::k_tsplit<<<p->ts_tu[cnt], tcsplit::NT, 0, s>>>(
-            tab<tcsplit::TJob>(p, base, p->t_tj_u), tab<int>(p, base, p->t_ts_tu), cnt);
+      orth_chol(p, base, s, 0, 2);
+      orth_apply(p, base, s, 0, 2);
       tcstream::k_stream<true><<<std::min((int)p->it_sc.size(), p->num_sms), tcstream::NTHREADS,
                                  tcstream::SMEM_BYTES, s>>>(tab<tcstream::SJob>(p, base, p->t_sj_c),
                                                             tab<tcstream::Item>(p, base, p->t_it_sc),
@@ -1288,7 +1437,8 @@ dion_status_t dion_plan_create(const dion_matrix_desc* descs, int32_t count, siz
     return fail(DION_ERR_UNSUPPORTED, "internal: work tables failed their check: %s", wrong.c_str());
   }
   // every grouped launch must fit in one grid dimension
-  const long long grids[] = {p->ts_gram_p[count], p->ts_trmm_p[count], p->ts_wred[count], p->ts_split[p->n_split]};
+  const long long grids[] = {p->ts_wred[count], p->ts_split[p->n_split], p->ts_tv[count], p->ts_wsplit[count],
+                             p->ts_atj[0].empty() ? 0 : p->ts_atj[0].back()};
   for (long long g : grids)
     if (g >= (1LL << 31)) {
       delete p;
@@ -1331,7 +1481,13 @@ dion_status_t dion_plan_upload(dion_plan* plan, void* workspace, size_t ws_bytes
         cudaFuncSetAttribute(simt::k_chol_inv<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              simt::CHOL_SMEM_MAX) != cudaSuccess ||
         cudaFuncSetAttribute(tcgram::k_gram, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tcgram::SMEM_BYTES) != cudaSuccess)
+                             (int)tcgram::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(bchol::k_diag, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bchol::DIAG_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(bchol::k_panel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bchol::PANEL_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(bchol::k_inv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bchol::INV_SMEM) != cudaSuccess)
       return cuda_check("kernel attributes");
   }
   st = build_image(plan, base);
@@ -1385,15 +1541,14 @@ dion_status_t dion_plan_get_status(dion_plan* plan, const void* workspace, size_
 
 int32_t dion_plan_launches_per_step(const dion_plan* plan) {
   if (!plan) return -1;
-  int n = 2;                                   // phase (a): V^T split + tensor-core P = M V
-  const int per_orth = plan->tc_orth ? 12 : 9;  // up to three CholeskyQR rounds (+ partial reduce)
-  n += plan->dion_idx.empty() ? 0 : per_orth + (plan->tc_orth ? 1 : 0);   // phase (a): orth(V) of Dion matrices
-  n += per_orth;                               // phase (b)
-  n += (plan->tc_orth ? 1 : 2) + (plan->any_split ? 1 : 0);   // phase (c): [U^T split], W = M^T U, reduce
-  n += plan->orth_idx.empty() ? 0 : per_orth;  // phase (d), Orth-Dion matrices
-  n += plan->dion_idx.empty() ? 0 : 1;         // phase (d), Dion matrices
-  n += plan->n_split > 0 ? 1 : 0;              // phase (d): tf32 halves left to split
-  n += (int)plan->it_epi.size();               // phase (e): tensor-core update, one launch per K pass
+  int n = 2;                                           // phase (a): V^T split + tensor-core P = M V
+  if (!plan->dion_idx.empty()) n += 1 + orth_launches(plan, 2);   // phase (a): copy + orth(V) of Dion matrices
+  n += orth_launches(plan, 0);                         // phase (b)
+  n += 1 + (plan->any_split ? 1 : 0);                  // phase (c): W = M^T U, reduce
+  n += orth_launches(plan, 1);                         // phase (d), Orth-Dion matrices
+  n += plan->dion_idx.empty() ? 0 : 1;                 // phase (d), Dion matrices
+  n += plan->n_split > 0 ? 1 : 0;                      // phase (d): tf32 halves left to split
+  n += (int)plan->it_epi.size();                       // phase (e): tensor-core update, one launch per K pass
   return n;
 }
 

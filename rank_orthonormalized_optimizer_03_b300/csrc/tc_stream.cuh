@@ -74,7 +74,8 @@ struct SJob {
   float* q1;                      // orth(): pass-0 result (ld rp)
   float* q2;                      // orth(): pass-1 result of a three-pass job (ld rp)
   const unsigned* flag;           // orth(): three-pass flag of the job
-  int pass;                       // orth(): CholeskyQR pass 0..2; -1 for phases (a), (c)
+  int pass;                       // orth(): CholeskyQR pass 0..2; -1 for phases (a), (c) and a
+                                  // Gram of pass 0 / 1, -2 for the Gram of a third pass
   int out_cols;                   // columns of out to write (rp, or r for Vbar into V)
   int rows;                       // output rows: m (a) or n (c), rows of A (orth)
   int kdim;                       // K extent: n (a), m (c), rp (orth)
@@ -92,6 +93,7 @@ struct SJob {
   long long ld_t;
   int hcols;
   float mu;                       // M = G + mu R: 1 for Dion / Orth-Dion, the momentum coefficient otherwise
+  int tr_fin, tr_inter;           // write th / tl for the final result, for an intermediate factor
 };
 static_assert(sizeof(SJob) % 64 == 0, "SJob must keep 64-byte alignment of its maps");
 
@@ -101,8 +103,10 @@ struct Item {
   int job, row0, ks, c0, k0, nk, pad0, pad1;
 };
 
+// pass 2 (an A T job) and pass -2 (the Gram of a third CholeskyQR pass) run only for
+// jobs whose first pass took the shifted branch
 __device__ __forceinline__ bool skip(const SJob& j) {
-  return (*j.status & ST_FATAL) != 0 || (j.pass == 2 && !*j.flag);
+  return (*j.status & ST_FATAL) != 0 || ((j.pass == 2 || j.pass == -2) && !*j.flag);
 }
 
 // Drain one finished TMEM slice (columns [col0, col0 + quarter) of this
@@ -179,9 +183,11 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
             tma_load_2d(rdst, &j.mR, &s_full[ss], k, it.row0);
           } else {
             // rows k..k+15 of M, columns row0..row0+127, in boxes of 128 bytes per row
-            const int gbox = j.gmode == G_BF16 ? 64 : 32;
-            for (int b = 0; b < BM / gbox; ++b)
-              tma_load_2d(gdst + b * 2048, &j.mG, &s_full[ss], it.row0 + b * gbox, k);
+            if (j.gmode != G_NONE) {
+              const int gbox = j.gmode == G_BF16 ? 64 : 32;
+              for (int b = 0; b < BM / gbox; ++b)
+                tma_load_2d(gdst + b * 2048, &j.mG, &s_full[ss], it.row0 + b * gbox, k);
+            }
             for (int b = 0; b < BM / 32; ++b)
               tma_load_2d(rdst + b * 2048, &j.mR, &s_full[ss], it.row0 + b * 32, k);
           }
@@ -432,10 +438,13 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
                 if (c + k < cols) dst[c + k] = acc[cb * 8 + k];
             }
           }
-        if (fin && j.sh) {
-          // the halves: c is a multiple of 8 and rp of 32, so a block of 8 is in or out
-          float* hrow = j.sh + (long long)grow * j.rp;
-          float* lrow = j.sl + (long long)grow * j.rp;
+        // tf32 halves for the next tensor-core kernel: row-major ones of the final
+        // result, transposed ones of the final result (tr_fin) or of an intermediate
+        // CholeskyQR factor (tr_inter: the next pass's Gram reads them)
+        const bool want_rm = fin && j.sh;
+        const bool want_tr = j.th && (fin ? j.tr_fin : j.tr_inter);
+        if (want_rm || want_tr) {
+          // c is a multiple of 8 and rp of 32, so a block of 8 is in or out
 #pragma unroll
           for (int cb = 0; cb < QMAX / 8; ++cb)
             if (cb * 8 < qw && cbase + cb * 8 < j.rp) {
@@ -443,11 +452,15 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
               float h[8], l[8];
 #pragma unroll
               for (int k = 0; k < 8; ++k) split_tf32(c + k < j.hcols ? acc[cb * 8 + k] : 0.f, h[k], l[k]);
-              *reinterpret_cast<float4*>(hrow + c) = make_float4(h[0], h[1], h[2], h[3]);
-              *reinterpret_cast<float4*>(hrow + c + 4) = make_float4(h[4], h[5], h[6], h[7]);
-              *reinterpret_cast<float4*>(lrow + c) = make_float4(l[0], l[1], l[2], l[3]);
-              *reinterpret_cast<float4*>(lrow + c + 4) = make_float4(l[4], l[5], l[6], l[7]);
-              if (j.th) {
+              if (want_rm) {
+                float* hrow = j.sh + (long long)grow * j.rp;
+                float* lrow = j.sl + (long long)grow * j.rp;
+                *reinterpret_cast<float4*>(hrow + c) = make_float4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<float4*>(hrow + c + 4) = make_float4(h[4], h[5], h[6], h[7]);
+                *reinterpret_cast<float4*>(lrow + c) = make_float4(l[0], l[1], l[2], l[3]);
+                *reinterpret_cast<float4*>(lrow + c + 4) = make_float4(l[4], l[5], l[6], l[7]);
+              }
+              if (want_tr) {
                 // transposed: the 32 lanes of a warp hold 32 consecutive rows, so each
                 // column is one 128-byte segment
 #pragma unroll
