@@ -224,3 +224,18 @@ def test_row_selection_plan(L):
     code, _, plan = muon_create(L, descs)
     assert L.muon_plan_selected_rows(plan, 0, ctypes.byref(off), ctypes.byref(k)) == dion.DION_ERR_INVALID_ARG
     L.muon_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("shapes", [[(8192, 8192, 2048)], [(3072, 3072, 768), (1024, 3072, 256), (8192, 3072, 768)],
+                                    [(1200, 640, 300), (200, 160, 16)]])
+def test_large_rank_plans_pass_their_table_checks(L, shapes):
+    """Ranks above 192 take the blocked-Cholesky orth() path: its Gram items (transposed
+    streaming mode, K split over rows) pass the plan's coverage checks."""
+    descs = [fake_desc(k, m=m, n=n, r=r, variant=k % 2) for k, (m, n, r) in enumerate(shapes)]
+    code, ws, plan = create(L, descs)
+    assert code == dion.DION_OK, L.dion_last_error()
+    rmax = max(r for _, _, r in shapes)
+    np_ = -(-rmax // 128)
+    # at least three CholeskyQR passes of (Gram, reduce, np panels, inverse, split, A T) for orth(P)
+    assert L.dion_plan_launches_per_step(plan) > 3 * (4 + np_)
+    L.dion_plan_destroy(plan)

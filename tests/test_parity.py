@@ -154,17 +154,24 @@ def test_gpt160m_chain_10_steps(dev, variant):
 
 
 def ill_conditioned_case(m, n, r, eps, seed):
-    """A step whose P = M V is ill conditioned (kappa ~ 8e3 for eps = 1e-2) through the warm start:
-    V is orthonormal except that its second column is the first one plus eps times
-    a unit vector orthogonal to it, so P's first two columns are nearly parallel
-    while M itself is an ordinary gradient (rank-4 signal plus noise).  span(P)
-    stays well determined, so the fp32 result can match the float64 oracle to
-    kappa(P) u.  (A P made ill conditioned by M's own spectrum instead -- singular
-    values falling below M's noise floor -- leaves W = M^T U ill determined in
-    fp32 whatever the algorithm.)"""
+    """A step whose P = M V is ill conditioned through the warm start: M is an
+    ordinary gradient (rank-4 signal A B^T plus noise), and V's first two columns
+    lie in the noise subspace (orthogonal to B), nearly parallel: the second is
+    the first plus eps times a unit vector.  For eps = 1e-2, kappa(P) ~ 1e4 and
+    the smallest Cholesky pivot of P^T P is ~1e-7 of its largest diagonal entry
+    (the pivot ratio that sends orth() down the shifted branch).  span(P) stays
+    well determined, so the fp32 inputs themselves move the oracle's result by
+    only ~1e-6.  (Nearly parallel columns in the signal subspace keep the pivot
+    ratio near eps^2; an ill-conditioned M spectrum below its noise floor leaves
+    W = M^T U ill determined in fp32 whatever the algorithm.)"""
     g = np.random.Generator(np.random.PCG64(seed))
-    G = (g.standard_normal((m, 4)) @ g.standard_normal((4, n)) + 0.1 * g.standard_normal((m, n)))
+    A, B = g.standard_normal((m, 4)), g.standard_normal((n, 4))
+    G = A @ B.T + 0.1 * g.standard_normal((m, n))
     V, _ = np.linalg.qr(g.standard_normal((n, r)))
+    Qb, _ = np.linalg.qr(B)
+    for k in (0, 1):
+        V[:, k] -= Qb @ (Qb.T @ V[:, k])
+        V[:, k] /= np.linalg.norm(V[:, k])
     V[:, 1] = V[:, 0] + eps * V[:, 1]
     return G.astype(np.float32), V.astype(np.float32), g.normal(0, 0.02, (m, n)).astype(np.float32)
 

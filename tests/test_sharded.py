@@ -27,10 +27,13 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def problem(m, n, r, seed):
+    """A gradient of rank-3 signal plus noise of comparable size, so that the
+    residual beyond rank r is not a tiny difference of large terms (its relative
+    error would then measure fp32 rounding of M, not the sharding)."""
     g = np.random.Generator(np.random.PCG64(seed))
     X = g.normal(0, 0.02, (m, n))
     R = 0.05 * g.standard_normal((m, n))
-    G = g.standard_normal((m, 3)) @ g.standard_normal((3, n)) + 0.1 * g.standard_normal((m, n))
+    G = g.standard_normal((m, 3)) @ g.standard_normal((3, n)) + 0.5 * g.standard_normal((m, n))
     V = g.standard_normal((n, r)) / math.sqrt(n)
     return X, G, R, V
 
