@@ -22,6 +22,7 @@
 #include "tc_stream.cuh"
 #include "tc_gram.cuh"
 #include "bchol.cuh"
+#include "chol_gj.cuh"
 
 using namespace dion;
 
@@ -1100,9 +1101,7 @@ void orth_chol(const dion_plan* p, unsigned char* base, cudaStream_t s, int L, i
   const OrthJob* jobs = ol.jobs;
   const int njob = ol.njob;
   if (!p->big_orth) {
-    const long long rmax = std::max<long long>(1, p->rmax_l[L]);
-    const size_t chol_smem = (size_t)((rmax * (rmax + 1) + rmax + 32 * rmax) * 4);
-    simt::k_chol_inv<true><<<njob, simt::CHOL_NT, chol_smem, s>>>(jobs, ps, 1, tab<int>(p, base, p->t_chol_order[L]));
+    gj::k_chol_gj<<<njob, gj::NT, 0, s>>>(jobs, ps, tab<int>(p, base, p->t_chol_order[L]));
     return;
   }
   const long long rmax = p->rmax_l[L];
