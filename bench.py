@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--e2e-groups", type=int, default=14,
                     help="matrix groups of the host-fed end-to-end step (copy/compute overlap)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-muon", action="store_true", help="skip the Muon comparator line on the same matrices")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
@@ -338,9 +339,20 @@ def run_cuda(args):
         out, plan, mats, cost = measure(wl, args, dev, world, args.variant, peaks, min_timed_s=0)
         if not args.no_e2e:
             out["e2e"] = run_e2e(args, mats, cost["step"].bytes, out["ms_per_step"], world)
+        if not args.no_muon:
+            plan.close()
+            del plan, mats
+            torch.cuda.empty_cache()
+            plan = None
+            mu = measure_muon(wl, args, dev, "bf16")
+            out["muon_comparator"] = dict(mu, muon_over_dion=round(mu["ms_per_step"] / out["ms_per_step"], 3),
+                                          note="same matrices, Muon momentum + cubic Newton-Schulz (cuBLAS bf16 "
+                                               "GEMMs); the pages' Dion3 claim of up to 6x lower step time than "
+                                               "Muon states no hardware")
         if rank == 0 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(wl, args, args.cpu_seconds)
-        plan.close()
+        if plan is not None:
+            plan.close()
         if rank == 0:
             print(json.dumps(out), flush=True)
     if world > 1:
