@@ -418,7 +418,8 @@ def measure_muon(wl, args, dev, precision, iters=MUON_ITERS, min_timed_s=1.0):
         plan.step()
     torch.cuda.synchronize()
     est = (time.perf_counter() - t0) / max(1, args.warmup)
-    steps = max(args.steps, min(2000, int(math.ceil(min_timed_s / max(est, 1e-5)))))
+    # about two seconds of timed steps, at most --steps and at least 3
+    steps = max(3, min(args.steps, int(math.ceil(2.0 / max(est, 1e-5)))))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(steps):
