@@ -6,8 +6,8 @@
 // Every job's Gram (the reduced sum in o.gsum, rp x rp, row-major) is copied to
 // o.S (k_stats, k_copy) and factored in place in 128-wide panels; T is built in
 // o.T.  Per panel p (one launch each, all jobs at once):
-//   k_diag    one CTA per job: Cholesky + inverse of the diagonal block S_pp in
-//             shared memory (the one-CTA kernels' device functions)
+//   k_diag_gj one CTA per job: Cholesky + inverse of the diagonal block S_pp by the
+//             register Gauss-Jordan elimination of chol_gj.cuh
 //   k_panel   one CTA per 64-column slab: the row panel R_pc = T_pp^T S_pc
 //   k_update  one CTA per 64 x 64 tile of the trailing upper triangle:
 //             S_ac -= R_pa^T R_pc
@@ -20,6 +20,7 @@
 // rank ends before panel p (or diagonal d) skips that launch.
 #pragma once
 
+#include "chol_gj.cuh"
 #include "common.cuh"
 #include "simt.cuh"
 
@@ -28,11 +29,9 @@ namespace bchol {
 
 constexpr int NB = 128;        // panel width
 constexpr int SLAB = 64;       // output column slab of k_panel and k_inv
-constexpr int NT = 256;        // threads of k_init, k_panel, k_update, k_inv
-constexpr int DIAG_NT = 512;   // threads of k_diag
-// dynamic shared memory: k_diag holds S_pp (NB x NB+1), its diagonal inverse and
-// 32 NB of scratch; k_inv holds T_pp (NB x NB+1) and C (NB x SLAB+1)
-constexpr size_t DIAG_SMEM = sizeof(float) * (NB * (NB + 1) + NB + 32 * NB);
+constexpr int NT = 256;        // threads of k_stats, k_copy, k_panel, k_inv
+// dynamic shared memory: k_inv holds T_pp (NB x NB+1) and C (NB x SLAB+1), k_panel
+// T_pp and the slab of S
 constexpr size_t INV_SMEM = sizeof(float) * (NB * (NB + 1) + NB * (SLAB + 1));
 constexpr size_t PANEL_SMEM = sizeof(float) * (NB * (NB + 1) + NB * SLAB);
 constexpr int COPY_ELEMS = 4096;   // elements of S and of T per CTA of k_copy
@@ -109,40 +108,41 @@ __global__ void __launch_bounds__(NT) k_copy(const OrthJob* __restrict__ jobs, i
   }
 }
 
-// Cholesky + inverse of the diagonal block of panel p, one CTA per job.
-__global__ void __launch_bounds__(DIAG_NT, 1) k_diag(const OrthJob* __restrict__ jobs, int pass, int retry, int p) {
-  extern __shared__ float sm_diag[];
-  __shared__ int s_bad;
-  __shared__ float s_min, s_max;
+// The diagonal block of panel p (nb <= 128) by the register Gauss-Jordan elimination
+// of chol_gj.cuh, one CTA per job: Rc_pp = D^1/2 L^T into S, T_pp = L^-T D^-1/2 into T.
+__global__ void __launch_bounds__(gj::NT, 1) k_diag_gj(const OrthJob* __restrict__ jobs, int pass, int retry, int p) {
+  __shared__ float row[2][gj::RMAX];
+  __shared__ float piv[gj::RMAX];
   const OrthJob& o = jobs[blockIdx.x];
   if (!live(o, pass, retry)) return;
   Scr* sc = scr(o);
   if (sc->bad) return;
   const int r = (int)o.r, rp = (int)o.rp, k0 = p * NB;
   if (k0 >= r) return;
-  const int nb = min(NB, r - k0), lds = nb + 1;
-  float* Ss = sm_diag;
-  float* tdiag = Ss + nb * lds;
-  float* scratch = tdiag + nb;
-  for (int e = threadIdx.x; e < nb * nb; e += DIAG_NT) {
-    const int a = e / nb, c = e % nb;
-    Ss[a * lds + c] = o.S[(long long)(k0 + a) * rp + k0 + c];
-  }
-  __syncthreads();
-  const int bad = simt::chol_factor(Ss, lds, nb, tdiag, scratch, &s_bad, &s_min, &s_max);
+  const int nb = min(NB, r - k0);
+  float E[gj::PR][gj::PC];
+  float minp;
+  const unsigned bad = gj::eliminate(E, o.S + (long long)k0 * rp + k0, rp, nb, 0.f, row, piv, &minp);
   if (bad) {
-    if (threadIdx.x == 0) sc->bad = (unsigned)bad;
+    if (threadIdx.x == 0) sc->bad = bad;
     return;
   }
-  simt::inverse_blocks(Ss, lds, nb, tdiag, scratch);
-  for (int e = threadIdx.x; e < nb * nb; e += DIAG_NT) {
-    const int a = e / nb, c = e % nb;
-    if (a <= c) {
-      o.S[(long long)(k0 + a) * rp + k0 + c] = simt::Rv(Ss, lds, nb, a, c);
-      o.T[(long long)(k0 + a) * rp + k0 + c] = simt::Tv(Ss, lds, tdiag, nb, a, c);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+#pragma unroll
+  for (int a = 0; a < gj::PR; ++a) {
+    const int i = w + gj::NW * a;
+    if (i >= nb) continue;
+    const float si = sqrtf(piv[i]), ti = 1.f / si;
+#pragma unroll
+    for (int b = 0; b < gj::PC; ++b) {
+      const int c = l + 32 * b;
+      if (c >= nb) continue;
+      if (c >= i) o.S[(long long)(k0 + i) * rp + k0 + c] = E[a][b] / si;            // Rc[i][c] = d_i L_ci / sqrt(d_i)
+      if (c < i) o.T[(long long)(k0 + c) * rp + k0 + i] = E[a][b] * ti;             // T[c][i] = (L^-1)_ic / sqrt(d_i)
+      else if (c == i) o.T[(long long)(k0 + i) * rp + k0 + i] = ti;
     }
   }
-  if (threadIdx.x == 0) sc->minp = fminf(sc->minp, s_min);
+  if (threadIdx.x == 0) sc->minp = fminf(sc->minp, minp);
 }
 
 // Row panel of panel p, 64 columns per CTA: R_pc = T_pp^T S_pc (in place in S).

@@ -31,6 +31,62 @@ constexpr int PC = 6;                // columns per thread (l + 32 b)
 constexpr int RMAX = NW * PR;        // 192
 static_assert(RMAX == 32 * PC, "rows and columns cover the same 192");
 
+// The elimination itself, by the whole CTA: loads the upper triangle of the n x n
+// symmetric S (leading dimension ld; + shift on the diagonal) into E, eliminates,
+// and returns 0 or the status bits of a breakdown.  Afterwards E's upper triangle
+// holds row i of D L^T (E[i][i] = d_i, also in piv[i]) and its strict lower
+// triangle L^-1; *minp receives the smallest pivot.  `row` is 2 x RMAX floats of
+// shared memory, `piv` RMAX floats.
+__device__ __forceinline__ unsigned eliminate(float (&E)[PR][PC], const float* S, long long ld, int n, float shift,
+                                              float (*row)[RMAX], float* piv, float* minp_out) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+#pragma unroll
+  for (int a = 0; a < PR; ++a)
+#pragma unroll
+    for (int b = 0; b < PC; ++b) {
+      const int i = w + NW * a, c = l + 32 * b;
+      E[a][b] = (i < n && c < n && c >= i) ? S[(long long)i * ld + c] + (i == c ? shift : 0.f) : 0.f;
+    }
+  unsigned bad = 0u;
+  float minp = INFINITY;
+  for (int j = 0; j < n; ++j) {
+    float* buf = row[j & 1];
+    if (w == j % NW) {
+      const int a = j / NW;
+#pragma unroll
+      for (int aa = 0; aa < PR; ++aa)
+        if (aa == a)
+#pragma unroll
+          for (int b = 0; b < PC; ++b) buf[l + 32 * b] = E[aa][b];
+    }
+    __syncthreads();
+    const float d = buf[j];
+    if (!(d > 0.f) || !isfinite(d)) {      // the same decision in every thread
+      bad = isfinite(d) ? ST_BREAKDOWN : (ST_BREAKDOWN | ST_NONFINITE);
+      break;
+    }
+    if (threadIdx.x == 0) piv[j] = d;
+    minp = fminf(minp, d);
+    const float inv = 1.f / d;
+#pragma unroll
+    for (int a = 0; a < PR; ++a) {
+      const int i = w + NW * a;
+      if (i <= j || i >= n) continue;
+      const float f = buf[i] * inv;        // l_ij = S_ji / S_jj (S_ji in row j's upper part)
+#pragma unroll
+      for (int b = 0; b < PC; ++b) {
+        const int c = l + 32 * b;
+        if (c >= n) continue;
+        if (c >= i || c < j) E[a][b] = fmaf(-f, buf[c], E[a][b]);   // S_ic, or (L^-1)_ic
+        else if (c == j) E[a][b] = -f;                               // (L^-1)_ij
+      }
+    }
+  }
+  __syncthreads();
+  *minp_out = minp;
+  return bad;
+}
+
 __global__ void __launch_bounds__(NT, 1) k_chol_gj(const OrthJob* __restrict__ jobs, int pass,
                                                    const int* __restrict__ order) {
   __shared__ float row[2][RMAX];     // the pivot row of the current step
@@ -64,51 +120,9 @@ __global__ void __launch_bounds__(NT, 1) k_chol_gj(const OrthJob* __restrict__ j
   for (;; ++attempt) {
     const float shift =
         attempt ? 11.f * ((float)o.rows * (float)r + (float)r * (float)(r + 1)) * 5.9604645e-8f * trace : 0.f;
-    // the upper triangle of S (+ shift), zero below: the identity's strict lower part
-#pragma unroll
-    for (int a = 0; a < PR; ++a)
-#pragma unroll
-      for (int b = 0; b < PC; ++b) {
-        const int i = w + NW * a, c = l + 32 * b;
-        E[a][b] = (i < r && c < r && c >= i) ? o.gsum[(long long)i * rp + c] + (i == c ? shift : 0.f) : 0.f;
-      }
-    bad = 0u;
-    float minp = INFINITY;
-    for (int j = 0; j < r; ++j) {
-      float* buf = row[j & 1];
-      if (w == j % NW) {
-        const int a = j / NW;
-#pragma unroll
-        for (int aa = 0; aa < PR; ++aa)
-          if (aa == a)
-#pragma unroll
-            for (int b = 0; b < PC; ++b) buf[l + 32 * b] = E[aa][b];
-      }
-      __syncthreads();
-      const float d = buf[j];
-      if (!(d > 0.f) || !isfinite(d)) {      // the same decision in every thread
-        bad = isfinite(d) ? ST_BREAKDOWN : (ST_BREAKDOWN | ST_NONFINITE);
-        break;
-      }
-      if (threadIdx.x == 0) piv[j] = d;
-      minp = fminf(minp, d);
-      const float inv = 1.f / d;
-#pragma unroll
-      for (int a = 0; a < PR; ++a) {
-        const int i = w + NW * a;
-        if (i <= j || i >= r) continue;
-        const float f = buf[i] * inv;        // l_ij = S_ji / S_jj (S_ji in row j's upper part)
-#pragma unroll
-        for (int b = 0; b < PC; ++b) {
-          const int c = l + 32 * b;
-          if (c >= r) continue;
-          if (c >= i || c < j) E[a][b] = fmaf(-f, buf[c], E[a][b]);   // S_ic, or (L^-1)_ic
-          else if (c == j) E[a][b] = -f;                               // (L^-1)_ij
-        }
-      }
-    }
+    float minp;
+    bad = eliminate(E, o.gsum, rp, r, shift, row, piv, &minp);
     const bool shifted_try = pass == 0 && attempt == 0 && (bad || minp < 1e-6f * maxd);
-    __syncthreads();
     if (!shifted_try) break;
   }
   if (bad) {

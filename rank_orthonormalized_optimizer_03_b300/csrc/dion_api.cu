@@ -22,7 +22,6 @@
 #include "tc_stream.cuh"
 #include "tc_gram.cuh"
 #include "bchol.cuh"
-#include "chol_gj.cuh"
 
 using namespace dion;
 
@@ -277,9 +276,12 @@ void layout(dion_plan* p) {
         p->gks[L][k] = (int)cdiv(rows, ch);
         (L == 0 ? p->nchunk_p[i] : p->nchunk_w[i]) = p->gks[L][k];
         (L == 0 ? p->chunk_p[i] : p->chunk_w[i]) = (int)ch;
+        // the Gram is symmetric and its consumers read the upper triangle only: tiles
+        // wholly below the diagonal (first row past the block's last column) are skipped
         for (long long r0 = 0; r0 < p->rp[i]; r0 += tcstream::BM)
           for (int ks = 0; ks < p->gks[L][k]; ++ks)
             for (int cb = 0; cb < p->ncb[i]; ++cb) {
+              if (r0 >= (long long)(cb + 1) * p->bn[i]) continue;
               const long long k0 = (long long)ks * ch, k1 = std::min<long long>(rows, k0 + ch);
               p->it_gs[L].push_back(tcstream::Item{(int)k, (int)r0, ks, cb * p->bn[i], (int)k0,
                                                    (int)cdiv(k1 - k0, tcstream::BK), 0, 0});
@@ -382,8 +384,10 @@ void layout(dion_plan* p) {
         const long long rows = L == 0 ? D(i).m : D(i).n;
         for (long long r0 = 0; r0 < rows; r0 += tcstream::BM)
           for (int cb = 0; cb < p->ncb[i]; ++cb)
-            p->it_tr[L].push_back(tcstream::Item{(int)k, (int)r0, 0, cb * p->bn[i], 0,
-                                                 (int)(p->rp[i] / tcstream::BK), 0, 0});
+            // T is upper triangular: output columns below c0 + bn need K below c0 + bn only
+            p->it_tr[L].push_back(tcstream::Item{
+                (int)k, (int)r0, 0, cb * p->bn[i], 0,
+                (int)(std::min<long long>(p->rp[i], (long long)(cb + 1) * p->bn[i]) / tcstream::BK), 0, 0});
         for (long long c = 0; c < cdiv(rows, tcgram::CHUNK_ROWS); ++c)
           p->it_g[L].push_back(tcgram::GItem{(int)k, (int)c, 0, 0});
       }
@@ -633,7 +637,7 @@ std::string verify_tables(const dion_plan* p) {
         if (it.job < 0 || (size_t)it.job >= nj) return bad("orth() item of an unknown job", it.job);
         const int i = mat(it.job);
         if (it.row0 % tcstream::BM || it.row0 >= rows(it.job) || it.c0 % p->bn[i] || it.c0 >= p->rp[i] ||
-            it.k0 != 0 || (long long)it.nk * tcstream::BK != p->rp[i])
+            it.k0 != 0 || (long long)it.nk * tcstream::BK != std::min<long long>(p->rp[i], (long long)it.c0 + p->bn[i]))
           return bad("orth() item out of range", i);
         if (++seen[it.job][(it.row0 / tcstream::BM) * p->ncb[i] + it.c0 / p->bn[i]] != 1)
           return bad("orth() tile covered twice", i);
@@ -670,8 +674,15 @@ std::string verify_tables(const dion_plan* p) {
       if (++seen[it.job][((it.row0 / tcstream::BM) * p->gks[L][it.job] + ks) * p->ncb[i] + it.c0 / p->bn[i]] != 1)
         return bad("Gram tile covered twice", i);
     }
-    for (size_t k = 0; k < nj; ++k)
-      for (int v : seen[k]) if (v != 1) return bad("Gram tile not covered", mat(k));
+    for (size_t k = 0; k < nj; ++k) {
+      const int i = mat(k);
+      for (size_t t = 0; t < seen[k].size(); ++t) {
+        const long long r0 = (long long)(t / ((size_t)p->gks[L][k] * p->ncb[i])) * tcstream::BM;
+        const long long cb = (long long)(t % p->ncb[i]);
+        const int want = r0 >= (cb + 1) * p->bn[i] ? 0 : 1;   // below the diagonal: skipped
+        if (seen[k][t] != want) return bad("Gram tile coverage", i);
+      }
+    }
   }
   // (e): every K pass covers the m x n tiles of exactly the matrices with rp > KPASS * pass
   for (size_t k = 0; k < p->it_epi.size(); ++k) {
@@ -1116,7 +1127,7 @@ void orth_chol(const dion_plan* p, unsigned char* base, cudaStream_t s, int L, i
     bchol::k_stats<<<njob, bchol::NT, 0, s>>>(jobs, ps, retry);
     bchol::k_copy<<<njob * ncopy, bchol::NT, 0, s>>>(jobs, ps, retry, ncopy);
     for (int pp = 0; pp < np; ++pp) {
-      bchol::k_diag<<<njob, bchol::DIAG_NT, bchol::DIAG_SMEM, s>>>(jobs, ps, retry, pp);
+      bchol::k_diag_gj<<<njob, gj::NT, 0, s>>>(jobs, ps, retry, pp);
       const long long trail = rmax - (long long)(pp + 1) * bchol::NB;   // columns right of the panel
       if (trail <= 0) continue;
       const int nslab = (int)cdiv(trail, bchol::SLAB);
@@ -1481,8 +1492,6 @@ dion_status_t dion_plan_upload(dion_plan* plan, void* workspace, size_t ws_bytes
                              simt::CHOL_SMEM_MAX) != cudaSuccess ||
         cudaFuncSetAttribute(tcgram::k_gram, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)tcgram::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(bchol::k_diag, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)bchol::DIAG_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(bchol::k_panel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)bchol::PANEL_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(bchol::k_inv, cudaFuncAttributeMaxDynamicSharedMemorySize,
