@@ -47,7 +47,6 @@ constexpr int QSTAGES_MAX = 4;   // streamed-state ring; the slot count is chose
 constexpr int NTHREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;   // 2 accumulators x NMMA
 constexpr int KPASS = 256;            // K accumulated per launch (per K pass)
-constexpr int PF = 4;                 // streamed sub-chunks brought into L2 ahead of their load
 
 constexpr uint32_t A_BYTES = BM * BK * 4;            // 8 KB
 constexpr uint32_t BH_BYTES = NMMA * BK * 4;         // 16 KB ([Vbar; W] 256 rows)
@@ -198,28 +197,6 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
       const uint32_t gbytes = kpass > 0 ? 0u : (e.g_bf16 ? BM * SUB * 2 : BM * SUB * 4);
       const int ns = nsub(e, tl.j0);
       for (int sc = 0; sc < ns; ++sc) {
-        // L2 prefetch of the sub-chunk PF ahead, in this tile or in this CTA's next one
-        {
-          int pt = t, psc = sc + PF;
-          if (sc == 0 && t == (int)blockIdx.x)   // the first tile: its own first sub-chunks too
-            for (int q = 0; q < PF && q < ns; ++q) {
-              const int xq = tl.j0 + q * SUB;
-              if (kpass == 0) tma_prefetch_2d(&e.map[MAP_G], xq, tl.i0);
-              tma_prefetch_2d(&e.map[MAP_R], xq, tl.i0);
-              tma_prefetch_2d(&e.map[MAP_X], xq, tl.i0);
-            }
-          if (psc >= ns) { psc -= ns; pt = t + gridDim.x; }
-          if (pt < ntiles) {
-            const Tile pn = tiles[pt];
-            const EpiMat& pe = mats[pn.mat];
-            if (!skip(pe) && kc0 * BK < pe.rp && psc < nsub(pe, pn.j0)) {
-              const int xp = pn.j0 + psc * SUB;
-              if (kpass == 0) tma_prefetch_2d(&pe.map[MAP_G], xp, pn.i0);
-              tma_prefetch_2d(&pe.map[MAP_R], xp, pn.i0);
-              tma_prefetch_2d(&pe.map[MAP_X], xp, pn.i0);
-            }
-          }
-        }
         if (!mbar_wait(&q_empty[q], ph ^ 1, abort_flag)) { failed_mat = tl.mat; goto stream_done; }
         mbar_arrive_expect_tx(&q_full[q], gbytes + 2 * RX_BYTES);
         unsigned char* b = qst + q * QST_BYTES;

@@ -45,7 +45,6 @@ constexpr int SSTAGES = 4;           // staging slots of G and R (HBM latency)
 constexpr int NCONV = 16;            // converter / drain warps: four groups of four
 constexpr int NGROUP = 4;            // converter groups; group g converts the chunks numbered g (mod 4)
 constexpr int BWARP = 2 + NCONV;      // warp of the B-operand producer
-constexpr int PF = 8;                // chunks of G / R brought into L2 ahead of their staging load
 constexpr int NTHREADS = (3 + NCONV) * 32;
 constexpr int BN_MAX = 192;          // widest column block (TMEM: 2 x 192 <= 512)
 constexpr int QMAX = BN_MAX / 4;     // accumulator columns per converter thread (one column quarter)
@@ -173,21 +172,6 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
       const uint32_t gbytes = j.gmode == G_NONE ? 0u : BM * BK * (j.gmode == G_BF16 ? 2 : 4);
       for (int kc = 0; kc < it.nk; ++kc) {
         const int k = it.k0 + kc * BK;
-        // L2 prefetch of the chunk PF ahead (the first PF chunks of an item as it starts)
-        for (int q = (kc == 0 ? 0 : PF); q <= PF; ++q) {
-          if (kc + q >= it.nk) break;
-          const int kp = k + q * BK;
-          if (!TRANS) {
-            if (j.gmode != G_NONE) tma_prefetch_2d(&j.mG, kp, it.row0);
-            tma_prefetch_2d(&j.mR, kp, it.row0);
-          } else {
-            if (j.gmode != G_NONE) {
-              const int gbox = j.gmode == G_BF16 ? 64 : 32;
-              for (int b = 0; b < BM / gbox; ++b) tma_prefetch_2d(&j.mG, it.row0 + b * gbox, kp);
-            }
-            for (int b = 0; b < BM / 32; ++b) tma_prefetch_2d(&j.mR, it.row0 + b * 32, kp);
-          }
-        }
         // staging: G and R tiles of M
         if (!mbar_wait(&s_empty[ss], sph ^ 1, abort_flag)) { failed = it.job; goto prod_done; }
         mbar_arrive_expect_tx(&s_full[ss], gbytes + BM * BK * 4);
