@@ -7,11 +7,13 @@
 //
 // M is never stored: every CTA streams G and R tiles by TMA into a staging
 // ring, and 16 converter warps form M = G + R in fp32, split it into the two
-// tf32 halves of a 3xTF32 product and write them into the 64-byte-swizzled
-// K-major operand layout the MMA reads (one thread per operand row; for M^T a
-// thread gathers one column of the staged rows).  The second operand (V^T or
-// U^T, already split) comes in by TMA.  Chunks of 16 along K keep four operand
-// stages and four staging slots in flight in shared memory.  The same kernel
+// tf32 halves of a 3xTF32 product and store them in tensor memory (one thread
+// per operand row, i.e. per TMEM lane; for M^T a thread gathers one column of the
+// staged rows), where the MMA reads its A operand.  A from TMEM keeps the
+// operand halves out of shared memory: the tensor core's operand reads from
+// shared memory, three products per K step, were what bounded this kernel.  The
+// second operand (V^T or U^T, already split) comes in by TMA.  Chunks of 16 along K
+// keep four operand stages and eight staging slots in flight.  The same kernel
 // runs the A T products of orth(); its final pass also writes the tf32 halves
 // of the result for the next tensor-core kernels.
 //
@@ -40,8 +42,8 @@ using namespace dion::tc;
 constexpr int BM = 128;              // output rows per tile (TMEM lanes)
 constexpr int BK = 16;               // K per chunk: one 64-byte swizzle row of fp32
 constexpr int SLICE = 16;            // chunks per TMEM slice (256 of K)
-constexpr int OSTAGES = 4;           // operand stages (A hi/lo written by the converters, B by TMA)
-constexpr int SSTAGES = 4;           // staging slots of G and R (HBM latency)
+constexpr int OSTAGES = 4;           // operand stages (A hi/lo in TMEM by the converters, B by TMA)
+constexpr int SSTAGES = 8;           // staging slots of G and R (HBM latency)
 constexpr int NCONV = 16;            // converter / drain warps: four groups of four
 constexpr int NGROUP = 4;            // converter groups; group g converts the chunks numbered g (mod 4)
 constexpr int BWARP = 2 + NCONV;      // warp of the B-operand producer
@@ -49,10 +51,13 @@ constexpr int NTHREADS = (3 + NCONV) * 32;
 constexpr int BN_MAX = 192;          // widest column block (TMEM: 2 x 192 <= 512)
 constexpr int QMAX = BN_MAX / 4;     // accumulator columns per converter thread (one column quarter)
 constexpr uint32_t TMEM_COLS = 512;
+// TMEM columns: accumulator slices at [0, 2 BN_MAX), then per operand stage the A
+// halves (hi: BK columns, lo: BK columns)
+constexpr uint32_t TMEM_A = 2 * BN_MAX;
+static_assert(TMEM_A + OSTAGES * 2 * BK <= TMEM_COLS, "accumulators and A stages fit in TMEM");
 
-constexpr uint32_t A_BYTES = BM * BK * 4;                // 8 KB
 constexpr uint32_t B_BYTES_MAX = BN_MAX * BK * 4;        // 12 KB
-constexpr uint32_t OST_BYTES = 2 * A_BYTES + 2 * B_BYTES_MAX;   // 40 KB
+constexpr uint32_t OST_BYTES = 2 * B_BYTES_MAX;          // 24 KB: B hi | B lo
 constexpr uint32_t SST_BYTES = 16384;                    // staging slot: G (<= 8 KB) | R (8 KB)
 constexpr uint32_t SST_R = 8192;                         // offset of the R tile in a slot
 constexpr uint32_t SMEM_BYTES = 1024 + OSTAGES * OST_BYTES + SSTAGES * SST_BYTES + 512;
@@ -215,7 +220,7 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
         // operand stage: the B half (already split), bn rows
         if (!mbar_wait(&o_empty[os], oph ^ 1, abort_flag)) { failed = it.job; goto bprod_done; }
         mbar_arrive_expect_tx(&o_full[os], 2 * bbytes);
-        unsigned char* b = ost + os * OST_BYTES + 2 * A_BYTES;
+        unsigned char* b = ost + os * OST_BYTES;
         tma_load_2d(b, &j.mBh, &o_full[os], k, it.c0);
         tma_load_2d(b + B_BYTES_MAX, &j.mBl, &o_full[os], k, it.c0);
         oused[os] = true; olast[os] = oph;
@@ -242,14 +247,14 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
         if (!mbar_wait(&o_full[os], oph, abort_flag)) { failed = it.job; goto mma_done; }
         tc_fence_after();
         const uint32_t d = tmem + b * BN_MAX;
-        const uint32_t ah = smem_u32(ost + os * OST_BYTES), al = ah + A_BYTES;
-        const uint32_t bh = ah + 2 * A_BYTES, bl = bh + B_BYTES_MAX;
+        const uint32_t ah = tmem + TMEM_A + os * 2 * BK, al = ah + BK;   // A halves in TMEM (columns)
+        const uint32_t bh = smem_u32(ost + os * OST_BYTES), bl = bh + B_BYTES_MAX;
 #pragma unroll
         for (int kk = 0; kk < BK / 8; ++kk) {
-          const uint32_t o = kk * 32;
-          mma_tf32(d, sdesc_k_sw64(al + o), sdesc_k_sw64(bh + o), idesc, ((kc % SLICE) | kk) != 0);
-          mma_tf32(d, sdesc_k_sw64(ah + o), sdesc_k_sw64(bl + o), idesc, 1);
-          mma_tf32(d, sdesc_k_sw64(ah + o), sdesc_k_sw64(bh + o), idesc, 1);
+          const uint32_t o = kk * 32;        // B: 8 fp32 of K = 32 bytes; A: 8 columns
+          mma_tf32_ts(d, al + kk * 8, sdesc_k_sw64(bh + o), idesc, ((kc % SLICE) | kk) != 0);
+          mma_tf32_ts(d, ah + kk * 8, sdesc_k_sw64(bl + o), idesc, 1);
+          mma_tf32_ts(d, ah + kk * 8, sdesc_k_sw64(bh + o), idesc, 1);
         }
         issued = true;
         mma_commit(&o_empty[os]);
@@ -304,12 +309,10 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
         if (!mbar_wait_warp(&o_empty[os], oph ^ 1, abort_flag)) { failed = it.job; ok = false; break; }
         const unsigned char* gsrc = sst + ss * SST_BYTES;
         const unsigned char* rsrc = gsrc + SST_R;
-        unsigned char* ahp = ost + os * OST_BYTES;
-        unsigned char* alp = ahp + A_BYTES;
         const float mu = j.mu;                // M = G + mu R (mu = 1: the error-feedback buffer)
+        float mv[16];                         // this thread's operand row: 16 of K
         if (!TRANS) {
           // row `row` of M, the chunk's 16 K elements (64-byte rows, 64-byte swizzle)
-          float mv[16];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float4 r = *reinterpret_cast<const float4*>(rsrc + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
@@ -337,23 +340,10 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
               mv[4 * c + 3] = fmaf(mu, mv[4 * c + 3], gv.w);
             }
           }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float4 hi, lo;
-            split_tf32(mv[4 * c], hi.x, lo.x);
-            split_tf32(mv[4 * c + 1], hi.y, lo.y);
-            split_tf32(mv[4 * c + 2], hi.z, lo.z);
-            split_tf32(mv[4 * c + 3], hi.w, lo.w);
-            const uint32_t off = sw64_off(row, 4 * c);
-            *reinterpret_cast<float4*>(ahp + off) = hi;
-            *reinterpret_cast<float4*>(alp + off) = lo;
-          }
         } else {
           // column `row` of M (row of the M^T operand), the chunk's 16 rows of M as K:
-          // scalar loads walk one staged row across the warp (conflict-free), the
-          // 16-byte stores go to 32 consecutive operand rows (conflict-free)
+          // scalar loads walk one staged row across the warp (conflict-free)
           const int jb = row >> 5, jj = row & 31;
-          float mv[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             mv[i] = *reinterpret_cast<const float*>(rsrc + jb * 2048 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4) +
@@ -373,19 +363,20 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
                            *reinterpret_cast<const float*>(gsrc + jb * 2048 + i * 128 + ((((jj >> 2) ^ i) & 7) << 4) +
                                                            ((jj & 3) << 2)));
           }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float4 hi, lo;
-            split_tf32(mv[4 * c], hi.x, lo.x);
-            split_tf32(mv[4 * c + 1], hi.y, lo.y);
-            split_tf32(mv[4 * c + 2], hi.z, lo.z);
-            split_tf32(mv[4 * c + 3], hi.w, lo.w);
-            const uint32_t off = sw64_off(row, 4 * c);
-            *reinterpret_cast<float4*>(ahp + off) = hi;
-            *reinterpret_cast<float4*>(alp + off) = lo;
-          }
         }
-        fence_async_smem();
+        // the tf32 halves into this stage's TMEM columns, lane `row` (the warp's own
+        // lane quarter); the MMA that last read these columns has completed (o_empty)
+        {
+          float hv[16], lv[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) split_tf32(mv[k], hv[k], lv[k]);
+          tc_fence_after();
+          const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + TMEM_A + os * 2 * BK;
+          tmem_st16(ta, hv);
+          tmem_st16(ta + BK, lv);
+          tmem_wait_st();
+          tc_fence_before();
+        }
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&s_empty[ss]);
