@@ -111,8 +111,9 @@ __global__ void __launch_bounds__(NT) k_copy(const OrthJob* __restrict__ jobs, i
 // The diagonal block of panel p (nb <= 128) by the register Gauss-Jordan elimination
 // of chol_gj.cuh, one CTA per job: Rc_pp = D^1/2 L^T into S, T_pp = L^-T D^-1/2 into T.
 __global__ void __launch_bounds__(gj::NT, 1) k_diag_gj(const OrthJob* __restrict__ jobs, int pass, int retry, int p) {
-  __shared__ float row[2][gj::RMAX];
-  __shared__ float piv[gj::RMAX];
+  extern __shared__ float4 gj_smem4[];
+  float* sm = reinterpret_cast<float*>(gj_smem4);
+  const float* piv = sm + gj::OFF_PIV;
   const OrthJob& o = jobs[blockIdx.x];
   if (!live(o, pass, retry)) return;
   Scr* sc = scr(o);
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(gj::NT, 1) k_diag_gj(const OrthJob* __restrict
   const int nb = min(NB, r - k0);
   float E[gj::PR][gj::PC];
   float minp;
-  const unsigned bad = gj::eliminate(E, o.S + (long long)k0 * rp + k0, rp, nb, 0.f, row, piv, &minp);
+  const unsigned bad = gj::eliminate(E, o.S + (long long)k0 * rp + k0, rp, nb, 0.f, sm, &minp);
   if (bad) {
     if (threadIdx.x == 0) sc->bad = bad;
     return;

@@ -4,15 +4,29 @@
 // glossary), one CTA per job, the whole r x r array in registers.
 //
 // Symmetric Gauss-Jordan elimination: step j subtracts l_ij = S_ij / S_jj times
-// row j from every row i > j, on the upper triangle of S (which stays the upper
-// triangle of the trailing Gram) and, in the strict lower triangle, on the
-// identity, which becomes L^-1 for S = L D L^T (L unit lower triangular, D the
-// pivots).  Then Rc = D^1/2 L^T and T = Rc^-1 = L^-T D^-1/2, so row c of T^T is
-// row c of L^-1 over sqrt(d_c): the kernel writes T^T's tf32 halves directly.
-// One barrier per column (the pivot row is published to shared memory in a
-// double buffer); no serial single-warp phase.
+// row j from every row i > j.  The array holds, in place, the upper triangle of
+// the eliminated Gram (row i of D L^T for S = L D L^T, L unit lower triangular,
+// D the pivots) and, in the strict lower triangle, the identity that the same
+// row operations turn into L^-1.  Then Rc = D^1/2 L^T and T = Rc^-1 = L^-T D^-1/2,
+// so row c of T^T is row c of L^-1 over sqrt(d_c): the kernel writes T^T's tf32
+// halves directly.
 //
-// Thread (warp w, lane l) holds the 72 entries (w + 16 a, l + 32 b), a < 12, b < 6.
+// The steps are taken 16 at a time (a block J of pivots, one row per warp):
+//   1. the 16 rows of J are staged in shared memory;
+//   2. one warp eliminates the 16 x 16 diagonal block (lane c holds column c;
+//      the multipliers come by shuffle), giving D_J, the upper part D_J L_JJ^T
+//      and L_JJ^-1;
+//   3. the rows of J are multiplied by L_JJ^-1 (their columns outside J: the
+//      finished part of L^-1 on the left, the Gram on the right);
+//   4. every row i after J takes the rank-16 update row_i -= sum_j l_ij row_j,
+//      j in J, over its L^-1 columns and its Gram columns.
+// Step 4 is where the work is; it has no per-element conditions: the rows after
+// J carry their strict lower Gram entries along as scratch (kept only where a
+// 16 x 32 register tile reaches the diagonal) and zero them when their block's
+// L^-1 columns start.  Three barriers per block instead of one per column.
+//
+// Thread (warp w, lane l) holds the 72 entries (w + 16 a, l + 32 b), a < 12, b < 6:
+// block J is row group a = J, and lanes 16 (J mod 2) .. + 15 of column group J / 2.
 // Conditioning as in simt::k_chol_inv: in pass 0 a breakdown or pivots implying
 // kappa > ~1e3 (min pivot < 1e-6 max diagonal) repeat the elimination on the
 // shifted Gram of shifted CholeskyQR and flag the job for a third pass.
@@ -30,67 +44,204 @@ constexpr int PR = 12;               // rows per thread (w + 16 a)
 constexpr int PC = 6;                // columns per thread (l + 32 b)
 constexpr int RMAX = NW * PR;        // 192
 static_assert(RMAX == 32 * PC, "rows and columns cover the same 192");
+constexpr int JB = 16;               // pivots per block: one row group
+constexpr int NBLK = RMAX / JB;      // 12
+constexpr int LDA = RMAX + 1;        // staged row (odd: the diagonal warp reads rows and columns)
+constexpr int LDD = JB + 1;
+
+// dynamic shared memory, in floats
+constexpr int OFF_A = 0;                         // JB x LDA: rows of J as they were
+constexpr int OFF_P = OFF_A + JB * LDA;           // JB x RMAX: rows of J after step 3
+constexpr int OFF_M = OFF_P + JB * RMAX;          // JB x RMAX: l_ij of row i at (i % 16) * 12 + i / 16
+constexpr int OFF_D = OFF_M + JB * RMAX;          // JB x LDD: the eliminated diagonal block
+constexpr int OFF_PIV = OFF_D + JB * LDD;         // RMAX pivots
+constexpr int OFF_FLAG = OFF_PIV + RMAX;          // status and smallest pivot of the block
+constexpr int SMEM_FLOATS = OFF_FLAG + 4;
+constexpr size_t SMEM_BYTES = sizeof(float) * SMEM_FLOATS;
+static_assert(OFF_M % 4 == 0, "multiplier rows are read as float4");
+
+// lane l of column group J / 2 holds a column of block J
+template <int J>
+__device__ __forceinline__ bool in_block(int l) { return (l >> 4) == (J & 1); }
+
+// Step 2, by warp 0: lane l holds rows 8 (l / 16) .. + 7 of column c = l mod 16 of
+// the diagonal block (upper triangle from the staged rows, mirrored below) and
+// eliminates them; the pivot row and the multipliers come by shuffle.  Afterwards
+// column c holds d_k L_ck (k < c), d_c (k = c) and (L_JJ^-1)_kc (k > c).
+__device__ __forceinline__ void diag_block(float* sm, int j0, int n) {
+  const int l = threadIdx.x & 31, c = l & 15, hf = l >> 4;
+  const float* A = sm + OFF_A;
+  float v[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int k = 8 * hf + s;
+    v[s] = k <= c ? A[k * LDA + j0 + c] : A[c * LDA + j0 + k];
+  }
+  unsigned bad = 0u;
+  float minp = INFINITY;
+#pragma unroll
+  for (int t = 0; t < JB; ++t) {
+    const int th = t >> 3, ts = t & 7;
+    const float d = __shfl_sync(0xffffffffu, v[ts], t + 16 * th);
+    const float pc = __shfl_sync(0xffffffffu, v[ts], c + 16 * th);   // row t at this lane's column
+    if (j0 + t < n) {                      // the same decision in every lane
+      if (!(d > 0.f) || !isfinite(d)) bad |= isfinite(d) ? ST_BREAKDOWN : (ST_BREAKDOWN | ST_NONFINITE);
+      minp = fminf(minp, d);
+    }
+    if (threadIdx.x == 0) sm[OFF_PIV + j0 + t] = d;
+    const float inv = 1.f / d;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const float f = __shfl_sync(0xffffffffu, v[s], t + 16 * hf) * inv;   // l_kt, k = 8 hf + s
+      if (8 * hf + s > t) v[s] = c == t ? -f : fmaf(-f, pc, v[s]);
+    }
+  }
+  float* D = sm + OFF_D;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) D[(8 * hf + s) * LDD + c] = v[s];
+  if (threadIdx.x == 0) {
+    reinterpret_cast<unsigned*>(sm)[OFF_FLAG] = bad;
+    sm[OFF_FLAG + 1] = minp;
+  }
+}
+
+// Step 3: row j0 + w times L_JJ^-1 (unit diagonal), in the registers and in P;
+// the multipliers l_ij = (row j of D L^T)_i / d_j of the rows i after J into M.
+template <int J>
+__device__ __forceinline__ void transform_row(float (&E)[PR][PC], float* sm) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const float* A = sm + OFF_A;
+  const float* D = sm + OFF_D;
+  float* P = sm + OFF_P;
+  float* M = sm + OFF_M;
+  float acc[PC];
+#pragma unroll
+  for (int b = 0; b < PC; ++b) acc[b] = A[w * LDA + l + 32 * b];
+  for (int k = 0; k < w; ++k) {
+    const float lk = D[w * LDD + k];       // (L_JJ^-1)_wk
+#pragma unroll
+    for (int b = 0; b < PC; ++b) acc[b] = fmaf(lk, A[k * LDA + l + 32 * b], acc[b]);
+  }
+  const float invd = 1.f / sm[OFF_PIV + J * JB + w];
+  const int cc = l & 15;
+  const bool inb = in_block<J>(l);
+#pragma unroll
+  for (int b = 0; b < PC; ++b) {
+    float e = acc[b], pv = acc[b];
+    if (b == J / 2 && inb) {
+      e = D[w * LDD + cc];
+      // the L^-1 columns of J as the later rows see them: unit diagonal, zero above
+      pv = cc < w ? e : (cc == w ? 1.f : 0.f);
+    }
+    E[J][b] = e;
+    P[w * RMAX + l + 32 * b] = pv;
+    if (b > J / 2 || (b == J / 2 && (J & 1) == 0 && l >= 16))
+      M[w * RMAX + cc * 12 + 2 * b + (l >> 4)] = acc[b] * invd;
+  }
+}
+
+// Step 4 for the row groups a = J + 1 .. AMAX - 1 below the block (every a < AMAX
+// when FULL, else the ones below amax): zero the L^-1 columns of J, then
+// row_i -= sum_k l_ik P_k over the column groups up to J / 2 (L^-1, and the next
+// block's diagonal) and the Gram tiles that reach the diagonal or above.
+template <int J, bool FULL>
+__device__ __forceinline__ void update_rows(float (&E)[PR][PC], const float* sm, int amax) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const float* P = sm + OFF_P;
+  const float4* M4 = reinterpret_cast<const float4*>(sm + OFF_M);
+  const bool inb = in_block<J>(l);
+#pragma unroll
+  for (int a = J + 1; a < PR; ++a)
+    if (inb) E[a][J / 2] = 0.f;
+#pragma unroll 2
+  for (int k = 0; k < JB; ++k) {
+    const float4 q0 = M4[k * (RMAX / 4) + w * 3], q1 = M4[k * (RMAX / 4) + w * 3 + 1],
+                 q2 = M4[k * (RMAX / 4) + w * 3 + 2];
+    const float m[PR] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w, q2.x, q2.y, q2.z, q2.w};
+    float p[PC];
+#pragma unroll
+    for (int b = 0; b < PC; ++b) p[b] = P[k * RMAX + l + 32 * b];
+#pragma unroll
+    for (int a = J + 1; a < PR; ++a)
+      if (FULL || a < amax)
+#pragma unroll
+        for (int b = 0; b < PC; ++b)
+          if (b <= J / 2 || 2 * b + 2 > a) E[a][b] = fmaf(-m[a], p[b], E[a][b]);
+  }
+}
+
+template <int J>
+__device__ __forceinline__ unsigned block_step(float (&E)[PR][PC], float* sm, int n, int nblk, float& minp) {
+  {
+    // step 1: row j0 + w
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+#pragma unroll
+    for (int b = 0; b < PC; ++b) sm[OFF_A + w * LDA + l + 32 * b] = E[J][b];
+  }
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 0) diag_block(sm, J * JB, n);
+  __syncthreads();
+  const unsigned bad = reinterpret_cast<const unsigned*>(sm)[OFF_FLAG];
+  minp = fminf(minp, sm[OFF_FLAG + 1]);
+  if (bad) return bad;                     // the same decision in every thread
+  transform_row<J>(E, sm);
+  __syncthreads();
+  if constexpr (J + 1 < PR) {
+    // row groups from nblk on are padding: they need no update
+    if (nblk == NBLK) update_rows<J, true>(E, sm, NBLK);
+    else if (J + 1 < nblk) update_rows<J, false>(E, sm, nblk);
+  }
+  return 0u;
+}
 
 // The elimination itself, by the whole CTA: loads the upper triangle of the n x n
-// symmetric S (leading dimension ld; + shift on the diagonal) into E, eliminates,
-// and returns 0 or the status bits of a breakdown.  Afterwards E's upper triangle
-// holds row i of D L^T (E[i][i] = d_i, also in piv[i]) and its strict lower
-// triangle L^-1; *minp receives the smallest pivot.  `row` is 2 x RMAX floats of
-// shared memory, `piv` RMAX floats.
+// symmetric S (leading dimension ld; + shift on the diagonal; identity on the
+// padding up to the next multiple of 16) into E, eliminates, and returns 0 or the
+// status bits of a breakdown.  Afterwards E's upper triangle holds row i of D L^T
+// (E[i][i] = d_i, also at sm[OFF_PIV + i]) and its strict lower triangle L^-1;
+// *minp receives the smallest pivot.  sm: SMEM_BYTES of shared memory.
 __device__ __forceinline__ unsigned eliminate(float (&E)[PR][PC], const float* S, long long ld, int n, float shift,
-                                              float (*row)[RMAX], float* piv, float* minp_out) {
+                                              float* sm, float* minp_out) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
 #pragma unroll
   for (int a = 0; a < PR; ++a)
 #pragma unroll
     for (int b = 0; b < PC; ++b) {
       const int i = w + NW * a, c = l + 32 * b;
-      E[a][b] = (i < n && c < n && c >= i) ? S[(long long)i * ld + c] + (i == c ? shift : 0.f) : 0.f;
+      E[a][b] = (i < n && c < n && c >= i) ? S[(long long)i * ld + c] + (i == c ? shift : 0.f)
+                                           : (i == c && i >= n ? 1.f : 0.f);
     }
+  const int nblk = (n + JB - 1) / JB;
   unsigned bad = 0u;
   float minp = INFINITY;
-  for (int j = 0; j < n; ++j) {
-    float* buf = row[j & 1];
-    if (w == j % NW) {
-      const int a = j / NW;
-#pragma unroll
-      for (int aa = 0; aa < PR; ++aa)
-        if (aa == a)
-#pragma unroll
-          for (int b = 0; b < PC; ++b) buf[l + 32 * b] = E[aa][b];
+  for (int jb = 0; jb < nblk && !bad; ++jb) {
+    switch (jb) {
+      case 0: bad = block_step<0>(E, sm, n, nblk, minp); break;
+      case 1: bad = block_step<1>(E, sm, n, nblk, minp); break;
+      case 2: bad = block_step<2>(E, sm, n, nblk, minp); break;
+      case 3: bad = block_step<3>(E, sm, n, nblk, minp); break;
+      case 4: bad = block_step<4>(E, sm, n, nblk, minp); break;
+      case 5: bad = block_step<5>(E, sm, n, nblk, minp); break;
+      case 6: bad = block_step<6>(E, sm, n, nblk, minp); break;
+      case 7: bad = block_step<7>(E, sm, n, nblk, minp); break;
+      case 8: bad = block_step<8>(E, sm, n, nblk, minp); break;
+      case 9: bad = block_step<9>(E, sm, n, nblk, minp); break;
+      case 10: bad = block_step<10>(E, sm, n, nblk, minp); break;
+      default: bad = block_step<11>(E, sm, n, nblk, minp); break;
     }
+    // the next block's rows are staged over A and its diagonal over D only after
+    // every thread has finished reading them
     __syncthreads();
-    const float d = buf[j];
-    if (!(d > 0.f) || !isfinite(d)) {      // the same decision in every thread
-      bad = isfinite(d) ? ST_BREAKDOWN : (ST_BREAKDOWN | ST_NONFINITE);
-      break;
-    }
-    if (threadIdx.x == 0) piv[j] = d;
-    minp = fminf(minp, d);
-    const float inv = 1.f / d;
-#pragma unroll
-    for (int a = 0; a < PR; ++a) {
-      const int i = w + NW * a;
-      if (i <= j || i >= n) continue;
-      const float f = buf[i] * inv;        // l_ij = S_ji / S_jj (S_ji in row j's upper part)
-#pragma unroll
-      for (int b = 0; b < PC; ++b) {
-        const int c = l + 32 * b;
-        if (c >= n) continue;
-        if (c >= i || c < j) E[a][b] = fmaf(-f, buf[c], E[a][b]);   // S_ic, or (L^-1)_ic
-        else if (c == j) E[a][b] = -f;                               // (L^-1)_ij
-      }
-    }
   }
-  __syncthreads();
   *minp_out = minp;
   return bad;
 }
 
 __global__ void __launch_bounds__(NT, 1) k_chol_gj(const OrthJob* __restrict__ jobs, int pass,
                                                    const int* __restrict__ order) {
-  __shared__ float row[2][RMAX];     // the pivot row of the current step
-  __shared__ float piv[RMAX];        // the pivots d_j
+  extern __shared__ float4 gj_smem4[];
+  float* sm = reinterpret_cast<float*>(gj_smem4);
+  const float* piv = sm + OFF_PIV;   // the pivots d_j
   __shared__ float red[2];
   const OrthJob& o = jobs[order ? order[blockIdx.x] : blockIdx.x];
   if (*o.status & ST_FATAL) return;
@@ -121,7 +272,7 @@ __global__ void __launch_bounds__(NT, 1) k_chol_gj(const OrthJob* __restrict__ j
     const float shift =
         attempt ? 11.f * ((float)o.rows * (float)r + (float)r * (float)(r + 1)) * 5.9604645e-8f * trace : 0.f;
     float minp;
-    bad = eliminate(E, o.gsum, rp, r, shift, row, piv, &minp);
+    bad = eliminate(E, o.gsum, rp, r, shift, sm, &minp);
     const bool shifted_try = pass == 0 && attempt == 0 && (bad || minp < 1e-6f * maxd);
     if (!shifted_try) break;
   }
@@ -147,8 +298,8 @@ __global__ void __launch_bounds__(NT, 1) k_chol_gj(const OrthJob* __restrict__ j
       const float v = (c < r && k < r) ? (k < c ? E[a][b] * sc : (k == c ? sc : 0.f)) : 0.f;
       float h, lo;
       tc::split_tf32(v, h, lo);
-      o.Tt_hi[(long long)c * rp + k] = h;
-      o.Tt_lo[(long long)c * rp + k] = lo;
+      o.Tt_hi[c * rp + k] = h;             // rp <= 192: 32-bit offsets
+      o.Tt_lo[c * rp + k] = lo;
     }
   }
 }

@@ -1112,7 +1112,7 @@ void orth_chol(const dion_plan* p, unsigned char* base, cudaStream_t s, int L, i
   const OrthJob* jobs = ol.jobs;
   const int njob = ol.njob;
   if (!p->big_orth) {
-    gj::k_chol_gj<<<njob, gj::NT, 0, s>>>(jobs, ps, tab<int>(p, base, p->t_chol_order[L]));
+    gj::k_chol_gj<<<njob, gj::NT, gj::SMEM_BYTES, s>>>(jobs, ps, tab<int>(p, base, p->t_chol_order[L]));
     return;
   }
   const long long rmax = p->rmax_l[L];
@@ -1127,7 +1127,7 @@ void orth_chol(const dion_plan* p, unsigned char* base, cudaStream_t s, int L, i
     bchol::k_stats<<<njob, bchol::NT, 0, s>>>(jobs, ps, retry);
     bchol::k_copy<<<njob * ncopy, bchol::NT, 0, s>>>(jobs, ps, retry, ncopy);
     for (int pp = 0; pp < np; ++pp) {
-      bchol::k_diag_gj<<<njob, gj::NT, 0, s>>>(jobs, ps, retry, pp);
+      bchol::k_diag_gj<<<njob, gj::NT, gj::SMEM_BYTES, s>>>(jobs, ps, retry, pp);
       const long long trail = rmax - (long long)(pp + 1) * bchol::NB;   // columns right of the panel
       if (trail <= 0) continue;
       const int nslab = (int)cdiv(trail, bchol::SLAB);
@@ -1495,7 +1495,11 @@ dion_status_t dion_plan_upload(dion_plan* plan, void* workspace, size_t ws_bytes
         cudaFuncSetAttribute(bchol::k_panel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)bchol::PANEL_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(bchol::k_inv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)bchol::INV_SMEM) != cudaSuccess)
+                             (int)bchol::INV_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(gj::k_chol_gj, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gj::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(bchol::k_diag_gj, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gj::SMEM_BYTES) != cudaSuccess)
       return cuda_check("kernel attributes");
   }
   st = build_image(plan, base);
