@@ -170,20 +170,17 @@ __device__ __forceinline__ void update_rows(float (&E)[PR][PC], const float* sm,
   }
 }
 
+// Steps 1, 3 and 4 of block J (J a template argument, so that its register rows
+// are addressed statically); step 2 is shared by all blocks.
 template <int J>
-__device__ __forceinline__ unsigned block_step(float (&E)[PR][PC], float* sm, int n, int nblk, float& minp) {
-  {
-    // step 1: row j0 + w
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+__device__ __forceinline__ void stage_rows(const float (&E)[PR][PC], float* sm) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
 #pragma unroll
-    for (int b = 0; b < PC; ++b) sm[OFF_A + w * LDA + l + 32 * b] = E[J][b];
-  }
-  __syncthreads();
-  if ((threadIdx.x >> 5) == 0) diag_block(sm, J * JB, n);
-  __syncthreads();
-  const unsigned bad = reinterpret_cast<const unsigned*>(sm)[OFF_FLAG];
-  minp = fminf(minp, sm[OFF_FLAG + 1]);
-  if (bad) return bad;                     // the same decision in every thread
+  for (int b = 0; b < PC; ++b) sm[OFF_A + w * LDA + l + 32 * b] = E[J][b];
+}
+
+template <int J>
+__device__ __forceinline__ void transform_update(float (&E)[PR][PC], float* sm, int nblk) {
   transform_row<J>(E, sm);
   __syncthreads();
   if constexpr (J + 1 < PR) {
@@ -191,8 +188,24 @@ __device__ __forceinline__ unsigned block_step(float (&E)[PR][PC], float* sm, in
     if (nblk == NBLK) update_rows<J, true>(E, sm, NBLK);
     else if (J + 1 < nblk) update_rows<J, false>(E, sm, nblk);
   }
-  return 0u;
 }
+
+// CALL with J bound to the block index jb as a compile-time constant
+#define GJ_SWITCH(CALL)                                                 \
+  switch (jb) {                                                         \
+    case 0: { constexpr int J = 0; CALL; } break;                       \
+    case 1: { constexpr int J = 1; CALL; } break;                       \
+    case 2: { constexpr int J = 2; CALL; } break;                       \
+    case 3: { constexpr int J = 3; CALL; } break;                       \
+    case 4: { constexpr int J = 4; CALL; } break;                       \
+    case 5: { constexpr int J = 5; CALL; } break;                       \
+    case 6: { constexpr int J = 6; CALL; } break;                       \
+    case 7: { constexpr int J = 7; CALL; } break;                       \
+    case 8: { constexpr int J = 8; CALL; } break;                       \
+    case 9: { constexpr int J = 9; CALL; } break;                       \
+    case 10: { constexpr int J = 10; CALL; } break;                     \
+    default: { constexpr int J = 11; CALL; } break;                     \
+  }
 
 // The elimination itself, by the whole CTA: loads the upper triangle of the n x n
 // symmetric S (leading dimension ld; + shift on the diagonal; identity on the
@@ -214,21 +227,16 @@ __device__ __forceinline__ unsigned eliminate(float (&E)[PR][PC], const float* S
   const int nblk = (n + JB - 1) / JB;
   unsigned bad = 0u;
   float minp = INFINITY;
-  for (int jb = 0; jb < nblk && !bad; ++jb) {
-    switch (jb) {
-      case 0: bad = block_step<0>(E, sm, n, nblk, minp); break;
-      case 1: bad = block_step<1>(E, sm, n, nblk, minp); break;
-      case 2: bad = block_step<2>(E, sm, n, nblk, minp); break;
-      case 3: bad = block_step<3>(E, sm, n, nblk, minp); break;
-      case 4: bad = block_step<4>(E, sm, n, nblk, minp); break;
-      case 5: bad = block_step<5>(E, sm, n, nblk, minp); break;
-      case 6: bad = block_step<6>(E, sm, n, nblk, minp); break;
-      case 7: bad = block_step<7>(E, sm, n, nblk, minp); break;
-      case 8: bad = block_step<8>(E, sm, n, nblk, minp); break;
-      case 9: bad = block_step<9>(E, sm, n, nblk, minp); break;
-      case 10: bad = block_step<10>(E, sm, n, nblk, minp); break;
-      default: bad = block_step<11>(E, sm, n, nblk, minp); break;
-    }
+  for (int jb = 0; jb < nblk; ++jb) {
+    GJ_SWITCH(stage_rows<J>(E, sm))
+    __syncthreads();
+    // one copy of the diagonal elimination for every block (its code is the largest part)
+    if (w == 0) diag_block(sm, jb * JB, n);
+    __syncthreads();
+    bad = reinterpret_cast<const unsigned*>(sm)[OFF_FLAG];
+    minp = fminf(minp, sm[OFF_FLAG + 1]);
+    if (bad) break;                        // the same decision in every thread
+    GJ_SWITCH(transform_update<J>(E, sm, nblk))
     // the next block's rows are staged over A and its diagonal over D only after
     // every thread has finished reading them
     __syncthreads();
