@@ -16,6 +16,20 @@ constexpr unsigned ST_NONFINITE = 2u;
 constexpr unsigned ST_TIMEOUT = 4u;     // a bounded wait inside a tensor-core kernel gave up
 constexpr unsigned ST_SHIFTED = 8u;     // informational: an orth() of this matrix needed the shifted pass
 
+// Layout of the tf32 operand halves that the update kernel (tcepi) reads: the
+// shared-memory image of its K-major operand tiles, stored tile after tile, so
+// that one tile is one contiguous 8 KB bulk copy (a TMA box of 64-byte rows is
+// 128 row requests).  Tile (row / 128, k / 16) of a rows x rp matrix holds rows
+// 128 t .. 128 t + 127 and columns 16 u .. 16 u + 15 in the 64-byte swizzle (row
+// r at 64 r bytes, its 16-byte piece q at q ^ ((r / 2) mod 4)); rows are padded to
+// a multiple of 128.  Returns the float offset of element (row, k).
+constexpr int OPT_ROWS = 128, OPT_K = 16, OPT_FLOATS = OPT_ROWS * OPT_K;
+__host__ __device__ __forceinline__ long long optile_idx(long long row, long long k, long long rp) {
+  const long long t = (row / OPT_ROWS) * (rp / OPT_K) + k / OPT_K;
+  const long long r = row % OPT_ROWS, kk = k % OPT_K;
+  return t * OPT_FLOATS + r * OPT_K + ((((kk >> 2) ^ (r >> 1)) & 3) << 2) + (kk & 3);
+}
+
 // One weight matrix of the batch, with the workspace buffers of its step.
 struct MatDev {
   float* X;            // m x n, ld ldx
@@ -35,7 +49,7 @@ struct MatDev {
   float* U;            // m x rp   U = orth(P)
   float* W;            // n x rp   W = M^T U
   float* Wpart;        // ksplit x n x rp partial sums of W (when ksplit > 1)
-  float* Wh;           // n x rp   tf32 halves of W (operands of the update), zero beyond column r
+  float* Wh;           // n x rp   tf32 halves of W (operands of the update, optile layout), zero beyond column r
   float* Wl;
   int ksplit;          // split of the m-range in phase (c)
   int kchunk;          // rows of M per split

@@ -223,16 +223,22 @@ void layout(dion_plan* p) {
     p->ldt_n[i] = cdiv(p->descs[i].n, 32) * 32;
     p->ldt_m[i] = cdiv(p->descs[i].m, 32) * 32;
   }
-  // phase (c) splits the rows of M (its K) into ranges of at most 2048 (8 TMEM
-  // slices), smaller when the batch has too few items to fill the GPU
-  long long items_c = 0;
-  for (int i = 0; i < cnt; ++i) items_c += cdiv(p->descs[i].n, tcstream::BM) * p->ncb[i];
+  // phase (c) splits the rows of M (its K) into ranges when the batch has too few
+  // items to fill the GPU (then of at most 2048 rows), and otherwise only where an
+  // item would exceed a third of a CTA's share of the work (or 2048 rows, if more):
+  // a split costs the write and the reduction of its K-range partials of W
+  long long items_c = 0, work_c = 0;
+  for (int i = 0; i < cnt; ++i) {
+    items_c += cdiv(p->descs[i].n, tcstream::BM) * p->ncb[i];
+    work_c += cdiv(p->descs[i].n, tcstream::BM) * p->ncb[i] * p->descs[i].m;
+  }
   const long long want = 2LL * 148;
   const long long split = items_c >= want ? 1 : cdiv(want, items_c);
+  const long long cap = split > 1 ? 2048 : std::max<long long>(2048, cdiv(work_c / (3 * 148), 256) * 256);
   for (int i = 0; i < cnt; ++i) {
     const long long m = p->descs[i].m;
     long long ch = cdiv(cdiv(m, split), 256) * 256;
-    ch = std::min<long long>(ch, 2048);
+    ch = std::min<long long>(ch, cap);
     ch = std::min<long long>(ch, cdiv(m, 32) * 32);
     p->kchunk[i] = (int)ch;
     p->ksplit[i] = (int)cdiv(m, ch);
@@ -329,8 +335,8 @@ void layout(dion_plan* p) {
     });
   }
   prefix(p->ts_wsplit, all, [&](int i) { return cdiv(D(i).n * p->rp[i], tcsplit::ELEMS_PER_CTA); });
-  prefix(p->ts_tv, all, [&](int i) { return cdiv(D(i).n, 32) * cdiv(p->rp[i], 32); });
-  prefix(p->ts_tu, all, [&](int i) { return cdiv(D(i).m, 32) * cdiv(p->rp[i], 32); });
+  prefix(p->ts_tv, all, [&](int i) { return cdiv(D(i).n, tcsplit::TROWS) * cdiv(p->rp[i], 32); });
+  prefix(p->ts_tu, all, [&](int i) { return cdiv(D(i).m, tcsplit::TROWS) * cdiv(p->rp[i], 32); });
   {
     const std::vector<int>* lists[3] = {&all, &p->orth_idx, &p->dion_idx};
     for (int L = 0; L < 3; ++L) {
@@ -434,8 +440,9 @@ void layout(dion_plan* p) {
       p->t_ttj[L] = take(sizeof(tcsplit::TJob) * nj);
       prefix(p->ts_atj[L], *lists[L], [&](int i) {
         const long long rows = L == 0 ? D(i).m : D(i).n;
-        return cdiv(rows, 32) * cdiv(p->rp[i], 32); });
-      prefix(p->ts_ttj[L], *lists[L], [&](int i) { return cdiv(p->rp[i], 32) * cdiv(p->rp[i], 32); });
+        return cdiv(rows, tcsplit::TROWS) * cdiv(p->rp[i], 32); });
+      prefix(p->ts_ttj[L], *lists[L],
+             [&](int i) { return cdiv(p->rp[i], tcsplit::TROWS) * cdiv(p->rp[i], 32); });
       p->t_ts_atj[L] = take(4 * p->ts_atj[L].size());
       p->t_ts_ttj[L] = take(4 * p->ts_ttj[L].size());
     }
@@ -524,7 +531,8 @@ void layout(dion_plan* p) {
   p->off_Uh.resize(cnt); p->off_Ul.resize(cnt); p->off_Vh.resize(cnt); p->off_Vl.resize(cnt);
   p->off_Wh.resize(cnt); p->off_Wl.resize(cnt);
   for (int i = 0; i < cnt; ++i) {
-    const long long m = D(i).m, n = D(i).n, rp = p->rp[i];
+    // the update's operand tiles: rows padded to a multiple of 128 (optile_idx)
+    const long long m = cdiv(D(i).m, OPT_ROWS) * OPT_ROWS, n = cdiv(D(i).n, OPT_ROWS) * OPT_ROWS, rp = p->rp[i];
     p->off_Uh[i] = region(4 * (size_t)(m * rp));
     p->off_Ul[i] = region(4 * (size_t)(m * rp));
     p->off_Vh[i] = region(4 * (size_t)(n * rp));
@@ -817,13 +825,8 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     tcepi::EpiMat& e = epi[i];
     std::memset(&e, 0, sizeof e);
     bool okm = true;
-    const CUtensorMapSwizzle OSW = CU_TENSOR_MAP_SWIZZLE_64B;   // operand boxes of 16 along K
-    okm &= make_map(&e.map[tcepi::MAP_UH], F32, Uh, rp, d.m, rp * 4, tcepi::BK, tcepi::BM, OSW);
-    okm &= make_map(&e.map[tcepi::MAP_UL], F32, Ul, rp, d.m, rp * 4, tcepi::BK, tcepi::BM, OSW);
-    okm &= make_map(&e.map[tcepi::MAP_VH], F32, Vh, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, OSW);
-    okm &= make_map(&e.map[tcepi::MAP_VL], F32, Vl, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, OSW);
-    okm &= make_map(&e.map[tcepi::MAP_WH], F32, Wh, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, OSW);
-    okm &= make_map(&e.map[tcepi::MAP_WL], F32, Wl, rp, d.n, rp * 4, tcepi::BK, tcepi::BNJ, OSW);
+    // the operand halves are read as whole tiles (optile_idx layout) by bulk copies
+    e.uh = Uh; e.ul = Ul; e.vh = Vh; e.vl = Vl; e.wh = Wh; e.wl = Wl;
     if (d.g_dtype == DION_DTYPE_BF16)
       okm &= make_map(&e.map[tcepi::MAP_G], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.G, d.n, d.m, d.ld_g * 2, tcepi::SUB,
                       tcepi::BM, CU_TENSOR_MAP_SWIZZLE_32B);
@@ -849,10 +852,10 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     const long long rp = p->rp[i];
     if (p->split_list[k].second == 0)
       sj[k] = tcsplit::SplitJob{x.U, rp, reinterpret_cast<float*>(base + p->off_Uh[i]),
-                                reinterpret_cast<float*>(base + p->off_Ul[i]), rp, d.m, d.r, x.status};
+                                reinterpret_cast<float*>(base + p->off_Ul[i]), rp, d.m, d.r, x.status, 1};
     else
       sj[k] = tcsplit::SplitJob{d.V, d.r, reinterpret_cast<float*>(base + p->off_Vh[i]),
-                                reinterpret_cast<float*>(base + p->off_Vl[i]), rp, d.n, d.r, x.status};
+                                reinterpret_cast<float*>(base + p->off_Vl[i]), rp, d.n, d.r, x.status, 1};
   }
   // ---- tensor-core phases (a) and (c)
   std::vector<tcstream::SJob> sa(cnt), sc(cnt);
@@ -1012,7 +1015,7 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     for (size_t k = 0; k < p->dion_idx.size(); ++k) {
       const int i = p->dion_idx[k];
       vc[k] = tcsplit::SplitJob{mats[i].V, p->descs[i].r, const_cast<float*>(mats[i].Vin), nullptr, p->rp[i],
-                                p->descs[i].n, p->descs[i].r, mats[i].status};
+                                p->descs[i].n, p->descs[i].r, mats[i].status, 0};
     }
     put(p->image, p->t_vcopy, vc.data(), vc.size());
     put(p->image, p->t_ts_vcopy, p->ts_vcopy.data(), p->ts_vcopy.size());
@@ -1040,7 +1043,7 @@ dion_status_t build_image(dion_plan* p, unsigned char* base) {
     std::vector<tcsplit::SplitJob> ws(cnt);
     for (int i = 0; i < cnt; ++i)
       ws[i] = tcsplit::SplitJob{mats[i].W, p->rp[i], mats[i].Wh, mats[i].Wl, p->rp[i], p->descs[i].n,
-                                p->descs[i].r, mats[i].status};
+                                p->descs[i].r, mats[i].status, 1};
     put(p->image, p->t_wsplit, ws.data(), ws.size());
     put(p->image, p->t_ts_wsplit, p->ts_wsplit.data(), p->ts_wsplit.size());
   }

@@ -138,9 +138,9 @@ __global__ void __launch_bounds__(NT) k_gram(const OrthJob* __restrict__ jobs,
 constexpr int CHOL_NT = 512;
 constexpr int CHOL_SMEM_MAX = 200 * 1024;
 
-// Sum of the Gram partials of every job, in a fixed order, into gsum
-// (gsum = sum_c gpart[c]); one thread per Gram element over the whole GPU,
-// four partials in flight per thread.
+// Sum of the Gram partials of every job, in a fixed order, into gsum (gsum =
+// sum_c gpart[c], on the upper triangle's 16-column blocks); one thread per Gram
+// element over the whole GPU, four partials in flight per thread.
 constexpr int GRED_ELEMS = 1024;
 __global__ void __launch_bounds__(256) k_gram_reduce(const OrthJob* __restrict__ jobs,
                                                      const int* __restrict__ tstart, int njob, int pass) {
@@ -152,6 +152,10 @@ __global__ void __launch_bounds__(256) k_gram_reduce(const OrthJob* __restrict__
   for (int e = threadIdx.x; e < GRED_ELEMS; e += blockDim.x) {
     const long long idx = (long long)(blockIdx.x - tstart[j]) * GRED_ELEMS + e;
     if (idx >= rp2) break;
+    // the partials hold, and the consumers read, the 16-column blocks of row a
+    // from the one with column a on (the upper triangle with a margin)
+    const long long ra = idx / o.rp, cb = (idx % o.rp) / 16;
+    if (cb * 16 + 15 < ra) continue;
     const float* g = o.gpart + idx;
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
     int c = 0;
@@ -438,8 +442,9 @@ __global__ void __launch_bounds__(NT) k_wreduce(const MatDev* __restrict__ mats,
     d.W[idx] = s;
     float h, l;
     tc::split_tf32(idx % d.rp < d.r ? s : 0.f, h, l);
-    d.Wh[idx] = h;
-    d.Wl[idx] = l;
+    const long long o = optile_idx(idx / d.rp, idx % d.rp, d.rp);   // the update's tile layout
+    d.Wh[o] = h;
+    d.Wl[o] = l;
   }
 }
 

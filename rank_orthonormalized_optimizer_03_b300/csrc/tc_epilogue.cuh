@@ -19,7 +19,8 @@
 //
 // One CTA per SM, persistent over 128 x 128 tiles of every m x n matrix.
 // Warp roles:
-//   0  TMA producer of the MMA operands (U hi/lo rows; [Vbar; W] hi/lo rows)
+//   0  producer of the MMA operands (U hi/lo rows; [Vbar; W] hi/lo rows): each
+//      128 x 16 operand tile is one contiguous 8 KB bulk copy (optile_idx layout)
 //   1  TMEM allocator and MMA issuer (one thread)
 //   2  TMA producer of the streamed state (G, R, X in 16-column sub-chunks)
 //   3  idle
@@ -57,10 +58,17 @@ constexpr uint32_t RX_BYTES = BM * SUB * 4;          // 8 KB
 constexpr uint32_t QREG_BYTES = 81920;
 constexpr uint32_t SMEM_BYTES = 1024 + OSTAGES * OST_BYTES + QREG_BYTES + 512;
 
-enum { MAP_UH, MAP_UL, MAP_VH, MAP_VL, MAP_WH, MAP_WL, MAP_G, MAP_R, MAP_X, NMAPS };
+enum { MAP_G, MAP_R, MAP_X, NMAPS };
+static_assert(BM == OPT_ROWS && BNJ == OPT_ROWS && BK == OPT_K, "operand tiles are whole optile tiles");
 
 struct EpiMat {
   CUtensorMap map[NMAPS];
+  const float* uh;      // tf32 halves of U, Vbar and W in the optile layout (rows padded to 128)
+  const float* ul;
+  const float* vh;
+  const float* vl;
+  const float* wh;
+  const float* wl;
   int m, n, rp, g_bf16;
   float eta_s, beta;
   unsigned* status;
@@ -133,17 +141,19 @@ k_epi(const EpiMat* __restrict__ mats, const Tile* __restrict__ tiles, int ntile
       if (skip(e) || kc0 * BK >= e.rp) continue;
       if (tl.mat == g_withhold_epi_matrix) goto prod_done;
       const int kc1 = min((e.rp + BK - 1) / BK, kc0 + KPASS / BK);
+      const int kt = e.rp / OPT_K;                          // tiles per 128 rows
+      const long long tu = (long long)(tl.i0 / OPT_ROWS) * kt, tv = (long long)(tl.j0 / OPT_ROWS) * kt;
       for (int kc = kc0; kc < kc1; ++kc) {
         if (!mbar_wait(&op_empty[s], ph ^ 1, abort_flag)) { failed_mat = tl.mat; goto prod_done; }
         mbar_arrive_expect_tx(&op_full[s], OST_BYTES);
         unsigned char* b = ost + s * OST_BYTES;
-        const int x = kc * BK;
-        tma_load_2d(b, &e.map[MAP_UH], &op_full[s], x, tl.i0);
-        tma_load_2d(b + A_BYTES, &e.map[MAP_UL], &op_full[s], x, tl.i0);
-        tma_load_2d(b + 2 * A_BYTES, &e.map[MAP_VH], &op_full[s], x, tl.j0);
-        tma_load_2d(b + 2 * A_BYTES + BH_BYTES / 2, &e.map[MAP_WH], &op_full[s], x, tl.j0);
-        tma_load_2d(b + 2 * A_BYTES + BH_BYTES, &e.map[MAP_VL], &op_full[s], x, tl.j0);
-        tma_load_2d(b + 2 * A_BYTES + BH_BYTES + BH_BYTES / 2, &e.map[MAP_WL], &op_full[s], x, tl.j0);
+        const long long ou = (tu + kc) * OPT_FLOATS, ov = (tv + kc) * OPT_FLOATS;
+        bulk_load(b, e.uh + ou, A_BYTES, &op_full[s]);
+        bulk_load(b + A_BYTES, e.ul + ou, A_BYTES, &op_full[s]);
+        bulk_load(b + 2 * A_BYTES, e.vh + ov, A_BYTES, &op_full[s]);
+        bulk_load(b + 2 * A_BYTES + BH_BYTES / 2, e.wh + ov, A_BYTES, &op_full[s]);
+        bulk_load(b + 2 * A_BYTES + BH_BYTES, e.vl + ov, A_BYTES, &op_full[s]);
+        bulk_load(b + 2 * A_BYTES + BH_BYTES + BH_BYTES / 2, e.wl + ov, A_BYTES, &op_full[s]);
         used[s] = true; last_ph[s] = ph;
         if (++s == OSTAGES) { s = 0; ph ^= 1; }
       }

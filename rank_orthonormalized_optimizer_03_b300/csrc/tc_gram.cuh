@@ -1,7 +1,8 @@
 // Gram partials of orth() on the 5th-generation tensor core: for every job and
 // every 256-row chunk of its argument A (rows x r, fp32),
 //
-//     gpart[chunk] = A[chunk rows]^T A[chunk rows]          (rp x rp, 3xTF32)
+//     gpart[chunk] = A[chunk rows]^T A[chunk rows]          (rp x rp, 3xTF32;
+//                    row a holds its 16-column blocks from the one with column a on)
 //
 // the first step of each CholeskyQR pass (orth() = thin QR with a positive
 // diagonal; junaidaliop.github.io "Orth-Dion", symbol glossary).  Both MMA
@@ -213,11 +214,15 @@ k_gram(const GJob* __restrict__ jobs, const GItem* __restrict__ items, int nitem
       if (blk < nblk) {
         const int a = blk * 128 + quarter * 32 + lane;
         float* dst = j.gpart + (long long)ch * j.rp * j.rp + (long long)a * j.rp;
-        for (int cb = 0; cb < j.rp / 16; ++cb) {
+        // the Gram is symmetric and its consumers read the upper triangle: only the
+        // 16-column blocks that reach the diagonal or above are written (the warp's
+        // first row decides which blocks it loads at all)
+        const int a0 = blk * 128 + quarter * 32;
+        for (int cb = a0 / 16; cb < j.rp / 16; ++cb) {
           float v[16];
           tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + blk * RP_MAX + cb * 16, v);
           tmem_wait_ld();
-          if (a < j.rp) {
+          if (a < j.rp && cb * 16 + 15 >= a) {
 #pragma unroll
             for (int k = 0; k < 16; k += 4)
               *reinterpret_cast<float4*>(dst + cb * 16 + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);

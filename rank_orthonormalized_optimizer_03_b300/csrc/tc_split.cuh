@@ -22,6 +22,7 @@ struct SplitJob {
   long long ldd;        // leading dimension of hi / lo (= padded columns)
   long long rows, cols; // valid region of src
   const unsigned* status;
+  int tiled;            // 1: hi / lo in the update's operand tile layout (optile_idx, ldd = rp)
 };
 
 __global__ void __launch_bounds__(NT) k_split(const SplitJob* __restrict__ jobs, const int* __restrict__ tstart,
@@ -42,14 +43,18 @@ __global__ void __launch_bounds__(NT) k_split(const SplitJob* __restrict__ jobs,
     }
     float h, l;
     tc::split_tf32(v, h, l);
-    o.hi[idx] = h;
-    o.lo[idx] = l;
+    const long long d = o.tiled ? optile_idx(row, c, o.ldd) : idx;
+    o.hi[d] = h;
+    o.lo[d] = l;
   }
 }
 
 // Transposed split: dst[c][r] = src[r][c] for r < rows, c < cols_pad (zero for
 // c >= cols), as hi / lo tf32 halves with leading dimension ldd (>= rows).
-// 32 x 32 tiles through shared memory so that reads and writes coalesce.
+// 32 x 32 tiles through shared memory so that reads and writes coalesce; a CTA
+// takes TROWS / 32 tiles down one 32-column strip (a launch of one tile per CTA
+// spent its time in CTA start-up).
+constexpr int TROWS = 128;
 struct TJob {
   const float* src;
   long long lds;
@@ -68,23 +73,26 @@ __global__ void __launch_bounds__(NT) k_tsplit(const TJob* __restrict__ jobs, co
   if (*o.status & ST_FATAL) return;
   const long long ntc = (o.cols_pad + 31) / 32;
   const long long local = blockIdx.x - tstart[j];
-  const long long r0 = (local / ntc) * 32, c0 = (local % ntc) * 32;
+  const long long c0 = (local % ntc) * 32;
   const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
+  for (long long r0 = (local / ntc) * TROWS, r1 = r0 + TROWS; r0 < r1 && r0 < o.rows; r0 += 32) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const long long r = r0 + ty + 8 * k, c = c0 + tx;
-    t[ty + 8 * k][tx] = (r < o.rows && c < o.cols) ? o.src[r * o.lds + c] : 0.f;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const long long c = c0 + ty + 8 * k, r = r0 + tx;
-    if (r < o.rows && c < o.cols_pad) {
-      float h, l;
-      tc::split_tf32(t[tx][ty + 8 * k], h, l);
-      o.hi[c * o.ldd + r] = h;
-      o.lo[c * o.ldd + r] = l;
+    for (int k = 0; k < 4; ++k) {
+      const long long r = r0 + ty + 8 * k, c = c0 + tx;
+      t[ty + 8 * k][tx] = (r < o.rows && c < o.cols) ? o.src[r * o.lds + c] : 0.f;
     }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const long long c = c0 + ty + 8 * k, r = r0 + tx;
+      if (r < o.rows && c < o.cols_pad) {
+        float h, l;
+        tc::split_tf32(t[tx][ty + 8 * k], h, l);
+        o.hi[c * o.ldd + r] = h;
+        o.lo[c * o.ldd + r] = l;
+      }
+    }
+    __syncthreads();
   }
 }
 

@@ -89,8 +89,9 @@ struct SJob {
   int rp, gmode;
   unsigned* status;
   // tf32 halves of the final result for the tensor-core kernels that read it next
-  // (null: none): row-major with leading dimension rp, and (th / tl) transposed with
-  // leading dimension ld_t; columns hcols..rp-1 are written as zero
+  // (null: none): in the update's operand tile layout (optile_idx with rp), and
+  // (th / tl) transposed with leading dimension ld_t; columns hcols..rp-1 are
+  // written as zero
   float* sh;
   float* sl;
   float* th;
@@ -115,16 +116,27 @@ __device__ __forceinline__ bool skip(const SJob& j) {
 }
 
 // Drain one finished TMEM slice (columns [col0, col0 + quarter) of this
-// thread's lane, a multiple of 8) into the register accumulator.
+// thread's lane, a multiple of 8) into the register accumulator: two batches of
+// three 8-column loads, one wait each (a wait per load cost a TMEM round trip per
+// 8 columns; the wait names the loaded registers so that no add moves above it).
 __device__ __forceinline__ void drain_add(uint32_t taddr, int quarter, float (&acc)[QMAX]) {
+  static_assert(QMAX % 24 == 0, "batches of three 8-column loads");
 #pragma unroll
-  for (int cb = 0; cb < QMAX / 8; ++cb) {
-    if (cb * 8 < quarter) {
-      float v[8];
-      tmem_ld8(taddr + cb * 8, v);
-      tmem_wait_ld();
+  for (int h = 0; h < QMAX / 24; ++h) {
+    if (h * 24 < quarter) {
+      float v0[8], v1[8], v2[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc[cb * 8 + k] += v[k];
+      for (int k = 0; k < 8; ++k) { v0[k] = 0.f; v1[k] = 0.f; v2[k] = 0.f; }
+      tmem_ld8(taddr + h * 24, v0);
+      if (h * 24 + 8 < quarter) tmem_ld8(taddr + h * 24 + 8, v1);
+      if (h * 24 + 16 < quarter) tmem_ld8(taddr + h * 24 + 16, v2);
+      tmem_wait_ld_dep(v0, v1, v2);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        acc[h * 24 + k] += v0[k];
+        acc[h * 24 + 8 + k] += v1[k];
+        acc[h * 24 + 16 + k] += v2[k];
+      }
     }
   }
 }
@@ -444,12 +456,12 @@ k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nite
 #pragma unroll
               for (int k = 0; k < 8; ++k) split_tf32(c + k < j.hcols ? acc[cb * 8 + k] : 0.f, h[k], l[k]);
               if (want_rm) {
-                float* hrow = j.sh + (long long)grow * j.rp;
-                float* lrow = j.sl + (long long)grow * j.rp;
-                *reinterpret_cast<float4*>(hrow + c) = make_float4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<float4*>(hrow + c + 4) = make_float4(h[4], h[5], h[6], h[7]);
-                *reinterpret_cast<float4*>(lrow + c) = make_float4(l[0], l[1], l[2], l[3]);
-                *reinterpret_cast<float4*>(lrow + c + 4) = make_float4(l[4], l[5], l[6], l[7]);
+                // two 16-byte pieces of the row in the update's operand tiles
+                const long long o0 = optile_idx(grow, c, j.rp), o1 = optile_idx(grow, c + 4, j.rp);
+                *reinterpret_cast<float4*>(j.sh + o0) = make_float4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<float4*>(j.sh + o1) = make_float4(h[4], h[5], h[6], h[7]);
+                *reinterpret_cast<float4*>(j.sl + o0) = make_float4(l[0], l[1], l[2], l[3]);
+                *reinterpret_cast<float4*>(j.sl + o1) = make_float4(l[4], l[5], l[6], l[7]);
               }
               if (want_tr) {
                 // transposed: the 32 lanes of a warp hold 32 consecutive rows, so each
