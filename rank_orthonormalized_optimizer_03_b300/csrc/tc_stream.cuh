@@ -145,13 +145,6 @@ template <bool TRANS>
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_stream(const SJob* __restrict__ jobs, const Item* __restrict__ items, int nitems) {
   extern __shared__ unsigned char smem_raw[];
-  // a CTA none of whose items is live (the third CholeskyQR pass of a batch with no
-  // flagged job, or failed matrices) leaves before its TMEM and barrier set-up
-  {
-    bool live = false;
-    for (int t = blockIdx.x; t < nitems && !live; t += gridDim.x) live = !skip(jobs[items[t].job]);
-    if (!live) return;
-  }
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* ost = smem;
   unsigned char* sst = smem + OSTAGES * OST_BYTES;
