@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(NT) k_inv(const OrthJob* __restrict__ jobs, in
   float* Tp = sm_inv;                                // NB x (NB + 1)
   float* Cs = sm_inv + NB * (NB + 1);                // NB x (SLAB + 1)
   float* Rs = Tp;                                    // phase 1 tiles reuse Tp's space:
-  float* Ts = Tp + 16 * NB;                          //   Rs 16 x NB (k, i), Ts 16 x SLAB (k, c)
+  float* Ts = Tp + 16 * (NB + 1);                    //   Rs 16 x (NB + 1) (k, i), Ts 16 x SLAB (k, c)
   // thread tile: rows i = ty * 8 + u (u < 8), columns c = tx * 4 + v (v < 4)
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
   float acc[8][4];
@@ -277,9 +277,12 @@ __global__ void __launch_bounds__(NT) k_inv(const OrthJob* __restrict__ jobs, in
 #pragma unroll
     for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
   for (int kt = kb; kt < ke; kt += 16) {
+    // 16 consecutive threads read 16 consecutive columns t of one row of S (a row
+    // segment, not a column walk); the padded row of Rs keeps the transposed
+    // stores off a single bank
     for (int e = threadIdx.x; e < 16 * NB; e += NT) {
-      const int kk = e / NB, i = e % NB, t = kt + kk;
-      Rs[kk * NB + i] = (t < ke && i < nb) ? o.S[(long long)(k0 + i) * rp + t] : 0.f;
+      const int kk = e % 16, i = e / 16, t = kt + kk;
+      Rs[kk * (NB + 1) + i] = (t < ke && i < nb) ? o.S[(long long)(k0 + i) * rp + t] : 0.f;
     }
     for (int e = threadIdx.x; e < 16 * SLAB; e += NT) {
       const int kk = e / SLAB, c = e % SLAB, t = kt + kk;
@@ -290,7 +293,7 @@ __global__ void __launch_bounds__(NT) k_inv(const OrthJob* __restrict__ jobs, in
     for (int kk = 0; kk < 16; ++kk) {
       float a[8], b[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) a[u] = Rs[kk * NB + ty * 8 + u];
+      for (int u = 0; u < 8; ++u) a[u] = Rs[kk * (NB + 1) + ty * 8 + u];
 #pragma unroll
       for (int v = 0; v < 4; ++v) b[v] = Ts[kk * SLAB + tx * 4 + v];
 #pragma unroll
