@@ -12,12 +12,11 @@
 //   k_update  one CTA per 64 x 64 tile of the trailing upper triangle:
 //             S_ac -= R_pa^T R_pc
 // then k_check (pivots; pass 0 may ask for the shifted repetition of shifted
-// CholeskyQR, see simt.cuh), and the off-diagonal blocks of T by block
-// diagonals d = q - p:
-//   k_inv     one CTA per 64-column slab of block (p, q):
-//             T_pq = -T_pp sum_{k=p+1..q} R_pk T_kq
+// CholeskyQR, see simt.cuh), and the off-diagonal blocks of T by recursive
+// doubling over pairs of diagonal blocks A, C (levels of NB, 2 NB, 4 NB ...):
+//   k_inv_pairs  one CTA per 64 x 64 tile: Y = R_AC T_C, then T_AC = -T_A Y
 // All arithmetic is fp32 with fp32 accumulation in a fixed order.  A job whose
-// rank ends before panel p (or diagonal d) skips that launch.
+// rank ends before panel p (or before a level's pair) skips that launch.
 #pragma once
 
 #include "chol_gj.cuh"
@@ -28,11 +27,9 @@ namespace dion {
 namespace bchol {
 
 constexpr int NB = 128;        // panel width
-constexpr int SLAB = 64;       // output column slab of k_panel and k_inv
-constexpr int NT = 256;        // threads of k_stats, k_copy, k_panel, k_inv
-// dynamic shared memory: k_inv holds T_pp (NB x NB+1) and C (NB x SLAB+1), k_panel
-// T_pp and the slab of S
-constexpr size_t INV_SMEM = sizeof(float) * (NB * (NB + 1) + NB * (SLAB + 1));
+constexpr int SLAB = 64;       // output column slab of k_panel
+constexpr int NT = 256;        // threads of k_stats, k_copy, k_panel
+// dynamic shared memory of k_panel: T_pp and the slab of S
 constexpr size_t PANEL_SMEM = sizeof(float) * (NB * (NB + 1) + NB * SLAB);
 constexpr int COPY_ELEMS = 4096;   // elements of S and of T per CTA of k_copy
 
@@ -249,81 +246,56 @@ __global__ void k_check(const OrthJob* __restrict__ jobs, int njob, int pass, in
   }
 }
 
-// Block (p, p + d) of T, one 64-column slab per CTA:
-//   C = sum_{k = p+1 .. q} R_pk T_kq  (K = the rows of panels p+1 .. q),  T_pq = -T_pp C.
-__global__ void __launch_bounds__(NT) k_inv(const OrthJob* __restrict__ jobs, int pass, int d, int nitem) {
-  extern __shared__ float sm_inv[];
-  const OrthJob& o = jobs[blockIdx.x / nitem];
-  const int it = blockIdx.x % nitem;
+
+// Off-diagonal blocks of T = Rc^-1 by recursive doubling, level `level` (block size
+// s = NB << level): for every pair of diagonal blocks A = [a, a + s) and
+// C = [a + s, min(a + 2 s, r)) with T_A and T_C complete,
+//     step 0:  Y   = R_AC T_C       (into the rows and columns of T_AC of Tt_hi, free
+//                                     until T's tf32 halves are written)
+//     step 1:  T_AC = -T_A Y
+// (the inverse of [[R_A, R_AC], [0, R_C]]).  One CTA per 64 x 64 output tile; T_C
+// upper triangular limits step 0's K to the tile's last column, T_A step 1's K to
+// the tile's first row.  log2 of the number of panels levels instead of one launch
+// per block diagonal, each over every pair of the level at once.
+__global__ void __launch_bounds__(simt::NT) k_inv_pairs(const OrthJob* __restrict__ jobs, int pass, int level,
+                                                        int step, int ntile) {
+  __shared__ float As[simt::TK * simt::LDS], Bs[simt::TK * simt::LDS];
+  const OrthJob& o = jobs[blockIdx.x / ntile];
+  int t = blockIdx.x % ntile;
   if (!live(o, pass, 0) || scr(o)->bad) return;
   const int r = (int)o.r, rp = (int)o.rp;
-  const int np = (r + NB - 1) / NB;
-  if (d >= np || it >= (np - d) * (NB / SLAB)) return;
-  const int p = it / (NB / SLAB), q = p + d;
-  const int k0 = p * NB, nb = min(NB, r - k0);
-  const int c0 = q * NB + (it % (NB / SLAB)) * SLAB;
-  if (c0 >= r) return;
-  const int nc = min(SLAB, r - c0);
-  const int kb = k0 + nb, ke = min(r, c0 + nc);     // T[t][c] = 0 for t > c
-  float* Tp = sm_inv;                                // NB x (NB + 1)
-  float* Cs = sm_inv + NB * (NB + 1);                // NB x (SLAB + 1)
-  float* Rs = Tp;                                    // phase 1 tiles reuse Tp's space:
-  float* Ts = Tp + 16 * (NB + 1);                    //   Rs 16 x (NB + 1) (k, i), Ts 16 x SLAB (k, c)
-  // thread tile: rows i = ty * 8 + u (u < 8), columns c = tx * 4 + v (v < 4)
+  const int sz = NB << level, tps = sz / simt::TM;       // tiles per side of a pair's block
+  const int m = t / (tps * tps);
+  t %= tps * tps;
+  const long long a = 2LL * sz * m, c_beg = a + sz;
+  if (c_beg >= r) return;
+  const long long c_end = a + 2LL * sz < r ? a + 2LL * sz : (long long)r;
+  const long long i0 = a + (long long)(t / tps) * simt::TM, c0 = c_beg + (long long)(t % tps) * simt::TN;
+  if (c0 >= c_end) return;
+  float* Y = o.Tt_hi;
+  float acc[4][4];
+  simt::zero(acc);
+  if (step == 0) {
+    simt::LoadRM la{o.S, rp, r, r};                     // R_AC(i, t) = S[i][t]
+    simt::LoadRM lb{o.T, rp, r, r};                     // T_C(t, c)
+    const long long ke = c0 + simt::TN < c_end ? c0 + simt::TN : c_end;   // T_C[t][c] = 0 for t > c
+    simt::tile_acc<true, true>(la, lb, i0, c0, c_beg, ke, acc, As, Bs);
+  } else {
+    simt::LoadRM la{o.T, rp, r, r};                     // T_A(i, u)
+    simt::LoadRM lb{Y, rp, r, r};                       // Y(u, c)
+    simt::tile_acc<true, true>(la, lb, i0, c0, i0, c_beg, acc, As, Bs);
+  }
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-  float acc[8][4];
+  float* dst = step == 0 ? Y : o.T;
+  const float sign = step == 0 ? 1.f : -1.f;
 #pragma unroll
-  for (int u = 0; u < 8; ++u)
-#pragma unroll
-    for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
-  for (int kt = kb; kt < ke; kt += 16) {
-    // 16 consecutive threads read 16 consecutive columns t of one row of S (a row
-    // segment, not a column walk); the padded row of Rs keeps the transposed
-    // stores off a single bank
-    for (int e = threadIdx.x; e < 16 * NB; e += NT) {
-      const int kk = e % 16, i = e / 16, t = kt + kk;
-      Rs[kk * (NB + 1) + i] = (t < ke && i < nb) ? o.S[(long long)(k0 + i) * rp + t] : 0.f;
-    }
-    for (int e = threadIdx.x; e < 16 * SLAB; e += NT) {
-      const int kk = e / SLAB, c = e % SLAB, t = kt + kk;
-      Ts[kk * SLAB + c] = (t < ke && c < nc) ? o.T[(long long)t * rp + c0 + c] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      float a[8], b[4];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) a[u] = Rs[kk * (NB + 1) + ty * 8 + u];
-#pragma unroll
-      for (int v = 0; v < 4; ++v) b[v] = Ts[kk * SLAB + tx * 4 + v];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(a[u], b[v], acc[u][v]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int u = 0; u < 8; ++u)
-#pragma unroll
-    for (int v = 0; v < 4; ++v) Cs[(ty * 8 + u) * (SLAB + 1) + tx * 4 + v] = acc[u][v];
-  for (int e = threadIdx.x; e < nb * nb; e += NT) {
-    const int i = e / nb, u = e % nb;
-    Tp[i * (NB + 1) + u] = o.T[(long long)(k0 + i) * rp + k0 + u];
-  }
-  __syncthreads();
-  // T_pq[i][c] = -sum_{u >= i} T_pp[i][u] C[u][c]
-#pragma unroll
-  for (int u8 = 0; u8 < 8; ++u8) {
-    const int i = ty * 8 + u8;
+  for (int u = 0; u < 4; ++u) {
+    const long long i = i0 + ty * 4 + u;
+    if (i >= c_beg) continue;
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-      const int c = tx * 4 + v;
-      if (i < nb && c < nc) {
-        float s = 0.f;
-        for (int u = i; u < nb; ++u) s = fmaf(Tp[i * (NB + 1) + u], Cs[u * (SLAB + 1) + c], s);
-        o.T[(long long)(k0 + i) * rp + c0 + c] = -s;
-      }
+      const long long c = c0 + tx * 4 + v;
+      if (c < c_end) dst[i * rp + c] = sign * acc[u][v];
     }
   }
 }

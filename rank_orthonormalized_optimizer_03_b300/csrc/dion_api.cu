@@ -1143,9 +1143,12 @@ void orth_chol(const dion_plan* p, unsigned char* base, cudaStream_t s, int L, i
   };
   factor(0);
   if (ps == 0) factor(1);   // the shifted repetition, for the jobs whose pivots asked for it
-  for (int d = 1; d < np; ++d) {
-    const int nitem = (np - d) * (bchol::NB / bchol::SLAB);
-    bchol::k_inv<<<njob * nitem, bchol::NT, bchol::INV_SMEM, s>>>(jobs, ps, d, nitem);
+  // off-diagonal blocks of T by recursive doubling: two launches per level
+  for (int lv = 0; ((long long)bchol::NB << lv) < rmax; ++lv) {
+    const long long sz = (long long)bchol::NB << lv, tps = sz / simt::TM;
+    const int ntile = (int)(cdiv(rmax, 2 * sz) * tps * tps);
+    for (int step = 0; step < 2; ++step)
+      bchol::k_inv_pairs<<<njob * ntile, simt::NT, 0, s>>>(jobs, ps, lv, step, ntile);
   }
   tcsplit::k_tsplit<<<p->ts_ttj[L][njob], tcsplit::NT, 0, s>>>(tab<tcsplit::TJob>(p, base, p->t_ttj[L]),
                                                                tab<int>(p, base, p->t_ts_ttj[L]), njob);
@@ -1178,7 +1181,9 @@ int orth_launches(const dion_plan* p, int L) {
   const int np = (int)cdiv(p->rmax_l[L], bchol::NB);
   int fac = 2 + 1;                                       // stats, copy, check
   for (int pp = 0; pp < np; ++pp) fac += (p->rmax_l[L] > (long long)(pp + 1) * bchol::NB) ? 3 : 1;
-  const int chol = fac + (np - 1) + 1;                   // + inverse diagonals + T^T split
+  int lv = 0;
+  while (((long long)bchol::NB << lv) < p->rmax_l[L]) ++lv;
+  const int chol = fac + 2 * lv + 1;                     // + inverse levels (two launches each) + T^T split
   return 3 * (2 + chol + 1) + 1 + fac;                   // gram + reduce, chol, apply; pass-0 split and repetition
 }
 
@@ -1497,8 +1502,6 @@ dion_status_t dion_plan_upload(dion_plan* plan, void* workspace, size_t ws_bytes
                              (int)tcgram::SMEM_BYTES) != cudaSuccess ||
         cudaFuncSetAttribute(bchol::k_panel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)bchol::PANEL_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(bchol::k_inv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)bchol::INV_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(gj::k_chol_gj, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)gj::SMEM_BYTES) != cudaSuccess ||
         cudaFuncSetAttribute(bchol::k_diag_gj, cudaFuncAttributeMaxDynamicSharedMemorySize,
