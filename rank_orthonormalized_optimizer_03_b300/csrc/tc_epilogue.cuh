@@ -54,7 +54,8 @@ constexpr uint32_t BH_BYTES = NMMA * BK * 4;         // 16 KB ([Vbar; W] 256 row
 constexpr uint32_t OST_BYTES = 2 * A_BYTES + 2 * BH_BYTES;   // 48 KB
 constexpr uint32_t RX_BYTES = BM * SUB * 4;          // 8 KB
 // Streamed-state region, cut per launch into slots of [G | R (8 KB) | X (8 KB)]:
-// 4 x 20 KB when every gradient of the launch is bf16, 3 x 24 KB with fp32 gradients.
+// three slots of 20 KB (bf16 gradients) or 24 KB (fp32).  A fourth bf16 slot fits but
+// was measured slower (its loads compete with the operand copies).
 constexpr uint32_t QREG_BYTES = 81920;
 constexpr uint32_t SMEM_BYTES = 1024 + OSTAGES * OST_BYTES + QREG_BYTES + 512;
 
