@@ -239,3 +239,20 @@ def test_large_rank_plans_pass_their_table_checks(L, shapes):
     # at least three CholeskyQR passes of (Gram, reduce, np panels, inverse, split, A T) for orth(P)
     assert L.dion_plan_launches_per_step(plan) > 3 * (4 + np_)
     L.dion_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("name, launches", [("llama3b_28L_rdiv16", 28), ("gpt160m_12L_rdiv4", 29)])
+def test_model_batch_launches_and_w_split(L, name, launches):
+    """Launches of one Orth-Dion step of the model batches: (a) split + stream, orth(P)
+    in three CholeskyQR passes of four launches, (c) stream (+ the reduction of W's
+    K-range partials only where phase (c) splits K), orth(W), one update launch.  The
+    Llama-3B batch has items enough to fill the GPU and none above its row cap; the
+    GPT-160M batch splits the K of its 3072-row matrices, which exceed the cap of
+    2048 rows (a third of a CTA's share of its work is less than that)."""
+    from rank_orthonormalized_optimizer_03_b300 import workloads
+    wl = workloads.by_name(name)
+    descs = [fake_desc(k, m=s.m, n=s.n, r=s.r, variant=1) for k, s in enumerate(wl.mats)]
+    code, ws, plan = create(L, descs)
+    assert code == dion.DION_OK, L.dion_last_error()
+    assert L.dion_plan_launches_per_step(plan) == launches
+    L.dion_plan_destroy(plan)
