@@ -256,3 +256,21 @@ def test_model_batch_launches_and_w_split(L, name, launches):
     assert code == dion.DION_OK, L.dion_last_error()
     assert L.dion_plan_launches_per_step(plan) == launches
     L.dion_plan_destroy(plan)
+
+
+def test_work_tables_pass_their_check_for_odd_large_rank_batches(L):
+    # ranks above 192 take the blocked orth() (tiled Gram, Cholesky across the GPU,
+    # inverse by recursive doubling) and ranks above 256 several update launches;
+    # ragged m, n and r exercise the tail tiles of every one of their tables; one
+    # large rank puts the whole batch, small ranks included, on the blocked orth()
+    g = np.random.Generator(np.random.PCG64(11))
+    for trial in range(24):
+        shapes = []
+        for j in range(int(g.integers(1, 5))):
+            m = int(g.integers(193, 9000))
+            n = int(g.integers(25, 1100)) * 8
+            r = int(g.integers(193 if j == 0 else 1, min(m, n, 2048) + 1))
+            shapes.append((m, n, r, int(g.integers(0, 2)), int(g.integers(0, 2))))
+        code, ws, msg = plan_of(L, shapes)
+        assert code == dion.DION_OK, (shapes, msg)
+        assert ws > 0
