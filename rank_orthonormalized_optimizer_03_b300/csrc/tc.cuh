@@ -101,10 +101,6 @@ __device__ __forceinline__ void fence_async_smem() {
 }
 
 // ------------------------------------------------------------------ TMA
-__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
@@ -229,37 +225,14 @@ __device__ __forceinline__ uint64_t sdesc_k_sw64(uint32_t saddr) {
   return d;
 }
 
-// Byte offset of element (row, k) of a 4-byte K-major operand tile in the 64-byte
-// swizzle layout (k in [0, 16)).
-__device__ __forceinline__ uint32_t sw64_off(uint32_t row, uint32_t k) {
-  return row * 64u + ((((k >> 2) ^ (row >> 1)) & 3u) << 4) + ((k & 3u) << 2);
-}
-
 // Byte offset of element (row, k) of a 4-byte K-major operand tile in the
 // 128-byte swizzle layout (k in [0, 32)).
 __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t k) {
   return row * 128u + ((((k >> 2) ^ row) & 7u) << 4) + ((k & 3u) << 2);
 }
 
-// 32 lanes x 32 columns of 32-bit values: thread t of the warp receives lane
-// (base lane + t), columns [col, col + 32).  Follow with tmem_wait_ld().
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-        "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 32 lanes x 8 columns (see tmem_ld32).
+// 32 lanes x 8 columns of 32-bit values: thread t of the warp receives lane
+// (base lane + t), columns [col, col + 8).  Follow with a tcgen05 wait::ld.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   uint32_t r[8];
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
@@ -269,7 +242,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 32 lanes x 16 columns (see tmem_ld32).
+// 32 lanes x 16 columns (as tmem_ld8).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
