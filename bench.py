@@ -107,10 +107,11 @@ def tensor_peak(peaks):
 
 
 # DRAM traffic of one k_epi launch per element of X, from the ncu capture of the
-# GPT-160M case (1.232 GB read + 0.635 GB written for 8.49e7 elements); the traffic
-# of a launch is this times the launch's elements.  Set EPI_TRAFFIC_CURRENT to
-# False when k_epi changes, until it is captured again.
-EPI_TRAFFIC_BYTES_PER_ELEM = (1232242000 + 634984704) / 84934656
+# GPT-160M case on the current kernel (three streamed-state slots: 1.2320 GB read +
+# 0.6347 GB written for 8.49e7 elements); the traffic of a launch is this times the
+# launch's elements.  Set EPI_TRAFFIC_CURRENT to False when k_epi changes, until it
+# is captured again.
+EPI_TRAFFIC_BYTES_PER_ELEM = (1231990784 + 634691328) / 84934656
 EPI_TRAFFIC_CURRENT = True
 
 
