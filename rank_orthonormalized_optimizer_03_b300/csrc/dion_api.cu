@@ -549,15 +549,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  // resolved once per process: a function-local static is initialised by exactly one
+  // thread, so host threads creating plans at the same time do not race on it
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
+      return reinterpret_cast<EncodeTiledFn>(f);
+    return nullptr;
+  }();
   return fn;
 }
 
