@@ -207,8 +207,10 @@ class Plan:
     """A batch of matrices stepped together (one grouped launch per phase).
 
     ``mats`` is a sequence of dicts with keys X, G, R, V (CUDA tensors owned by
-    the caller and updated in place) and eta, beta, variant ("orth" | "dion"),
-    optional scale (<= 0 or missing: sqrt(m/n)).  The workspace is a torch
+    the caller and updated in place) and eta, beta, variant ("orth" | "dion" |
+    "lowrank_muon"; with "lowrank_muon" R holds Muon's momentum, beta is its
+    coefficient and V must hold a fresh sketch before every step), optional
+    scale (<= 0 or missing: sqrt(m/n)).  The workspace is a torch
     uint8 tensor allocated here unless one is passed in.
     """
 
@@ -433,7 +435,11 @@ class HostFedStep:
         self._read = [None] * len(self.plans)   # per group: event after its last step
 
     def host_grad(self, i: int):
-        """The pinned host buffer (a tensor view) that matrix i's gradient is read from."""
+        """The pinned host buffer (a tensor view) that matrix i's gradient is read from.
+
+        The copies are asynchronous: rewrite it for the next step only once the
+        previous step's copy has completed (after :meth:`status`, or a
+        synchronize of the stream passed to :meth:`step`)."""
         return self._host_views[i]
 
     def h2d_bytes(self) -> int:
