@@ -45,3 +45,15 @@ def test_orth_noalloc_refuses_host_tensors():
     import torch
     with pytest.raises(ValueError, match="CUDA tensor"):
         dion.orth_noalloc(torch.zeros(128, 8), torch.zeros(128, 8))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without libdion.so there is no fallback: every entry point raises."""
+    monkeypatch.setattr(dion, "LIB_PATH", str(tmp_path / "libdion.so"))
+    monkeypatch.setattr(dion, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        dion.lib()
+    with pytest.raises(RuntimeError, match="not built"):
+        dion.Plan([cpu_mat()])
+    with pytest.raises(RuntimeError, match="not built"):
+        dion.MuonPlan([dict(X=None, G=None, B=None, eta=0.01, mu=0.9)])
