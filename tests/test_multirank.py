@@ -50,3 +50,16 @@ def test_job_throughput_counts_every_rank():
     two = bench.job_throughput_gbs(87e9, 40.0, 2)
     assert two == pytest.approx(2 * one)
     assert bench.max_over_ranks(3.5, 1, None) == 3.5
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun the reference arm (the oracle on the host cores) runs on rank 0;
+    every other rank exits 0 at once, without work or output."""
+    import subprocess
+    env = dict(os.environ, RANK="1", LOCAL_RANK="1", WORLD_SIZE="2", MASTER_ADDR="127.0.0.1",
+               MASTER_PORT=str(_free_port()))
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                          "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=300, env=env,
+                         cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    assert res.stdout.strip() == ""
