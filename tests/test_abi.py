@@ -274,3 +274,30 @@ def test_work_tables_pass_their_check_for_odd_large_rank_batches(L):
         code, ws, msg = plan_of(L, shapes)
         assert code == dion.DION_OK, (shapes, msg)
         assert ws > 0
+
+
+def test_last_error_is_per_host_thread(L):
+    """dion_last_error() keeps each host thread's own message: two threads fail plan
+    creation for different reasons at once and each reads back its own reason."""
+    import threading
+    barrier = threading.Barrier(2)
+    seen = {}
+
+    def worker(name, desc):
+        arr = (dion.MatrixDesc * 1)(desc)
+        ws, plan = ctypes.c_size_t(0), ctypes.c_void_p()
+        for _ in range(200):
+            barrier.wait()
+            code = L.dion_plan_create(arr, 1, ctypes.byref(ws), ctypes.byref(plan))
+            barrier.wait()
+            msg = L.dion_last_error().decode()
+            seen.setdefault(name, set()).add((code, msg))
+
+    t1 = threading.Thread(target=worker, args=("rank", fake_desc(0, r=40)))
+    t2 = threading.Thread(target=worker, args=("dtype", fake_desc(0, g_dtype=9)))
+    t1.start(); t2.start(); t1.join(); t2.join()
+    assert len(seen["rank"]) == 1 and len(seen["dtype"]) == 1, seen
+    (c1, m1), = seen["rank"]
+    (c2, m2), = seen["dtype"]
+    assert c1 == c2 == dion.DION_ERR_INVALID_ARG
+    assert "rank" in m1 and "dtype" in m2, (m1, m2)
