@@ -301,3 +301,40 @@ def test_last_error_is_per_host_thread(L):
     (c2, m2), = seen["dtype"]
     assert c1 == c2 == dion.DION_ERR_INVALID_ARG
     assert "rank" in m1 and "dtype" in m2, (m1, m2)
+
+
+def test_exchange_regions_of_the_sharded_step(L):
+    """dion_plan_exchange: the W region is every matrix's n x rp W back to back in plan
+    order (the buffers dion_plan_buffer reports), the Gram region every rp x rp Gram;
+    both aligned, inside the workspace and apart from each other and from P and U."""
+    shapes = [(100, 40, 40), (64, 96, 7), (300, 128, 33), (17, 24, 1)]
+    descs = [fake_desc(k, m=m, n=n, r=r) for k, (m, n, r) in enumerate(shapes)]
+    code, ws, plan = create(L, descs)
+    assert code == dion.DION_OK, L.dion_last_error()
+    rp = [-(-r // 32) * 32 for _, _, r in shapes]
+    off, nb = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.dion_plan_exchange(plan, 1, ctypes.byref(off), ctypes.byref(nb)) == dion.DION_OK
+    w_off, w_bytes = off.value, nb.value
+    assert w_bytes == sum(4 * n * q for (_, n, _), q in zip(shapes, rp))
+    assert L.dion_plan_exchange(plan, 0, ctypes.byref(off), ctypes.byref(nb)) == dion.DION_OK
+    g_off, g_bytes = off.value, nb.value
+    assert g_bytes == sum(4 * q * q for q in rp)
+    for o, b in ((w_off, w_bytes), (g_off, g_bytes)):
+        assert o % 16 == 0 and o + b <= ws
+    assert w_off + w_bytes <= g_off or g_off + g_bytes <= w_off
+    bo, rows, cols, ld = ctypes.c_size_t(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    expect = w_off
+    for i, (m, n, r) in enumerate(shapes):
+        assert L.dion_plan_buffer(plan, i, dion.BUF_W, ctypes.byref(bo), ctypes.byref(rows), ctypes.byref(cols),
+                                  ctypes.byref(ld)) == dion.DION_OK
+        assert (bo.value, rows.value, cols.value, ld.value) == (expect, n, r, rp[i])
+        expect += 4 * n * rp[i]
+        for which in (dion.BUF_P, dion.BUF_U):
+            assert L.dion_plan_buffer(plan, i, which, ctypes.byref(bo), ctypes.byref(rows), ctypes.byref(cols),
+                                      ctypes.byref(ld)) == dion.DION_OK
+            lo, hi = bo.value, bo.value + 4 * m * rp[i]
+            for o, b in ((w_off, w_bytes), (g_off, g_bytes)):
+                assert hi <= o or o + b <= lo
+    assert L.dion_plan_exchange(plan, 2, ctypes.byref(off), ctypes.byref(nb)) == dion.DION_ERR_INVALID_ARG
+    assert L.dion_plan_exchange(plan, 0, None, ctypes.byref(nb)) == dion.DION_ERR_INVALID_ARG
+    L.dion_plan_destroy(plan)
