@@ -350,7 +350,7 @@ def run_cuda(args):
                                           note="same matrices, Muon momentum + cubic Newton-Schulz (cuBLAS bf16 "
                                                "GEMMs); the pages' Dion3 claim of up to 6x lower step time than "
                                                "Muon states no hardware")
-        if rank == 0 and not args.no_cpu_baseline:
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(wl, args, args.cpu_seconds)
         if plan is not None:
             plan.close()
@@ -500,11 +500,15 @@ def run_e2e(args, mats, step_bytes, device_ms, world):
     steps = max(2, min(args.steps, 10))
     stepper.step()
     stepper.status()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     t0 = time.perf_counter()
     for _ in range(steps):
         stepper.step()
         stepper.status()        # device -> host read of the step's result
-    dt = (time.perf_counter() - t0) / steps
+    # the slowest rank's time, as for the device-timed value
+    dt = max_over_ranks((time.perf_counter() - t0) / steps * 1e3, world, mats[0]["X"].device) * 1e-3
     groups = len(stepper.plans)
     stepper.close()
     del stepper
